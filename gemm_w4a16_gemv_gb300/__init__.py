@@ -1,0 +1,191 @@
+"""Python binding of the w4a16 CUDA library (include/w4a16.h).
+
+Argument marshalling only: every entry point checks tensor dtypes, shapes,
+devices and contiguity, then calls the C ABI of ``_lib/libw4a16.so`` through
+ctypes with raw device pointers and the current CUDA stream.  All arithmetic
+happens in the library's CUDA kernels; there is no fallback of any kind.  If
+the library has not been built, importing this package succeeds but every
+call raises ``RuntimeError`` (build it with ``__graft_entry__.build()``).
+
+Tensors: packed codes are ``torch.uint8``; scales and zero points
+``torch.float16``; activations and outputs ``torch.bfloat16``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "w4a16_gemv", "w4a16_gemm", "fp4_moe_gemv", "w4a16_dequant",
+    "w4a16_check_device_error", "w4a16_last_error_string", "w4a16_version",
+    "library_path", "W4A16Error", "STATUS", "FMT_INT4", "FMT_FP4",
+    "OUT_F32", "OUT_BF16",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_lib", "libw4a16.so")
+_lock = threading.Lock()
+_lib = None
+
+STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "MISALIGNED",
+          4: "CUDA", 5: "TIMEOUT", 6: "DEVICE"}
+FMT_INT4, FMT_FP4 = 0, 1
+OUT_F32, OUT_BF16 = 0, 1
+
+# Exported symbols and their ctypes signatures (mirrors include/w4a16.h).
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_INT = ctypes.c_int
+SIGNATURES = {
+    "w4a16_gemv": ([_P, _P, _P, _P, _P, _I64, _I64, _INT, _P], _INT),
+    "w4a16_gemm": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _INT, _P], _INT),
+    "fp4_moe_gemv": ([_P, _P, _P, _P, _INT, _P, _I64, _I64, _I64, _INT, _P], _INT),
+    "w4a16_dequant": ([_INT, _P, _P, _P, _P, _INT, _I64, _I64, _INT, _P], _INT),
+    "w4a16_check_device_error": ([_P], _INT),
+    "w4a16_last_error_string": ([], ctypes.c_char_p),
+    "w4a16_version": ([], _INT),
+}
+
+
+class W4A16Error(RuntimeError):
+    """A nonzero status returned by the library."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__("%s (%d): %s" % (STATUS.get(status, "?"), status, message))
+        self.status = status
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """The loaded CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(
+                    "libw4a16.so is not built (%s); run __graft_entry__.build()" % _LIB_PATH)
+            handle = ctypes.CDLL(_LIB_PATH)
+            for name, (argtypes, restype) in SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.argtypes = argtypes
+                fn.restype = restype
+            _lib = handle
+        return _lib
+
+
+def _check(status: int):
+    if status != 0:
+        msg = lib().w4a16_last_error_string().decode(errors="replace")
+        raise W4A16Error(status, msg)
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _need(t: torch.Tensor, name: str, dtype, numel=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if device is not None and t.device != device:
+        raise ValueError("%s is on %s, expected %s" % (name, t.device, device))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if numel is not None and t.numel() != numel:
+        raise ValueError("%s has %d elements, expected %d" % (name, t.numel(), numel))
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def w4a16_gemv(x, qw, s, z, y=None, group: int = 128, stream=None):
+    """y[N] = x[K] W^T with INT4 weights qw [N, K/2], s/z [N, K/group]."""
+    N = qw.shape[0]
+    K = 2 * qw.shape[-1]
+    dev = qw.device
+    px = _need(x, "x", torch.bfloat16, K, dev)
+    pq = _need(qw, "qw", torch.uint8, N * K // 2, dev)
+    ps = _need(s, "s", torch.float16, N * (K // group), dev)
+    pz = _need(z, "z", torch.float16, N * (K // group), dev)
+    if y is None:
+        y = torch.empty(N, dtype=torch.bfloat16, device=dev)
+    py = _need(y, "y", torch.bfloat16, N, dev)
+    _check(lib().w4a16_gemv(px, pq, ps, pz, py, N, K, group, _stream(stream)))
+    return y
+
+
+def w4a16_gemm(X, qw, s, z, Y=None, group: int = 128, stream=None):
+    """Y[M, N] = X[M, K] W^T with INT4 weights qw [N, K/2], s/z [N, K/group]."""
+    N = qw.shape[0]
+    K = 2 * qw.shape[-1]
+    M = X.numel() // K
+    dev = qw.device
+    pX = _need(X, "X", torch.bfloat16, M * K, dev)
+    pq = _need(qw, "qw", torch.uint8, N * K // 2, dev)
+    ps = _need(s, "s", torch.float16, N * (K // group), dev)
+    pz = _need(z, "z", torch.float16, N * (K // group), dev)
+    if Y is None:
+        Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    pY = _need(Y, "Y", torch.bfloat16, M * N, dev)
+    _check(lib().w4a16_gemm(pX, pq, ps, pz, pY, M, N, K, group, _stream(stream)))
+    return Y
+
+
+def fp4_moe_gemv(x, qw, s, expert_ids, y=None, group: int = 32, stream=None):
+    """y[topk, N]: row i = x W_{expert_ids[i]}^T, FP4 stack qw [E, N, K/2]."""
+    E, N = qw.shape[0], qw.shape[1]
+    K = 2 * qw.shape[2]
+    topk = expert_ids.numel()
+    dev = qw.device
+    px = _need(x, "x", torch.bfloat16, K, dev)
+    pq = _need(qw, "qw", torch.uint8, E * N * K // 2, dev)
+    ps = _need(s, "s", torch.float16, E * N * (K // group), dev)
+    pi = _need(expert_ids, "expert_ids", torch.int32, topk, dev)
+    if y is None:
+        y = torch.empty(topk, N, dtype=torch.bfloat16, device=dev)
+    py = _need(y, "y", torch.bfloat16, topk * N, dev)
+    _check(lib().fp4_moe_gemv(px, pq, ps, pi, topk, py, E, N, K, group, _stream(stream)))
+    return y
+
+
+def w4a16_dequant(fmt: int, qw, s, z=None, out=None, out_dtype: int = OUT_F32,
+                  group=None, stream=None):
+    """Dequantised weights [rows, K] (float32 or bfloat16) -- debug entry."""
+    K = 2 * qw.shape[-1]
+    rows = qw.numel() // (K // 2)
+    if group is None:
+        group = 128 if fmt == FMT_INT4 else 32
+    dev = qw.device
+    pq = _need(qw, "qw", torch.uint8, rows * K // 2, dev)
+    ps = _need(s, "s", torch.float16, rows * (K // group), dev)
+    pz = _need(z, "z", torch.float16, rows * (K // group), dev) if z is not None else None
+    odt = torch.float32 if out_dtype == OUT_F32 else torch.bfloat16
+    if out is None:
+        out = torch.empty(rows, K, dtype=odt, device=dev)
+    po = _need(out, "out", odt, rows * K, dev)
+    _check(lib().w4a16_dequant(fmt, pq, ps, pz, po, out_dtype, rows, K, group, _stream(stream)))
+    return out
+
+
+def w4a16_check_device_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status."""
+    return int(lib().w4a16_check_device_error(_stream(stream)))
+
+
+def w4a16_last_error_string() -> str:
+    return lib().w4a16_last_error_string().decode(errors="replace")
+
+
+def w4a16_version() -> int:
+    return int(lib().w4a16_version())

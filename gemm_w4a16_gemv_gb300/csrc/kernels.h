@@ -1,0 +1,37 @@
+// Internal launchers, one per kernel family.  Arguments are validated by the
+// C-ABI layer (api.cu) before these are called.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace w4 {
+
+struct DeviceInfo {
+    int device;
+    int num_sms;
+    int max_smem_optin;
+};
+
+cudaError_t launch_dequant(int fmt, const uint8_t *qw, const uint16_t *s,
+                           const uint16_t *z, void *out, int out_dtype,
+                           int64_t rows, int64_t K, int group,
+                           cudaStream_t st, const DeviceInfo &dev);
+
+cudaError_t launch_gemv_int4(const uint16_t *x, const uint8_t *qw,
+                             const uint16_t *s, const uint16_t *z, uint16_t *y,
+                             int64_t N, int64_t K, cudaStream_t st,
+                             unsigned int *status, const DeviceInfo &dev);
+
+cudaError_t launch_moe_fp4(const uint16_t *x, const uint8_t *qw,
+                           const uint16_t *s, const int32_t *ids, int topk,
+                           uint16_t *y, int64_t E, int64_t N, int64_t K,
+                           cudaStream_t st, unsigned int *status,
+                           const DeviceInfo &dev);
+
+cudaError_t launch_gemm_int4(const uint16_t *X, const uint8_t *qw,
+                             const uint16_t *s, const uint16_t *z, uint16_t *Y,
+                             int64_t M, int64_t N, int64_t K, cudaStream_t st,
+                             unsigned int *status, const DeviceInfo &dev);
+
+}  // namespace w4

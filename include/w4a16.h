@@ -1,0 +1,138 @@
+/*
+ * w4a16.h -- C ABI of the fused 4-bit-weight x BF16-activation kernels for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Operation (problem statement of the pages; "Lab 5: Gemma4 end-to-end
+ * inference optimisation", sections "INT4 fused GEMV" and "Final
+ * configuration"; "DeepSeek V4 Triton FP4 optimisation in practice", deep
+ * analysis item 2):
+ *
+ *     Y[m, n] = sum_k X[m, k] * W[n, k]            (Y = X * W^T)
+ *     INT4:  W[n, k] = (q[n, k] - z[n, k/g]) * s[n, k/g],  g = 128
+ *     FP4:   W[n, k] = e2m1(q[n, k]) * s[n, k/g],           g = 32
+ *
+ * with q a 4-bit code packed two per byte along K: byte n*(K/2) + k/2 holds
+ * column k in its low nibble when k is even and in its high nibble when k is
+ * odd.  s and z are IEEE binary16, X and Y bfloat16 (passed as raw 16-bit
+ * patterns in uint16_t buffers), all row-major and contiguous.  e2m1 is the
+ * OCP MX FP4 format (values 0, 0.5, 1, 1.5, 2, 3, 4, 6 and their negatives).
+ * Products accumulate in binary32; outputs are rounded to bfloat16 with
+ * round-to-nearest-even.  No dequantised weight is written to memory except
+ * by the debug entry w4a16_dequant.
+ *
+ * Conventions shared by every entry point:
+ *  - all data pointers are DEVICE pointers owned by the caller; the library
+ *    keeps no reference after the call returns and allocates no memory;
+ *  - every data pointer must be 16-byte aligned (else W4A16_ERR_MISALIGNED);
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream); calls are
+ *    asynchronous on it and never synchronise the host, so they may be
+ *    captured into a CUDA graph;
+ *  - arguments are checked on the host before anything is launched; a failed
+ *    check launches nothing and returns a nonzero w4a16_status, with a
+ *    message available from w4a16_last_error_string();
+ *  - kernels never trap: a device-side problem (an expert id out of range, a
+ *    pipeline wait that timed out) sets a sticky per-device status word that
+ *    w4a16_check_device_error() reports and clears.
+ */
+#ifndef W4A16_H
+#define W4A16_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    W4A16_OK = 0,
+    W4A16_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, bad enum  */
+    W4A16_ERR_UNSUPPORTED = 2,  /* valid but not implemented (group, K range) */
+    W4A16_ERR_MISALIGNED = 3,   /* a pointer is not 16-byte aligned           */
+    W4A16_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed       */
+    W4A16_ERR_TIMEOUT = 5,      /* a device pipeline wait gave up             */
+    W4A16_ERR_DEVICE = 6        /* a device-side data error (bad expert id)   */
+} w4a16_status;
+
+typedef enum { W4_FMT_INT4_ASYM = 0, W4_FMT_FP4_E2M1 = 1 } w4_format;
+typedef enum { W4_OUT_F32 = 0, W4_OUT_BF16 = 1 } w4_out_dtype;
+
+/*
+ * Decode GEMV, M = 1 ("Lab 5", section "INT4 fused GEMV": the decode linear
+ * reads the packed INT4 weight once, unpacks it in registers, applies the
+ * per-group scale and zero and dots it with the activation vector).
+ *   x  : bfloat16 [K]          activation
+ *   qw : uint8    [N, K/2]     packed INT4 codes
+ *   s  : binary16 [N, K/group] scales
+ *   z  : binary16 [N, K/group] zero points
+ *   y  : bfloat16 [N]          output (overwritten)
+ * Requires group == 128, N >= 1, 128 <= K <= 16384, K % 128 == 0.
+ */
+int w4a16_gemv(const uint16_t *x, const uint8_t *qw, const uint16_t *s,
+               const uint16_t *z, uint16_t *y, int64_t N, int64_t K,
+               int group, void *stream);
+
+/*
+ * Prefill GEMM, M >= 1 ("Lab 5", sections "Triton dequant + cuBLAS" and
+ * "INT4 fused GEMV", M = 128 prefill check; here fused: weight tiles are
+ * dequantised into shared memory and fed to the tcgen05 tensor cores, so no
+ * BF16 weight matrix is written to HBM).
+ *   X : bfloat16 [M, K];  qw, s, z as for w4a16_gemv;  Y : bfloat16 [M, N].
+ * Requires group == 128, K % 128 == 0, N % 16 == 0.  Any M >= 1 is accepted
+ * (rows past M in the last tile are masked).
+ */
+int w4a16_gemm(const uint16_t *X, const uint8_t *qw, const uint16_t *s,
+               const uint16_t *z, uint16_t *Y, int64_t M, int64_t N,
+               int64_t K, int group, void *stream);
+
+/*
+ * Batched-expert FP4 GEMV for one token ("DeepSeek V4 Triton FP4
+ * optimisation in practice": six routed experts per token; stacking the
+ * experts on the host cost 20% end to end, so all experts run in one launch
+ * reading the expert weights in place).
+ *   x          : bfloat16 [K]
+ *   qw         : uint8    [E, N, K/2]     packed E2M1 codes of every expert
+ *   s          : binary16 [E, N, K/group] scales
+ *   expert_ids : int32    [topk]          DEVICE array; row i of y uses
+ *                                         expert expert_ids[i]; repeats allowed
+ *   y          : bfloat16 [topk, N]
+ * Requires group == 32, K % 64 == 0, 64 <= K <= 16384, 1 <= topk.
+ * An id outside [0, E) cannot be checked on the host: that output row is
+ * written as zeros and the device status is set (W4A16_ERR_DEVICE).
+ */
+int fp4_moe_gemv(const uint16_t *x, const uint8_t *qw, const uint16_t *s,
+                 const int32_t *expert_ids, int topk, uint16_t *y, int64_t E,
+                 int64_t N, int64_t K, int group, void *stream);
+
+/*
+ * Debug dequantisation: writes the dequantised weight matrix (the step the
+ * fused kernels keep in registers / shared memory; "Lab 5", section "Triton
+ * dequant + cuBLAS", first pass).  Bit-exact contract:
+ *   INT4: W = fl32(fl32((float)q - (float)z) * (float)s)
+ *   FP4 : W = fl32(e2m1(q) * (float)s)           (exact)
+ *   out_dtype W4_OUT_F32 writes binary32, W4_OUT_BF16 writes
+ *   round-to-nearest-even bfloat16 of that binary32 value.
+ *   qw : uint8 [rows, K/2];  s (and z for INT4) binary16 [rows, K/group];
+ *   z must be NULL for FP4;  out : [rows, K] binary32 or bfloat16.
+ * group must be 128 (INT4) or 32 (FP4); K % group == 0; rows >= 1.
+ */
+int w4a16_dequant(int fmt, const uint8_t *qw, const uint16_t *s,
+                  const uint16_t *z, void *out, int out_dtype, int64_t rows,
+                  int64_t K, int group, void *stream);
+
+/*
+ * Synchronises `stream`, then reads and clears this device's sticky status.
+ * Returns W4A16_OK, W4A16_ERR_TIMEOUT, W4A16_ERR_DEVICE or W4A16_ERR_CUDA.
+ */
+int w4a16_check_device_error(void *stream);
+
+/* Message for the last failed call on this host thread ("" if none). */
+const char *w4a16_last_error_string(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int w4a16_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H */

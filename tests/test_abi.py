@@ -1,0 +1,75 @@
+"""The C ABI library: builds for sm_103a, loads, exports every declared
+symbol, and rejects bad arguments on the host before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tests.conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def libw4():
+    from gemm_w4a16_gemv_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for fn in os.listdir(inc):
+        if fn.endswith(".h"):
+            text = open(os.path.join(inc, fn)).read()
+            names += re.findall(r"^(?:int|const char \*)\s*(\w+)\s*\(", text, re.M)
+    return names
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("w4a16_gemv", "w4a16_gemm", "fp4_moe_gemv", "w4a16_dequant",
+              "w4a16_check_device_error", "w4a16_last_error_string", "w4a16_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(libw4):
+    import gemm_w4a16_gemv_gb300 as w4
+    for n in declared_functions():
+        assert hasattr(libw4, n), n
+        assert n in w4.SIGNATURES, "binding lacks " + n
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    import gemm_w4a16_gemv_gb300 as w4
+    monkeypatch.setattr(w4, "_LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(w4, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        w4.lib()
+
+
+def _call(lib, name, *args):
+    import gemm_w4a16_gemv_gb300 as w4
+    fn = getattr(lib, name)
+    fn.argtypes, fn.restype = w4.SIGNATURES[name]
+    return fn(*args)
+
+
+def test_host_validation_codes(libw4):
+    # every case fails before any CUDA call, so it runs without a GPU
+    A = 1 << 20      # a 16-byte aligned fake address; never dereferenced
+    assert _call(libw4, "w4a16_gemv", None, A, A, A, A, 16, 256, 128, None) == 1
+    assert _call(libw4, "w4a16_gemv", A, A, A, A, A, 0, 256, 128, None) == 1
+    assert _call(libw4, "w4a16_gemv", A, A, A, A, A, 16, 256, 64, None) == 2
+    assert _call(libw4, "w4a16_gemv", A, A, A, A, A, 16, 320, 128, None) == 1
+    assert _call(libw4, "w4a16_gemv", A, A, A, A, A, 16, 32768, 128, None) == 2
+    assert _call(libw4, "w4a16_gemv", A + 8, A, A, A, A, 16, 256, 128, None) == 3
+    assert _call(libw4, "w4a16_gemm", A, A, A, A, A, 4, 24, 256, 128, None) == 2
+    assert _call(libw4, "fp4_moe_gemv", A, A, A, A, 0, A, 4, 8, 128, 32, None) == 1
+    assert _call(libw4, "fp4_moe_gemv", A, A, A, A, 2, A, 4, 8, 96, 32, None) == 1
+    assert _call(libw4, "fp4_moe_gemv", A, A, A, A + 2, 2, A, 4, 8, 128, 32, None) == 3
+    assert _call(libw4, "w4a16_dequant", 1, A, A, A, A, 0, 4, 128, 32, None) == 1
+    assert _call(libw4, "w4a16_dequant", 0, A, A, A, A, 2, 4, 128, 128, None) == 1
+    assert _call(libw4, "w4a16_dequant", 0, A, A, A, A, 0, 4, 128, 64, None) == 2
+    msg = _call(libw4, "w4a16_last_error_string").decode()
+    assert "group" in msg
