@@ -92,12 +92,11 @@ def test_gemv_rejects_bad_arguments_without_launch():
     p = synth.int4_problem(16, 256, seed=1)
     x = dev_tensor(p["x"], torch.bfloat16).view(-1)
     qw = dev_tensor(p["qw"], torch.uint8)
-    s = dev_tensor(p["s"], torch.float16)
-    z = dev_tensor(p["z"], torch.float16)
+    s64 = torch.zeros(16 * 4, dtype=torch.float16, device="cuda")
     with pytest.raises(w4.W4A16Error) as e:
-        w4.w4a16_gemv(x, qw, s, z, group=64)
+        w4.w4a16_gemv(x, qw, s64, s64, group=64)
     assert e.value.status == 2
-    big = torch.empty(16 * 16384 + 8, dtype=torch.uint8, device="cuda")
+    big = torch.empty(16 * 8192 + 8, dtype=torch.uint8, device="cuda")
     mis = big[8:].view(16, 8192)                   # 8-byte aligned only
     with pytest.raises(w4.W4A16Error) as e:
         w4.w4a16_gemv(torch.zeros(16384, dtype=torch.bfloat16, device="cuda"), mis,
