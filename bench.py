@@ -1,0 +1,492 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused INT4 dequant-GEMV on one GB300 (or N replicas).
+
+Workload (one "step"): the decode MLP GEMV pair at M = 1 -- the up projection
+N=15360, K=3840 followed by the down projection N=3840, K=15360, INT4
+asymmetric weights with FP16 scale/zero per 128 codes, BF16 activations and
+outputs (Gemma4-12B-shaped linears; synthetic seeded data).  Eight rotating
+weight sets (about 500 MB) keep every step's weights out of the 129 MB L2.
+
+Metric: whole-job HBM throughput in GB/s over the algorithmic bytes (packed
+weights + scales + zeros + activations + outputs).  Also reported: the
+roofline of the GEMV kernel, the same metric end to end through the C ABI
+with host buffers, per-configuration kernel timings, GPU clocks during the
+timed region, and the CPU oracle timed on a bounded sample.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Multi-GPU: launched under torchrun, one process per GPU; every rank runs an
+independent replica (the path needs no exchange), rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused INT4 dequant-GEMV HBM GB/s (% of peak) at M=1; TFLOPS at M=128"
+WORKLOAD = ("decode MLP GEMV pair, M=1: up N=15360 K=3840 then down N=3840 K=15360, "
+            "INT4 group-128 asymmetric, FP16 scale/zero, BF16 x and y")
+UP = (15360, 3840)
+DOWN = (3840, 15360)
+L2_SETS = 8
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def gemv_bytes(N, K, group=128):
+    """Algorithmic bytes of one M=1 GEMV: packed W + s + z + x + y."""
+    G = K // group
+    return N * K // 2 + 2 * N * G * 2 + 2 * K + 2 * N
+
+
+STEP_BYTES = gemv_bytes(*UP) + gemv_bytes(*DOWN)
+
+
+def kernel_sources_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gemm_w4a16_gemv_gb300", "csrc")
+    for name in ("gemv_kernel.cuh", "gemv_common.cuh", "common.cuh", "gemv_int4.cu"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def read_traffic(digest):
+    """DRAM bytes per launch of the GEMV kernel from the committed ncu summary,
+    or None when the summary was taken on different kernel sources."""
+    path = os.path.join(ROOT, "profiles", "gemv_int4_decode_mlp_pair.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if line.startswith("- ") and ":" in line:
+            k, v = line[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_sources_sha256_16") != digest:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch_pair_avg"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def dist_setup():
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not dist.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def dist_max(value, device=None):
+    """Max of a float over ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# --------------------------------------------------------------- CPU oracle
+
+def oracle_rows_per_second(oracle, synth, N, K, rows):
+    p = synth.int4_problem(rows, K, seed=11)
+    t0 = time.perf_counter()
+    oracle.gemv_int4(p["x"], p["qw"], p["s"], p["z"], K=K)
+    return rows / (time.perf_counter() - t0)
+
+
+def oracle_step_sample(oracle, synth, seconds):
+    """A bounded sample of one step for the CPU oracle: the same fraction of
+    the up and the down projection rows, sized to take about `seconds`.
+    Returns (callable running the sample, algorithmic bytes of the sample)."""
+    oracle_rows_per_second(oracle, synth, UP[0], UP[1], 2)  # load the library first
+    up_rps = oracle_rows_per_second(oracle, synth, UP[0], UP[1], 64)
+    dn_rps = oracle_rows_per_second(oracle, synth, DOWN[0], DOWN[1], 16)
+    # fraction f of both projections: f*UP[0]/up_rps + f*DOWN[0]/dn_rps = seconds
+    f = seconds / (UP[0] / up_rps + DOWN[0] / dn_rps)
+    f = max(min(f, 1.0), 1e-4)
+    n_up = max(2, int(UP[0] * f))
+    n_dn = max(2, int(DOWN[0] * f))
+    pu = synth.int4_problem(n_up, UP[1], seed=0)
+    pd = synth.int4_problem(n_dn, DOWN[1], seed=1)
+
+    def run():
+        oracle.gemv_int4(pu["x"], pu["qw"], pu["s"], pu["z"], K=UP[1])
+        oracle.gemv_int4(pd["x"], pd["qw"], pd["s"], pd["z"], K=DOWN[1])
+
+    sample_bytes = (n_up * (UP[1] // 2 + 4 * (UP[1] // 128)) + 2 * UP[1] + 2 * n_up
+                    + n_dn * (DOWN[1] // 2 + 4 * (DOWN[1] // 128)) + 2 * DOWN[1] + 2 * n_dn)
+    desc = "%d of %d up rows + %d of %d down rows per step, single thread" % (n_up, UP[0], n_dn, DOWN[0])
+    return run, sample_bytes, desc
+
+
+def cpu_baseline(seconds=8.0):
+    import oracle
+    import synth
+    run, nbytes, desc = oracle_step_sample(oracle, synth, seconds / 2)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        run()
+        n += 1
+        if time.perf_counter() - t0 >= seconds / 2 and n >= 1:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(nbytes * n / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": desc + ", %d repetitions in %.1f s" % (n, dt)}
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: K timed steps, each a bounded
+    sample of the workload, on the host cores (rank 0 only)."""
+    world, rank, _ = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0
+    if rank != 0:
+        return 0
+    import oracle
+    import synth
+    per_step = max(0.05, 100.0 / max(1, args.steps + args.warmup))
+    run, nbytes, desc = oracle_step_sample(oracle, synth, per_step)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = time.perf_counter() - t0
+    value = nbytes * args.steps / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": desc},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def make_gemv_sets(torch, synth, dev, N, K, seed, nsets):
+    """Seeded host problem; `nsets` device copies of its weights (distinct
+    addresses, so rotating through them streams from HBM, not L2)."""
+    p = synth.int4_problem(N, K, seed=seed)
+    base = {"qw": torch.from_numpy(p["qw"]).to(dev),
+            "s": torch.from_numpy(p["s"]).view(torch.float16).to(dev),
+            "z": torch.from_numpy(p["z"]).view(torch.float16).to(dev)}
+    sets = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(nsets - 1)]
+    x_host = torch.from_numpy(p["x"].reshape(-1)).view(torch.bfloat16)
+    return sets, x_host
+
+
+def time_launches(torch, fn, n, stream):
+    """Average device time of n back-to-back launches (CUDA events)."""
+    for i in range(3):
+        fn(i)
+    torch.cuda.synchronize()
+    torch.cuda._sleep(int(5e7))  # queue the launches behind a short spin
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(n):
+        fn(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e-3 / n
+
+
+def per_config(torch, w4, synth, dev, stream, hbm_peak, tf_peak):
+    """Kernel-only timings of every configuration (launches back to back)."""
+    out = {}
+    for name, (N, K) in {"gemv_3840x3840": (3840, 3840), "gemv_up_15360x3840": UP,
+                         "gemv_down_3840x15360": DOWN, "gemv_vocab_262144x3840": (262144, 3840)}.items():
+        nsets = max(1, min(L2_SETS, int(4e8 // gemv_bytes(N, K)) + 1))
+        sets, xh = make_gemv_sets(torch, synth, dev, N, K, seed=0, nsets=nsets)
+        x = xh.to(dev)
+        y = torch.empty(N, dtype=torch.bfloat16, device=dev)
+        t = time_launches(torch, lambda i: w4.w4a16_gemv(x, sets[i % nsets]["qw"], sets[i % nsets]["s"],
+                                                          sets[i % nsets]["z"], y), 40, stream)
+        gbs = gemv_bytes(N, K) / t / 1e9
+        out[name] = {"us": round(t * 1e6, 2), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm_peak, 3)}
+        del sets
+        torch.cuda.empty_cache()
+    # MoE FP4: 64 experts resident (~1 GB), 6 selected per launch
+    E, N, K, topk = 64, 4096, 7168, 6
+    m = synth.fp4_moe_problem(E, N, K, topk, seed=0)
+    qw = torch.from_numpy(m["qw"]).to(dev)
+    s = torch.from_numpy(m["s"]).view(torch.float16).to(dev)
+    x = torch.from_numpy(m["x"]).view(torch.bfloat16).to(dev)
+    ids = [torch.from_numpy(synth.sample_experts(synth.Stream(100 + i), E, topk)).to(dev) for i in range(16)]
+    y = torch.empty(topk, N, dtype=torch.bfloat16, device=dev)
+    t = time_launches(torch, lambda i: w4.fp4_moe_gemv(x, qw, s, ids[i % 16], y), 40, stream)
+    mb = topk * (N * K // 2 + 2 * N * (K // 32)) + 2 * K + 2 * topk * N + 4 * topk
+    out["moe_fp4_64x4096x7168_top6"] = {"us": round(t * 1e6, 2), "GB/s": round(mb / t / 1e9, 1),
+                                        "frac_hbm": round(mb / t / 1e9 / hbm_peak, 3)}
+    del qw, s
+    torch.cuda.empty_cache()
+    # prefill GEMM through the tensor cores
+    for M in (128, 2048):
+        name = "gemm_m%d_15360x3840" % M
+        try:
+            N, K = 15360, 3840
+            sets, _ = make_gemv_sets(torch, synth, dev, N, K, seed=0, nsets=4)
+            X = torch.randn(M, K, device=dev).to(torch.bfloat16)
+            Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+            t = time_launches(torch, lambda i: w4.w4a16_gemm(X, sets[i % 4]["qw"], sets[i % 4]["s"],
+                                                              sets[i % 4]["z"], Y), 20, stream)
+            tf = 2.0 * M * N * K / t / 1e12
+            out[name] = {"us": round(t * 1e6, 2), "TFLOP/s": round(tf, 1), "frac_bf16": round(tf / tf_peak, 3)}
+            del sets
+        except Exception as e:  # the tensor-core GEMM may be unavailable in this build
+            out[name] = {"unavailable": str(e).splitlines()[0][:120]}
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args):
+    import torch
+    import gemm_w4a16_gemv_gb300 as w4
+    import synth
+
+    world, rank, local = dist_setup()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (use --impl reference for the CPU oracle)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    hbm_peak, tf_peak, tf_sust, peak_src = read_peaks()
+
+    up_sets, xu_h = make_gemv_sets(torch, synth, dev, *UP, seed=0, nsets=L2_SETS)
+    dn_sets, xd_h = make_gemv_sets(torch, synth, dev, *DOWN, seed=1, nsets=L2_SETS)
+    xu, xd = xu_h.to(dev), xd_h.to(dev)
+    yu = torch.empty(UP[0], dtype=torch.bfloat16, device=dev)
+    yd = torch.empty(DOWN[0], dtype=torch.bfloat16, device=dev)
+
+    def step(i, x_up=xu, x_dn=xd, y_up=yu, y_dn=yd):
+        a, b = up_sets[i % L2_SETS], dn_sets[i % L2_SETS]
+        w4.w4a16_gemv(x_up, a["qw"], a["s"], a["z"], y_up)
+        w4.w4a16_gemv(x_dn, b["qw"], b["s"], b["z"], y_dn)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if w4.w4a16_check_device_error() != 0:
+        raise SystemExit("device status set during warm-up")
+
+    # one captured graph per weight set: a step is one replay
+    graphs = None
+    if not args.no_graph:
+        try:
+            graphs = []
+            for i in range(L2_SETS):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    step(i)
+                graphs.append(g)
+            for g in graphs:
+                g.replay()
+            torch.cuda.synchronize()
+        except Exception:
+            graphs = None
+            torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    dist_barrier()
+    torch.cuda.synchronize()
+    torch.cuda._sleep(int(2e7))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        if graphs is not None:
+            graphs[i % L2_SETS].replay()
+        else:
+            step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    dist_barrier()
+    clk = clocks.stop()
+    elapsed = e0.elapsed_time(e1) * 1e-3
+    status = w4.w4a16_check_device_error()
+    elapsed_max = dist_max(elapsed, dev if torch.distributed.is_initialized() and
+                           torch.distributed.get_backend() == "nccl" else None)
+    value = STEP_BYTES * args.steps * world / elapsed_max / 1e9
+
+    # roofline of the GEMV kernel: the step is two launches of it
+    launch_s = elapsed / (2 * args.steps)
+    achieved = (STEP_BYTES / 2) / launch_s / 1e9
+    digest = kernel_sources_digest()
+    traffic = read_traffic(digest)
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
+                "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs: copy bandwidth)" if peak_src == "measured"
+                else "fallback 6.8 TB/s", "kernel": "gemv_stream_kernel<INT4>",
+                "bytes_per_launch": STEP_BYTES // 2, "launch_us": round(launch_s * 1e6, 3)}
+
+    # end to end through the C ABI with host buffers: H2D x, two GEMVs, D2H y
+    xu_pin = xu_h.clone().pin_memory()
+    xd_pin = xd_h.clone().pin_memory()
+    yu_pin = torch.empty(UP[0], dtype=torch.bfloat16).pin_memory()
+    yd_pin = torch.empty(DOWN[0], dtype=torch.bfloat16).pin_memory()
+    xu_d = torch.empty_like(xu)
+    xd_d = torch.empty_like(xd)
+    e2e_steps = min(args.steps, 300)
+
+    def e2e_step(i):
+        xu_d.copy_(xu_pin, non_blocking=True)
+        xd_d.copy_(xd_pin, non_blocking=True)
+        step(i, xu_d, xd_d, yu, yd)
+        yu_pin.copy_(yu, non_blocking=True)
+        yd_pin.copy_(yd, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for i in range(3):
+        e2e_step(i)
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        e2e_step(i)
+    e2e_dt = time.perf_counter() - t0
+    e2e_dt = dist_max(e2e_dt, dev if torch.distributed.is_initialized() and
+                      torch.distributed.get_backend() == "nccl" else None)
+    h2d = 2 * (UP[1] + DOWN[1])
+    d2h = 2 * (UP[0] + DOWN[0])
+    e2e = {"value": round(STEP_BYTES * e2e_steps * world / e2e_dt / 1e9, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+           "sync_per_step": True}
+
+    extra = {}
+    if rank == 0 and not args.no_configs:
+        extra = per_config(torch, w4, synth, dev, stream, hbm_peak, tf_peak)
+    base = None
+    if rank == 0 and not args.no_cpu:
+        try:
+            base = cpu_baseline(args.cpu_seconds)
+        except Exception as e:
+            base = {"unavailable": str(e)[:120]}
+    if rank != 0:
+        return 0
+    line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(elapsed_max / args.steps * 1e3, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "bytes_per_step": STEP_BYTES,
+                       "l2": "%d rotating weight sets of %.1f MB each (inputs larger than the 129 MB L2)"
+                             % (L2_SETS, STEP_BYTES / 1e6),
+                       "launch": "CUDA graph per step" if graphs is not None else "eager",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "roofline": roofline, "cpu_baseline": base, "e2e": e2e,
+            "gpu_launches": 2 * args.steps, "clocks": clk, "device_status": status,
+            "per_config": extra}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-graph", action="store_true", help="launch steps eagerly")
+    ap.add_argument("--no-configs", action="store_true", help="skip per-configuration timings")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    if args.steps < 1 or args.warmup < 0:
+        ap.error("--steps must be >= 1 and --warmup >= 0")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -16,8 +16,9 @@ OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "libw4a16.so")
 SOURCES = ["api.cu", "dequant.cu", "gemv_int4.cu", "moe_fp4.cu", "gemm_int4_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
-                     "-Xcompiler", "-Wall", "--expt-relaxed-constexpr"]
+                     "-Xcompiler", "-Wall", "--expt-relaxed-constexpr", "-I", INCLUDE]
 
 
 def nvcc() -> str:

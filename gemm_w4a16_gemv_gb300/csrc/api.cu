@@ -5,7 +5,7 @@
 #include <cstdio>
 #include <cstring>
 
-#include "../../include/w4a16.h"
+#include "w4a16.h"
 #include "common.cuh"
 #include "kernels.h"
 

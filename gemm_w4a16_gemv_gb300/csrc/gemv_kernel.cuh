@@ -61,7 +61,7 @@ struct GemvHeader {
     uint64_t full[kGemvMaxStages];
     uint64_t empty[kGemvMaxStages];
     StageMeta meta[kGemvMaxStages];
-    float psum[kGemvMaxStages][CW][RPT];  // per-warp row partials
+    float psum[kGemvMaxStages][2][CW][RPT];  // per-warp row partials, by phase parity
 };
 
 // Per-unit constants: INT4 bias sum, effective activation sum; scale undo.
@@ -87,21 +87,25 @@ __device__ __forceinline__ void gemv_producer(const GemvParams &a, GemvHeader<CW
     constexpr int WPT = TT / 32;  // warps per team
     const int half_k = a.K >> 1;
     const uint64_t pol = policy_evict_first();
-    auto finalize = [&](int slot) {
-        const StageMeta m = h.meta[slot];
+    // Write the outputs of a finished block.  Its metadata is copied out before
+    // the slot is reused, and its partials sit in the half of psum indexed by
+    // the block's phase parity, which the slot's next block does not touch.
+    auto finalize = [&](int slot, int par, const StageMeta m) {
         for (int r = lane; r < m.rows; r += 32) {
             const int team = r / RPT, rr = r - team * RPT;
             float acc = 0.0f;
 #pragma unroll
-            for (int w = 0; w < WPT; ++w) acc += h.psum[slot][team * WPT + w][rr];
+            for (int w = 0; w < WPT; ++w) acc += h.psum[slot][par][team * WPT + w][rr];
             a.y[m.vrow + r] = m.valid ? f32_to_bf16_bits(acc) : static_cast<uint16_t>(0);
         }
     };
     int slot = 0, phase = 0, issued = 0;
     for (int64_t v = begin; v < end; ++issued) {
-        if (issued >= a.stages) {
+        const bool recycle = issued >= a.stages;
+        StageMeta old{};
+        if (recycle) {
             if (!mbar_wait(&h.empty[slot], phase ^ 1, a.status)) return;
-            finalize(slot);
+            old = h.meta[slot];
             __syncwarp();
         }
         const int rows = gemv_block_rows(v, end, a.rows_per_slot, a.RB);
@@ -139,6 +143,8 @@ __device__ __forceinline__ void gemv_producer(const GemvParams &a, GemvHeader<CW
             }
         }
         cp_async_arrive_noinc(&h.full[slot]);
+        // the next copy is in flight; now finish the block this slot held
+        if (recycle) finalize(slot, phase ^ 1, old);
         v += rows;
         if (++slot == a.stages) {
             slot = 0;
@@ -150,7 +156,7 @@ __device__ __forceinline__ void gemv_producer(const GemvParams &a, GemvHeader<CW
     for (int it = first; it < issued; ++it) {
         const int sl = it % a.stages;
         if (!mbar_wait(&h.empty[sl], (it / a.stages) & 1, a.status)) return;
-        finalize(sl);
+        finalize(sl, (it / a.stages) & 1, h.meta[sl]);
     }
 }
 
@@ -318,7 +324,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_stream_kernel(const Gem
             }
         }
         const float red = warp_reduce_rows<RPT>(part, lane);
-        if ((lane & (32 / RPT - 1)) == 0) h.psum[slot][warp][reduced_row<RPT>(lane)] = red;
+        if ((lane & (32 / RPT - 1)) == 0) h.psum[slot][phase][warp][reduced_row<RPT>(lane)] = red;
         __syncwarp();
         if (lane == 0) mbar_arrive(&h.empty[slot]);
         v += rows;
