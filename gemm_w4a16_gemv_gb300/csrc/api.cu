@@ -105,7 +105,8 @@ int w4a16_gemm(const uint16_t *X, const uint8_t *qw, const uint16_t *s,
     if (group != 128) return fail(W4A16_ERR_UNSUPPORTED, "w4a16_gemm: group %d (only 128)", group);
     if (K % 128 != 0) return fail(W4A16_ERR_INVALID_ARG, "w4a16_gemm: K=%lld not a multiple of the group", (long long)K);
     if (N % 16 != 0) return fail(W4A16_ERR_UNSUPPORTED, "w4a16_gemm: N=%lld not a multiple of 16", (long long)N);
-    if (M > (int64_t(1) << 31) || N > (int64_t(1) << 31) || K > (int64_t(1) << 20))
+    if (K > 16384) return fail(W4A16_ERR_UNSUPPORTED, "w4a16_gemm: K=%lld > 16384", (long long)K);
+    if (M > (int64_t(1) << 30) || N > (int64_t(1) << 30) || M * N > (int64_t(1) << 40))
         return fail(W4A16_ERR_UNSUPPORTED, "w4a16_gemm: sizes too large");
     if (!aligned16(X) || !aligned16(qw) || !aligned16(s) || !aligned16(z) || !aligned16(Y))
         return fail(W4A16_ERR_MISALIGNED, "w4a16_gemm: pointers must be 16-byte aligned");
@@ -181,6 +182,8 @@ int w4a16_check_device_error(void *stream) {
     }
     if (v & w4::kDevTimeout) return fail(W4A16_ERR_TIMEOUT, "a device pipeline wait timed out");
     if (v & w4::kDevBadExpert) return fail(W4A16_ERR_DEVICE, "an expert id was outside [0, E)");
+    if (v & w4::kDevRange)
+        return fail(W4A16_ERR_DEVICE, "a w4a16_gemm activation was outside the FP16 range (|x| >= 65520)");
     return ok();
 }
 

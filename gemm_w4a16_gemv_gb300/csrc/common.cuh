@@ -13,6 +13,7 @@ namespace w4 {
 enum : unsigned int {
     kDevTimeout = 1u,    // a pipeline wait exceeded its time limit
     kDevBadExpert = 2u,  // an expert id outside [0, E)
+    kDevRange = 4u,      // a GEMM activation outside the F16 range
 };
 
 // Wait limit for every mbarrier spin, in nanoseconds of %globaltimer.

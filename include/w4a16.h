@@ -77,8 +77,8 @@ int w4a16_gemv(const uint16_t *x, const uint8_t *qw, const uint16_t *s,
  * dequantised into shared memory and fed to the tcgen05 tensor cores, so no
  * BF16 weight matrix is written to HBM).
  *   X : bfloat16 [M, K];  qw, s, z as for w4a16_gemv;  Y : bfloat16 [M, N].
- * Requires group == 128, K % 128 == 0, N % 16 == 0.  Any M >= 1 is accepted
- * (rows past M in the last tile are masked).
+ * Requires group == 128, K % 128 == 0, 128 <= K <= 16384, N % 16 == 0.  Any
+ * M >= 1 is accepted (rows past M in the last tile are masked).
  */
 int w4a16_gemm(const uint16_t *X, const uint8_t *qw, const uint16_t *s,
                const uint16_t *z, uint16_t *Y, int64_t M, int64_t N,
