@@ -8,12 +8,12 @@
 //  * warp 0 (one lane) loads the X tile (TMA, 128-byte swizzle) and the packed
 //    weight bytes of the tile (TMA, 32 B x 128 rows) into a 4-stage ring, and
 //    once per CTA the tile's scale and zero rows (one bulk copy each);
-//  * warps 4-7 prepare both operands of each block in shared memory: thread n
-//    converts row n of the BF16 X tile in place to F16, and turns its W row's
-//    64 codes into binary32 W = (q - z) * s with one FMA per code (exact for
-//    integer zero points), rounded once to F16, stored in the K-major
-//    128-byte-swizzled layout the MMA reads; then it fences the async proxy
-//    and arrives;
+//  * warps 4-11 prepare both operands of each block in shared memory: thread
+//    (n, h) takes half h of row n -- it converts half of the 16-byte chunks of
+//    X row n in place from BF16 to F16, and turns 32 codes of W row n into
+//    binary32 W = (q - z) * s with one FMA per code (exact for integer zero
+//    points), rounded once to F16 and stored in the K-major 128-byte-swizzled
+//    layout the MMA reads; then it fences the async proxy and arrives;
 //  * warp 1 (one lane) issues 4 x tcgen05.mma kind::f16 (F16 x F16 -> F32,
 //    M=128, N=128, K=16) per block into a TMEM accumulator and commits the
 //    stage back to the producer;
@@ -38,7 +38,8 @@ constexpr int BM = 128, BN = 128, BK = 64, STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB X tile (BF16 as loaded, F16 after conversion)
 constexpr int B_BYTES = BN * BK * 2;  // 16 KB F16 W tile
 constexpr int P_BYTES = BN * BK / 2;  // 4 KB packed codes
-constexpr int THREADS = 256;
+constexpr int THREADS = 384;   // 12 warps: producer, MMA, 2 idle, 8 operand warps
+constexpr int PREP_WARPS = 8;
 constexpr uint32_t TMEM_COLS = BN;    // 128 FP32 columns
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
@@ -57,7 +58,7 @@ struct GemmArgs {
 
 struct Barriers {
     uint64_t full[STAGES];    // X + packed tile landed (TMA tx bytes)
-    uint64_t bready[STAGES];  // dequantised W tile written (4 warps)
+    uint64_t bready[STAGES];  // F16 X and W tiles written (8 warps)
     uint64_t empty[STAGES];   // MMAs of the stage done (commit)
     uint64_t szfull;          // scale/zero tiles landed
     uint64_t accfull;         // accumulator complete (commit)
@@ -95,7 +96,7 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&bar.full[s], 1);
-            mbar_init(&bar.bready[s], 4);
+            mbar_init(&bar.bready[s], PREP_WARPS);
             mbar_init(&bar.empty[s], 1);
         }
         mbar_init(&bar.szfull, 1);
@@ -155,8 +156,10 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
     } else if (warp >= 4) {
-        // ------------------------------------------- dequantise, then epilogue
-        const int n = threadIdx.x - 128;  // W row of this thread / TMEM lane
+        // ------------------------------------------- operands, then epilogue
+        const int t = threadIdx.x - 128;
+        const int n = t & (BN - 1);  // W row of this thread (and TMEM lane in warps 4-7)
+        const int h = t >> 7;        // which half of the row's codes / chunks
         const bool row_ok = n < rows_n;
         bool ok = mbar_wait(&bar.szfull, 0, a.status);
         float2 c_ev = make_float2(0.f, 0.f), c_12 = c_ev, c_16 = c_ev;
@@ -181,11 +184,14 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                 c_16 = make_float2(c128, c128);
             }
             {
-                // X row n of this block: BF16 -> F16 in place (chunk order is
-                // irrelevant, each 16-byte chunk is converted where it lies)
+                // X row n of this block: BF16 -> F16 in place.  Conversion is
+                // elementwise, so each 16-byte chunk is converted where it lies;
+                // the chunk visited is rotated by the row so that the 8 lanes of
+                // a shared-memory phase touch 8 different bank groups.
                 uint4 *xr = reinterpret_cast<uint4 *>(smem + OFF_A + st * A_BYTES + (n >> 3) * 1024 + (n & 7) * 128);
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
+                for (int q = 0; q < 4; ++q) {
+                    const int c = (q + 4 * h + n) & 7;
                     uint4 v = xr[c];
                     xmax = __vmaxu2(xmax, __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
                                                    __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu)));
@@ -196,16 +202,16 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                     xr[c] = v;
                 }
             }
-            const uint4 *p = reinterpret_cast<const uint4 *>(smem + OFF_P + st * P_BYTES + n * 32);
-            const uint4 p0 = p[0], p1 = p[1];
-            const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+            const uint4 p0 = *reinterpret_cast<const uint4 *>(smem + OFF_P + st * P_BYTES + n * 32 + h * 16);
+            const uint32_t words[4] = {p0.x, p0.y, p0.z, p0.w};
             unsigned char *b_row = b_row_base + st * B_BYTES;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int jj = 0; jj < 4; ++jj) {
+                const int j = 4 * h + jj;  // 16-byte chunk (8 codes) of the row
                 // codes k = 8j .. 8j+7 of this block; code i sits at bits 4i..4i+3.
                 // Binary32 with the code at mantissa bits 12-15 (exponent of
                 // 2048) is 2048 + q; at bits 16-19 (exponent of 128) 128 + q.
-                const uint32_t w = words[j];
+                const uint32_t w = words[jj];
                 const uint32_t l12 = w << 12, l4 = w << 4, r4 = w >> 4, r12 = w >> 12;
                 const float2 v01 = make_float2(__uint_as_float((l12 & 0x0000F000u) | 0x45000000u),
                                                __uint_as_float((l12 & 0x000F0000u) | 0x43000000u));
@@ -230,7 +236,8 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         }
         // BF16 0x4780 = 65536: from there on F16 rounds to infinity
         if (max(xmax & 0xFFFFu, xmax >> 16) > 0x477Fu) atomicOr(a.status, kDevRange);
-        // epilogue: accumulator lane n = output row m0 + n
+        if (warp >= 8) return;  // warps 8-11: operands only
+        // epilogue (warps 4-7): accumulator lane n = output row m0 + n
         if (mbar_wait(&bar.accfull, 0, a.status)) {
             tc_fence_after();
             const int m = m0 + n;
