@@ -80,17 +80,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity to complete.  Returns
-// false (and records kDevTimeout) if it did not complete within the limit.
+// false (and records kDevTimeout) if it did not complete within the limit, or
+// at once if some wait of this device already timed out, so that a failing
+// launch winds down quickly instead of sitting out one limit per wait.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
                                           unsigned int *status) {
     const uint32_t a = smem_u32(bar);
+    // try_wait suspends the thread until the phase completes or a short
+    // hardware time slice ends, so polling it costs no memory traffic; the
+    // clock and the status word are consulted only between batches.
 #pragma unroll 1
-    for (int i = 0; i < 64; ++i)
+    for (int i = 0; i < 1024; ++i)
         if (mbar_try_wait(a, parity)) return true;
     const unsigned long long t0 = global_timer_ns();
 #pragma unroll 1
     while (true) {
-        if (mbar_try_wait(a, parity)) return true;
+#pragma unroll 1
+        for (int i = 0; i < 1024; ++i)
+            if (mbar_try_wait(a, parity)) return true;
+        if (status && (*reinterpret_cast<volatile unsigned int *>(status) & kDevTimeout)) return false;
         if (global_timer_ns() - t0 > kWaitLimitNs) {
             if (status) atomicOr(status, kDevTimeout);
             return false;
@@ -123,6 +131,18 @@ __device__ __forceinline__ void cp_async_4(void *dst, const void *src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)),
                  "l"(src)
                  : "memory");
+}
+
+// Sixteen-byte asynchronous copy global -> shared that bypasses L1; only the
+// first `src_bytes` (0 or 16) are read, the rest of the 16 bytes are zeros.
+__device__ __forceinline__ void cp_async_16_zfill(void *dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_group() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // Arrive on `bar` once all of this thread's earlier cp.async copies land;

@@ -2,28 +2,43 @@
 //   Y[m, n] = sum_k X[m, k] * (q[n, k] - z[n, k/128]) * s[n, k/128]
 // ("Lab 5: Gemma4 end-to-end inference optimisation": prefill (M > 1) went
 // through a Triton dequantiser writing BF16 weights and a cuBLAS GEMM; here the
-// dequantised tile never leaves shared memory, so HBM sees only packed codes).
+// weight tile never leaves shared memory, so HBM sees only packed codes).
 //
-// One CTA computes a 128 x 128 output tile, looping over K in blocks of 64:
-//  * warp 0 (one lane) loads the X tile (TMA, 128-byte swizzle) and the packed
-//    weight bytes of the tile (TMA, 32 B x 128 rows) into a 4-stage ring, and
-//    once per CTA the tile's scale and zero rows (one bulk copy each);
-//  * warps 4-11 prepare both operands of each block in shared memory: thread
-//    (n, h) takes half h of row n -- it converts half of the 16-byte chunks of
-//    X row n in place from BF16 to F16, and turns 32 codes of W row n into
-//    binary32 W = (q - z) * s with one FMA per code (exact for integer zero
-//    points), rounded once to F16 and stored in the K-major 128-byte-swizzled
-//    layout the MMA reads; then it fences the async proxy and arrives;
-//  * warp 1 (one lane) issues 4 x tcgen05.mma kind::f16 (F16 x F16 -> F32,
-//    M=128, N=128, K=16) per block into a TMEM accumulator and commits the
-//    stage back to the producer;
-//  * warps 4-7 finally read the accumulator with tcgen05.ld (each warp its
-//    32-lane quarter), round to BF16 and store Y.
-// F16 rather than BF16 operands: a BF16 weight keeps 8 significant bits, and
-// at K = 3840 its rounding alone moves outputs near zero by more than the
-// accepted 2e-2 absolute; F16 keeps 11 bits.  An activation outside the F16
-// range (|x| >= 65520) cannot be represented: it sets kDevRange.
-// Every wait is bounded; on timeout the status word is set and each role still
+// The dequantisation is split into an exact part that feeds the tensor cores
+// and an affine part applied per group to the accumulator:
+//   sum_{k in g} X[m,k] (q - z) s = s * A_g[m,n] - s * (128 + z) * S_g[m]
+//   A_g[m,n] = sum_{k in g} X[m,k] * (128 + q[n,k])     (BF16 x BF16 MMA)
+//   S_g[m]   = sum_{k in g} X[m,k]                       (same MMA: 16 rows of
+//                                                         ones below the B tile)
+// 128 + q is an integer of at most 8 significant bits, so the B operand is an
+// exact BF16 number and X enters as loaded; every product is exact and all
+// sums are binary32.
+//
+// One CTA computes a 128 x 128 output tile over K blocks of 64 (two per group):
+//  * CTAs that share an X tile (neighbours along N) form a cluster of C = 4
+//    (or 2, 1); all of them need the same 128 x 64 X tile per K block, and
+//    128 CTAs reading the same lines make a few L2 slices the bottleneck, so
+//    each CTA loads only 128 / C rows and multicasts them to the cluster;
+//  * warp 0 (one lane): one bulk copy each of the tile's scale and zero rows;
+//    per K block its X rows (TMA, 128-byte swizzle, multicast), and every
+//    four K blocks the packed weight bytes of its own tile, 128 bytes of each
+//    of the 128 rows per load (TMA, 128-byte swizzle);
+//  * warps 8-11: thread n builds row n of the B tile, 64 BF16 values 128 + q
+//    from 32 packed bytes with byte permutes, in the same swizzled layout;
+//    once per group it also writes the row's (s, -s(128 + z)) into a 4-slot
+//    table ring;
+//  * warp 1 (one lane): per K block 4 x tcgen05.mma (M=128, N=144, K=16) into
+//    the group's TMEM accumulator: columns 0-127 are A_g, column 128 is S_g
+//    (a separate N=16 MMA would cost as much as the main one: an instruction
+//    takes about as long for N=16 as for N=128);
+//    the two accumulator pairs are double-buffered across groups; an X stage
+//    is free again only when the MMAs of every CTA of the cluster are done
+//    with it, so its commits go to the stage's barrier in all of them;
+//  * warps 4-7 and 12-15: per group, read A_g and S_g with tcgen05.ld (warp w
+//    serves TMEM lanes 32 (w mod 4) .. +31 and one half of the columns),
+//    release the buffers, and accumulate y += s A_g - s (128 + z) S_g in
+//    registers; at the end round to BF16 and store Y.
+// Every wait is bounded; on timeout the status word is set, each role still
 // performs the arrivals the others wait for, and TMEM is always released.
 #include <mutex>
 
@@ -34,17 +49,27 @@
 namespace w4 {
 namespace {
 
-constexpr int BM = 128, BN = 128, BK = 64, STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;  // 16 KB X tile (BF16 as loaded, F16 after conversion)
-constexpr int B_BYTES = BN * BK * 2;  // 16 KB F16 W tile
-constexpr int P_BYTES = BN * BK / 2;  // 4 KB packed codes
-constexpr int THREADS = 384;   // 12 warps: producer, MMA, 2 idle, 8 operand warps
-constexpr int PREP_WARPS = 8;
-constexpr uint32_t TMEM_COLS = BN;    // 128 FP32 columns
-constexpr int OFF_A = 0;
-constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-constexpr int OFF_P = OFF_B + STAGES * B_BYTES;
-constexpr int OFF_SZ = OFF_P + STAGES * P_BYTES;
+constexpr int BM = 128, BN = 128, BK = 64;
+constexpr int KB_PER_W = 4;           // K blocks per packed-weight load (128 B a row)
+constexpr int MAX_XS = 6;             // X ring depth (runtime, from shared memory)
+constexpr int WS = 2;                 // packed-weight ring
+constexpr int BS = 4;                 // ring of built B tiles
+constexpr int TROWS = 16;             // rows of ones appended to each B tile
+constexpr int BNX = BN + TROWS;       // MMA N = 144
+constexpr int X_BYTES = BM * BK * 2;  // 16 KB BF16 X tile
+constexpr int B_BYTES = BNX * BK * 2; // 18 KB BF16 (128 + q) rows, then 16 rows of 1.0
+constexpr int W_BYTES = BN * 128;     // 16 KB packed codes, four K blocks
+constexpr int TSLOTS = 4;             // group-table ring
+constexpr int THREADS = 512;          // 16 warps (2-3 idle)
+constexpr int PREP_WARPS = 4;         // warps 8-11
+constexpr int EPI_WARPS = 8;          // warps 4-7, 12-15
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TM_ACC0 = 0, TM_ACC1 = 256;  // 144 columns each; column 128 is S_g
+// layout: [B ring][W ring][table][X ring][s tile][z tile][barriers]
+constexpr int OFF_B = 0;
+constexpr int OFF_W = OFF_B + BS * B_BYTES;
+constexpr int OFF_TAB = OFF_W + WS * W_BYTES;
+constexpr int OFF_X = ((OFF_TAB + TSLOTS * BN * 8) + 1023) & ~1023;
 constexpr int MAX_K = 16384;
 
 struct GemmArgs {
@@ -54,26 +79,37 @@ struct GemmArgs {
     unsigned int *status;
     int M, N, K, G;
     int sz_bytes;  // bytes of one staged scale (or zero) tile, 16-aligned
+    int xs;        // X ring depth
+    int csize;     // CTAs per cluster along N (X multicast)
+    int off_sz;    // byte offset of the scale tile
 };
 
 struct Barriers {
-    uint64_t full[STAGES];    // X + packed tile landed (TMA tx bytes)
-    uint64_t bready[STAGES];  // F16 X and W tiles written (8 warps)
-    uint64_t empty[STAGES];   // MMAs of the stage done (commit)
+    uint64_t xfull[MAX_XS];   // X tile landed (TMA tx bytes from every cluster CTA)
+    uint64_t xempty[MAX_XS];  // MMAs of every cluster CTA done with the stage
+    uint64_t wfull[WS];       // packed codes landed (TMA tx bytes)
+    uint64_t wempty[WS];      // packed codes read (prep warps)
+    uint64_t bready[BS];      // B tile written (prep warps)
+    uint64_t bempty[BS];      // MMAs reading the B tile done (commit)
+    uint64_t accfull[2];      // group accumulators complete (commit)
+    uint64_t accempty[2];     // group accumulators read (epilogue warps)
+    uint64_t tfull[TSLOTS];   // group table written (prep warps)
+    uint64_t tempty[TSLOTS];  // group table consumed (epilogue warps)
     uint64_t szfull;          // scale/zero tiles landed
-    uint64_t accfull;         // accumulator complete (commit)
-    uint64_t done;            // epilogue finished reading TMEM (4 warps)
+    uint64_t done;            // epilogue finished with TMEM
     uint32_t tmem_holder;
 };
-
-__device__ __forceinline__ uint32_t f16x2_rn(float lo, float hi) {
-    const __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t *>(&h);
-}
 
 __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// 32x32b.x1: one FP32 column of this warp's 32 TMEM lanes.
+__device__ __forceinline__ uint32_t tmem_ld_32x32b_x1(uint32_t taddr) {
+    uint32_t r;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+    return r;
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -82,26 +118,43 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     extern __shared__ unsigned char smem_raw[];
     // operand tiles need 1024-byte alignment for the 128-byte swizzle
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint16_t *s_tile = reinterpret_cast<uint16_t *>(smem + OFF_SZ);
-    uint16_t *z_tile = reinterpret_cast<uint16_t *>(smem + OFF_SZ + a.sz_bytes);
-    Barriers &bar = *reinterpret_cast<Barriers *>(smem + OFF_SZ + 2 * a.sz_bytes);
+    float2 *table = reinterpret_cast<float2 *>(smem + OFF_TAB);  // [TSLOTS][BN]
+    uint16_t *s_tile = reinterpret_cast<uint16_t *>(smem + a.off_sz);
+    uint16_t *z_tile = reinterpret_cast<uint16_t *>(smem + a.off_sz + a.sz_bytes);
+    Barriers &bar = *reinterpret_cast<Barriers *>(smem + a.off_sz + 2 * a.sz_bytes);
+    const int XS = a.xs;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * BN;
     const int m0 = blockIdx.y * BM;
     const int nkb = a.K / BK;
+    const int ngroups = a.G;
     const int rows_n = min(BN, a.N - n0);  // a multiple of 16
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&bar.full[s], 1);
-            mbar_init(&bar.bready[s], PREP_WARPS);
-            mbar_init(&bar.empty[s], 1);
+        for (int i = 0; i < XS; ++i) {
+            mbar_init(&bar.xfull[i], 1);
+            mbar_init(&bar.xempty[i], a.csize);
+        }
+        for (int i = 0; i < WS; ++i) {
+            mbar_init(&bar.wfull[i], 1);
+            mbar_init(&bar.wempty[i], PREP_WARPS);
+        }
+        for (int i = 0; i < BS; ++i) {
+            mbar_init(&bar.bready[i], PREP_WARPS);
+            mbar_init(&bar.bempty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar.accfull[i], 1);
+            mbar_init(&bar.accempty[i], EPI_WARPS);
+        }
+        for (int i = 0; i < TSLOTS; ++i) {
+            mbar_init(&bar.tfull[i], PREP_WARPS);
+            mbar_init(&bar.tempty[i], EPI_WARPS);
         }
         mbar_init(&bar.szfull, 1);
-        mbar_init(&bar.accfull, 1);
-        mbar_init(&bar.done, 4);
+        mbar_init(&bar.done, EPI_WARPS);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -111,156 +164,189 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    cluster_sync();  // every CTA's barriers exist before any multicast reaches them
     const uint32_t tmem = bar.tmem_holder;
+    const uint32_t crank = cluster_ctarank();
+    const uint16_t cmask = static_cast<uint16_t>((1u << a.csize) - 1u);
+    const int xrows = BM / a.csize;  // X rows this CTA loads for the cluster
 
     if (warp == 0) {
-        // ------------------------------------------------------ TMA producer
+        // ------------------------------------------------ packed-weight TMA
         if (lane == 0) {
-            tma_prefetch_desc(&tmX);
             tma_prefetch_desc(&tmW);
             const uint64_t pol = policy_evict_first();
             const uint32_t szb = static_cast<uint32_t>(rows_n) * a.G * 2;
             mbar_arrive_expect_tx(&bar.szfull, 2 * szb);
             bulk_g2s(s_tile, a.s + static_cast<size_t>(n0) * a.G, szb, &bar.szfull, pol);
             bulk_g2s(z_tile, a.z + static_cast<size_t>(n0) * a.G, szb, &bar.szfull, pol);
+            tma_prefetch_desc(&tmX);
             for (int kb = 0; kb < nkb; ++kb) {
-                const int st = kb % STAGES;
-                if (kb >= STAGES && !mbar_wait(&bar.empty[st], ((kb / STAGES) - 1) & 1, a.status)) break;
-                mbar_arrive_expect_tx(&bar.full[st], A_BYTES + P_BYTES);
-                tma_load_2d(smem + OFF_A + st * A_BYTES, &tmX, kb * BK, m0, &bar.full[st]);
-                tma_load_2d(smem + OFF_P + st * P_BYTES, &tmW, kb * BK / 2, n0, &bar.full[st]);
+                if (kb % KB_PER_W == 0) {
+                    const int wb = kb / KB_PER_W, ws = wb % WS;
+                    if (wb >= WS && !mbar_wait(&bar.wempty[ws], ((wb / WS) - 1) & 1, a.status)) break;
+                    mbar_arrive_expect_tx(&bar.wfull[ws], W_BYTES);
+                    tma_load_2d(smem + OFF_W + ws * W_BYTES, &tmW, wb * 128, n0, &bar.wfull[ws]);
+                }
+                const int st = kb % XS;
+                if (kb >= XS && !mbar_wait(&bar.xempty[st], ((kb / XS) - 1) & 1, a.status)) break;
+                mbar_arrive_expect_tx(&bar.xfull[st], X_BYTES);  // the whole tile, from all slices
+                unsigned char *dst = smem + OFF_X + st * X_BYTES + static_cast<int>(crank) * xrows * 128;
+                if (a.csize > 1)
+                    tma_load_2d_multicast(dst, &tmX, kb * BK, m0 + static_cast<int>(crank) * xrows, &bar.xfull[st], cmask);
+                else
+                    tma_load_2d(dst, &tmX, kb * BK, m0, &bar.xfull[st]);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_kind_f16(BM, BN, 0u);  // F16 operands
-            for (int kb = 0; kb < nkb; ++kb) {
-                const int st = kb % STAGES;
-                const uint32_t par = (kb / STAGES) & 1;
-                if (!mbar_wait(&bar.full[st], par, a.status)) break;
-                if (!mbar_wait(&bar.bready[st], par, a.status)) break;
+            constexpr uint32_t idesc_main = idesc_kind_f16(BM, BNX, 1u);  // BF16, N = 144
+            bool ok = true;
+            for (int g = 0; ok && g < ngroups; ++g) {
+                const int ab = g & 1;
+                if (g >= 2 && !mbar_wait(&bar.accempty[ab], ((g >> 1) - 1) & 1, a.status)) break;
                 tc_fence_after();
-                const uint32_t a_addr = smem_u32(smem + OFF_A + st * A_BYTES);
-                const uint32_t b_addr = smem_u32(smem + OFF_B + st * B_BYTES);
+                const uint32_t t_acc = tmem + (ab ? TM_ACC1 : TM_ACC0);
+                for (int kk = 0; kk < 2; ++kk) {
+                    const int kb = 2 * g + kk;
+                    const int st = kb % XS, bs = kb % BS;
+                    if (!mbar_wait(&bar.xfull[st], (kb / XS) & 1, a.status) ||
+                        !mbar_wait(&bar.bready[bs], (kb / BS) & 1, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(smem + OFF_X + st * X_BYTES);
+                    const uint32_t b_addr = smem_u32(smem + OFF_B + bs * B_BYTES);
 #pragma unroll
-                for (int k = 0; k < BK / 16; ++k)
-                    umma_f16(tmem, smem_desc_sw128_kmajor(a_addr + 32 * k), smem_desc_sw128_kmajor(b_addr + 32 * k),
-                              idesc, (kb | k) != 0);
-                umma_commit(&bar.empty[st]);
+                    for (int k = 0; k < BK / 16; ++k) {
+                        umma_f16(t_acc, smem_desc_sw128_kmajor(a_addr + 32 * k), smem_desc_sw128_kmajor(b_addr + 32 * k),
+                                 idesc_main, (kk | k) != 0);
+                    }
+                    if (a.csize > 1)
+                        umma_commit_multicast(&bar.xempty[st], cmask);
+                    else
+                        umma_commit(&bar.xempty[st]);
+                    umma_commit(&bar.bempty[bs]);
+                }
+                if (!ok) break;
+                umma_commit(&bar.accfull[ab]);
             }
-            umma_commit(&bar.accfull);  // after everything issued, on every path
+            // Only after a timeout: one more commit so that the epilogue's wait
+            // also ends once the MMAs already issued have completed.
+            if (!ok) umma_commit(&bar.accfull[0]);
         }
         __syncwarp();
         mbar_wait(&bar.done, 0, a.status);
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
-    } else if (warp >= 4) {
-        // ------------------------------------------- operands, then epilogue
-        const int t = threadIdx.x - 128;
-        const int n = t & (BN - 1);  // W row of this thread (and TMEM lane in warps 4-7)
-        const int h = t >> 7;        // which half of the row's codes / chunks
+    } else if (warp >= 8 && warp < 12) {
+        // -------------------------------------------------- B-tile builders
+        const int n = threadIdx.x - 256;  // W row of this thread
         const bool row_ok = n < rows_n;
+        // rows 128-143 of every B stage: BF16 1.0 (every chunk alike, swizzle moot)
+        for (int b = 0; b < BS; ++b)
+            reinterpret_cast<uint4 *>(smem + OFF_B + b * B_BYTES + BN * 128)[n] =
+                make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+        fence_proxy_async_smem();
         bool ok = mbar_wait(&bar.szfull, 0, a.status);
-        float2 c_ev = make_float2(0.f, 0.f), c_12 = c_ev, c_16 = c_ev;
-        float2 s2 = c_ev;
-        uint32_t xmax = 0;  // two packed maxima of |x| bit patterns (BF16)
         unsigned char *b_row_base = smem + OFF_B + (n >> 3) * 1024 + (n & 7) * 128;
         for (int kb = 0; ok && kb < nkb; ++kb) {
-            const int st = kb % STAGES;
-            if (!mbar_wait(&bar.full[st], (kb / STAGES) & 1, a.status)) {
-                ok = false;
-                break;
-            }
+            const int bs = kb % BS;
             if ((kb & 1) == 0) {
-                // new group: W = (128+q)*s - (128+z)*s or (2048+q)*s - (2048+z)*s
-                const int g = kb >> 1;
+                // this group's (s, -s (128 + z)) for row n into the table ring
+                const int g = kb >> 1, slot = g % TSLOTS;
+                if (g >= TSLOTS && !mbar_wait(&bar.tempty[slot], ((g / TSLOTS) - 1) & 1, a.status)) break;
                 const float sf = row_ok ? f16_bits_to_f32(s_tile[n * a.G + g]) : 0.0f;
                 const float zf = row_ok ? f16_bits_to_f32(z_tile[n * a.G + g]) : 0.0f;
-                const float c128 = -(128.0f + zf) * sf, c2048 = -(2048.0f + zf) * sf;
-                s2 = make_float2(sf, sf);
-                c_ev = make_float2(c2048, c128);  // (12-bit slot, 16-bit slot)
-                c_12 = make_float2(c2048, c2048);
-                c_16 = make_float2(c128, c128);
+                table[slot * BN + n] = make_float2(sf, -sf * (128.0f + zf));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar.tfull[slot]);
             }
-            {
-                // X row n of this block: BF16 -> F16 in place.  Conversion is
-                // elementwise, so each 16-byte chunk is converted where it lies;
-                // the chunk visited is rotated by the row so that the 8 lanes of
-                // a shared-memory phase touch 8 different bank groups.
-                uint4 *xr = reinterpret_cast<uint4 *>(smem + OFF_A + st * A_BYTES + (n >> 3) * 1024 + (n & 7) * 128);
+            const int wb = kb / KB_PER_W, kk = kb % KB_PER_W, ws = wb % WS;
+            if (kk == 0 && !mbar_wait(&bar.wfull[ws], (wb / WS) & 1, a.status)) break;
+            if (kb >= BS && !mbar_wait(&bar.bempty[bs], ((kb / BS) - 1) & 1, a.status)) break;
+            // row n of the packed stage: 16-byte chunk c sits at c ^ (n mod 8)
+            const unsigned char *wrow = smem + OFF_W + ws * W_BYTES + n * 128;
+            const uint4 p0 = *reinterpret_cast<const uint4 *>(wrow + (((2 * kk) ^ (n & 7)) << 4));
+            const uint4 p1 = *reinterpret_cast<const uint4 *>(wrow + (((2 * kk + 1) ^ (n & 7)) << 4));
+            const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+            unsigned char *b_row = b_row_base + bs * B_BYTES;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int c = (q + 4 * h + n) & 7;
-                    uint4 v = xr[c];
-                    xmax = __vmaxu2(xmax, __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
-                                                   __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu)));
-                    v.x = f16x2_rn(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u));
-                    v.y = f16x2_rn(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
-                    v.z = f16x2_rn(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u));
-                    v.w = f16x2_rn(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xFFFF0000u));
-                    xr[c] = v;
-                }
-            }
-            const uint4 p0 = *reinterpret_cast<const uint4 *>(smem + OFF_P + st * P_BYTES + n * 32 + h * 16);
-            const uint32_t words[4] = {p0.x, p0.y, p0.z, p0.w};
-            unsigned char *b_row = b_row_base + st * B_BYTES;
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                const int j = 4 * h + jj;  // 16-byte chunk (8 codes) of the row
-                // codes k = 8j .. 8j+7 of this block; code i sits at bits 4i..4i+3.
-                // Binary32 with the code at mantissa bits 12-15 (exponent of
-                // 2048) is 2048 + q; at bits 16-19 (exponent of 128) 128 + q.
-                const uint32_t w = words[jj];
-                const uint32_t l12 = w << 12, l4 = w << 4, r4 = w >> 4, r12 = w >> 12;
-                const float2 v01 = make_float2(__uint_as_float((l12 & 0x0000F000u) | 0x45000000u),
-                                               __uint_as_float((l12 & 0x000F0000u) | 0x43000000u));
-                const float2 v23 = make_float2(__uint_as_float((l4 & 0x0000F000u) | 0x45000000u),
-                                               __uint_as_float((w & 0x0000F000u) | 0x45000000u));
-                const float2 v45 = make_float2(__uint_as_float((w & 0x000F0000u) | 0x43000000u),
-                                               __uint_as_float((r4 & 0x000F0000u) | 0x43000000u));
-                const float2 v67 = make_float2(__uint_as_float((r12 & 0x0000F000u) | 0x45000000u),
-                                               __uint_as_float((r12 & 0x000F0000u) | 0x43000000u));
-                const float2 w01 = __ffma2_rn(v01, s2, c_ev);
-                const float2 w23 = __ffma2_rn(v23, s2, c_12);
-                const float2 w45 = __ffma2_rn(v45, s2, c_16);
-                const float2 w67 = __ffma2_rn(v67, s2, c_ev);
-                const uint4 out = make_uint4(f16x2_rn(w01.x, w01.y), f16x2_rn(w23.x, w23.y),
-                                             f16x2_rn(w45.x, w45.y), f16x2_rn(w67.x, w67.y));
+            for (int j = 0; j < 8; ++j) {
+                // codes 8j..8j+7 (code i at bits 4i..4i+3) -> BF16 128 + q,
+                // which is the byte q under the byte 0x43
+                const uint32_t w = words[j];
+                const uint32_t lo = w & 0x0F0F0F0Fu;         // q0 q2 q4 q6
+                const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;  // q1 q3 q5 q7
+                const uint32_t q0123 = __byte_perm(lo, hi, 0x5140);
+                const uint32_t q4567 = __byte_perm(lo, hi, 0x7362);
+                const uint4 out = make_uint4(__byte_perm(q0123, 0x43434343u, 0x4140), __byte_perm(q0123, 0x43434343u, 0x4342),
+                                             __byte_perm(q4567, 0x43434343u, 0x4140), __byte_perm(q4567, 0x43434343u, 0x4342));
                 // 16-byte chunk j of row n goes to chunk j ^ (n mod 8)
                 *reinterpret_cast<uint4 *>(b_row + ((j ^ (n & 7)) << 4)) = out;
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bar.bready[st]);
+            if (lane == 0) {
+                mbar_arrive(&bar.bready[bs]);
+                if (kk == KB_PER_W - 1 || kb == nkb - 1) mbar_arrive(&bar.wempty[ws]);
+            }
         }
-        // BF16 0x4780 = 65536: from there on F16 rounds to infinity
-        if (max(xmax & 0xFFFFu, xmax >> 16) > 0x477Fu) atomicOr(a.status, kDevRange);
-        if (warp >= 8) return;  // warps 8-11: operands only
-        // epilogue (warps 4-7): accumulator lane n = output row m0 + n
-        if (mbar_wait(&bar.accfull, 0, a.status)) {
-            tc_fence_after();
-            const int m = m0 + n;
-            const uint32_t t_lane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(t_lane + c * 32, r);
-                tmem_ld_wait();
-                if (m < a.M) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(a.Y + static_cast<size_t>(m) * a.N + n0 + c * 32);
-                    const int valid_cols = rows_n - c * 32;  // columns of the tile inside N
+    } else if (warp >= 4) {
+        // ------------------------------------------------ group epilogue
+        const int qd = warp & 3;                 // TMEM lane quarter
+        const int hc = warp >= 12 ? 1 : 0;       // column half
+        const int row = qd * 32 + lane;          // output row in the tile
+        const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
+        float y[64];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        if (q * 8 < valid_cols) {
-                            uint4 o;
-                            o.x = bf16x2_rn(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1]));
-                            o.y = bf16x2_rn(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3]));
-                            o.z = bf16x2_rn(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5]));
-                            o.w = bf16x2_rn(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7]));
-                            dst[q] = o;
-                        }
-                    }
+        for (int j = 0; j < 64; ++j) y[j] = 0.0f;
+        bool ok = true;
+        for (int g = 0; ok && g < ngroups; ++g) {
+            const int ab = g & 1, slot = g % TSLOTS;
+            if (!mbar_wait(&bar.accfull[ab], (g >> 1) & 1, a.status) ||
+                !mbar_wait(&bar.tfull[slot], (g / TSLOTS) & 1, a.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t t_acc = tmem + lane_off + (ab ? TM_ACC1 : TM_ACC0) + hc * 64;
+            const float ssum = __uint_as_float(tmem_ld_32x32b_x1(tmem + lane_off + (ab ? TM_ACC1 : TM_ACC0) + BN));
+            const float2 *tab = table + slot * BN + hc * 64;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(t_acc + c * 32, r);
+                tmem_ld_wait();
+                if (c == 1) {
+                    // both halves are in registers: hand the buffers back
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar.accempty[ab]);
+                }
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float2 sc = tab[c * 32 + j];
+                    y[c * 32 + j] = fmaf(sc.x, __uint_as_float(r[j]), fmaf(sc.y, ssum, y[c * 32 + j]));
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar.tempty[slot]);
+        }
+        const int m = m0 + row;
+        if (ok && m < a.M) {
+            uint4 *dst = reinterpret_cast<uint4 *>(a.Y + static_cast<size_t>(m) * a.N + n0 + hc * 64);
+            const int valid_cols = rows_n - hc * 64;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                if (q * 8 < valid_cols) {
+                    uint4 o;
+                    o.x = bf16x2_rn(y[8 * q + 0], y[8 * q + 1]);
+                    o.y = bf16x2_rn(y[8 * q + 2], y[8 * q + 3]);
+                    o.z = bf16x2_rn(y[8 * q + 4], y[8 * q + 5]);
+                    o.w = bf16x2_rn(y[8 * q + 6], y[8 * q + 7]);
+                    dst[q] = o;
                 }
             }
         }
@@ -268,6 +354,8 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar.done);
     }
+    // no CTA leaves while cluster peers may still signal or fill its memory
+    cluster_sync();
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -296,11 +384,14 @@ cudaError_t launch_gemm_int4(const uint16_t *X, const uint8_t *qw, const uint16_
     if (K > MAX_K) return cudaErrorNotSupported;
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
+    const unsigned gx = static_cast<unsigned>((N + BN - 1) / BN), gy = static_cast<unsigned>((M + BM - 1) / BM);
+    const int csize = (gx % 4 == 0) ? 4 : (gx % 2 == 0) ? 2 : 1;
     CUtensorMap tmX, tmW;
     {
+        // X as BF16 [M, K]; box of 64 (one K block) x 128/csize rows, 128-byte swizzle
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-        const cuuint32_t box[2] = {BK, BM};
+        const cuuint32_t box[2] = {BK, static_cast<cuuint32_t>(BM / csize)};
         const cuuint32_t estr[2] = {1, 1};
         if (enc(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(X), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -308,16 +399,18 @@ cudaError_t launch_gemm_int4(const uint16_t *X, const uint8_t *qw, const uint16_
             return cudaErrorInvalidValue;
     }
     {
+        // packed codes as bytes [N, K/2]; box of 128 bytes (four K blocks) x 128 rows
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(N)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
-        const cuuint32_t box[2] = {BK / 2, BN};
+        const cuuint32_t box[2] = {128, BN};
         const cuuint32_t estr[2] = {1, 1};
         if (enc(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(qw), dims, strides, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
     GemmArgs a;
+    a.csize = csize;
     a.s = s;
     a.z = z;
     a.Y = Y;
@@ -327,7 +420,14 @@ cudaError_t launch_gemm_int4(const uint16_t *X, const uint8_t *qw, const uint16_
     a.K = static_cast<int>(K);
     a.G = static_cast<int>(K / 128);
     a.sz_bytes = (BN * a.G * 2 + 15) & ~15;
-    const int smem = 1024 + OFF_SZ + 2 * a.sz_bytes + static_cast<int>(sizeof(Barriers));
+    // as many X stages as shared memory allows (3 .. MAX_XS)
+    const int fixed = 1024 + OFF_X + 2 * a.sz_bytes + static_cast<int>(sizeof(Barriers)) + 16;
+    int xs = (dev.max_smem_optin - fixed) / X_BYTES;
+    if (xs > MAX_XS) xs = MAX_XS;
+    if (xs < 2) return cudaErrorNotSupported;
+    a.xs = xs;
+    a.off_sz = OFF_X + xs * X_BYTES;
+    const int smem = 1024 + a.off_sz + 2 * a.sz_bytes + static_cast<int>(sizeof(Barriers));
     static int configured[64] = {0};
     const int d = dev.device & 63;
     if (configured[d] < smem) {
@@ -335,9 +435,19 @@ cudaError_t launch_gemm_int4(const uint16_t *X, const uint8_t *qw, const uint16_
         if (e != cudaSuccess) return e;
         configured[d] = smem;
     }
-    const dim3 grid(static_cast<unsigned>((N + BN - 1) / BN), static_cast<unsigned>((M + BM - 1) / BM));
-    gemm_int4_tc_kernel<<<grid, THREADS, smem, st>>>(tmX, tmW, a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(gx, gy, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(csize);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_int4_tc_kernel, tmX, tmW, a);
 }
 
 }  // namespace w4

@@ -41,7 +41,7 @@ def test_gemm_full_size_sampled(M):
     assert_close(Y[np.ix_(rows, cols)], ref, "gemm M=%d sample" % M)
 
 
-def test_gemm_identity_weights_exact():
+def test_gemm_identity_weights():
     torch, w4 = cuda_or_skip()
     K = 256
     codes = np.eye(K, dtype=np.uint8)
@@ -49,7 +49,11 @@ def test_gemm_identity_weights_exact():
     one = np.float16(1.0).view(np.uint16)
     p = {"qw": qw, "s": np.full((K, 2), one, np.uint16), "z": np.zeros((K, 2), np.uint16),
          "x": synth.normal_bf16(synth.Stream(3), (200, K)), "M": 200, "N": K}
-    assert np.array_equal(_run(w4, torch, p), p["x"])
+    # y = x up to the binary32 cancellation of the 128 * sum(x) offset
+    ref = oracle.gemm_int4(p["x"], p["qw"], p["s"], p["z"], K=K)
+    y = _run(w4, torch, p)
+    assert_close(y, ref, "identity")
+    assert np.mean(y == p["x"]) > 0.99
 
 
 def test_gemm_repeatable():
@@ -61,14 +65,22 @@ def test_gemm_repeatable():
     assert w4.w4a16_check_device_error() == 0
 
 
-def test_gemm_activation_beyond_f16_range_sets_status():
+def test_gemm_large_activations_keep_bf16_range():
+    # X enters the tensor cores as loaded BF16: magnitudes far beyond the F16
+    # range are fine
     torch, w4 = cuda_or_skip()
-    p = synth.int4_problem(128, 256, M=4, seed=6)
-    big = np.float32(1e5)
-    xb = (p["x"].astype(np.uint32) << 16).view(np.float32).copy()
-    xb[2, 7] = big
-    p["x"] = (xb.view(np.uint32) >> 16).astype(np.uint16)
+    p = synth.int4_problem(256, 512, M=8, seed=6)
+    xb = (p["x"].astype(np.uint32) << 16).view(np.float32) * np.float32(1e6)
+    p["x"] = torch.tensor(xb).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    ref = oracle.gemm_int4(p["x"], p["qw"], p["s"], p["z"], K=512)
+    assert_close(_run(w4, torch, p), ref, "gemm large x")
     assert w4.w4a16_check_device_error() == 0
-    _run(w4, torch, p)
-    assert w4.w4a16_check_device_error() == 6
-    assert w4.w4a16_check_device_error() == 0
+
+
+def test_gemm_fractional_zero_points():
+    torch, w4 = cuda_or_skip()
+    p = synth.int4_problem(384, 1024, M=64, seed=8)
+    rng = np.random.default_rng(8)
+    p["z"] = rng.uniform(0, 15, size=p["z"].shape).astype(np.float16).view(np.uint16)
+    ref = oracle.gemm_int4(p["x"], p["qw"], p["s"], p["z"], K=1024)
+    assert_close(_run(w4, torch, p), ref, "gemm fractional z")
