@@ -360,19 +360,28 @@ def run_ours(args):
     if w4.w4a16_check_device_error() != 0:
         raise SystemExit("device status set during warm-up")
 
-    # one captured graph per weight set: a step is one replay
+    # CUDA graphs: one holding a step for each of the L2_SETS weight sets back
+    # to back (so consecutive launches chain inside the graph), and one per
+    # single step for the remainder; the timed loop runs exactly args.steps
+    # steps.
     graphs = None
     if not args.no_graph:
         try:
-            graphs = []
+            whole = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(whole):
+                for i in range(L2_SETS):
+                    step(i)
+            singles = []
             for i in range(L2_SETS):
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g):
                     step(i)
-                graphs.append(g)
-            for g in graphs:
+                singles.append(g)
+            whole.replay()
+            for g in singles:
                 g.replay()
             torch.cuda.synchronize()
+            graphs = (whole, singles)
         except Exception:
             graphs = None
             torch.cuda.synchronize()
@@ -385,10 +394,14 @@ def run_ours(args):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for i in range(args.steps):
-        if graphs is not None:
-            graphs[i % L2_SETS].replay()
-        else:
+    if graphs is not None:
+        whole, singles = graphs
+        for _ in range(args.steps // L2_SETS):
+            whole.replay()
+        for i in range(args.steps % L2_SETS):
+            singles[i].replay()
+    else:
+        for i in range(args.steps):
             step(i)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -461,7 +474,8 @@ def run_ours(args):
             "config": {"workload": WORKLOAD, "bytes_per_step": STEP_BYTES,
                        "l2": "%d rotating weight sets of %.1f MB each (inputs larger than the 129 MB L2)"
                              % (L2_SETS, STEP_BYTES / 1e6),
-                       "launch": "CUDA graph per step" if graphs is not None else "eager",
+                       "launch": ("CUDA graph of %d steps (programmatic dependent launch between kernels)" % L2_SETS)
+                       if graphs is not None else "eager (programmatic dependent launch between kernels)",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": roofline, "cpu_baseline": base, "e2e": e2e,
             "gpu_launches": 2 * args.steps, "clocks": clk, "device_status": status,

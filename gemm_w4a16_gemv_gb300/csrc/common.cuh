@@ -114,6 +114,13 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return p;
 }
 
+// L2 policy for small operands that every CTA reads (the activation).
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 // One-dimensional bulk copy global -> this CTA's shared memory, completing
 // `bytes` transaction bytes on `bar`.  dst, src 16-byte aligned; bytes % 16 == 0.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src,
@@ -125,6 +132,23 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src,
         "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
+
+// Bulk prefetch of [src, src + bytes) into L2 (no destination, no barrier);
+// src 16-byte aligned, bytes % 16 == 0.  L2 is the point of coherence, so a
+// prefetched line never hides a later write by another kernel.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Programmatic dependent launch.  launch_dependents lets the next kernel of
+// the stream (launched with programmatic stream serialisation) be scheduled
+// before this grid ends; wait blocks the calling thread until every grid this
+// one depends on has completed and its memory operations are visible.  Both
+// are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Four-byte asynchronous copy global -> shared (LDGSTS), 4-byte aligned.
 __device__ __forceinline__ void cp_async_4(void *dst, const void *src) {

@@ -1,17 +1,22 @@
 // Consumer-side building blocks of the M = 1 GEMV kernels (INT4 and FP4):
-// activation staging, the mixed-precision multiply-add, code unpacking and
-// the multi-row warp reduction.
+// activation conversion, code unpacking, the dot-product instructions and the
+// multi-row warp reduction.
 //
-// Arithmetic budget.  On sm_103a the logic / variable-shift / convert pipe
-// runs at half the FMA rate, and a GEMV streaming at HBM speed leaves about
-// two issue slots per weight element.  The unpack therefore produces two
-// codes per logic op as an f16x2 pair, and the multiply-add is the
-// mixed-precision fma.rn.f32.f16 (f16 x f16 + f32 -> f32, full rate): every
-// product is exact in binary32 and every sum is binary32.
-//
-// Activations are held as f16 after an exact power-of-two scaling chosen per
-// 32-element unit (the largest |x| of the unit lands in [2^14, 2^15)), so the
-// BF16 range is never clipped; the scale is undone once per unit.
+// Arithmetic budget.  A GEMV streaming at HBM speed on 152 SMs must retire
+// about 40 weight codes per SM clock.  Measured on sm_103a (codes per SM
+// clock, instruction stream alone): the binary16 route -- two codes per
+// logic op via the exponent-bias OR, then the mixed-precision
+// fma.rn.f32.f16 -- sustains about 43; the integer route -- even codes as
+// bytes c, odd codes as bytes 16c (one logic op each for four codes), then
+// dp2a against 16-bit activations -- about 87.  INT4 therefore takes the
+// integer route: activations become signed 16-bit integers with one
+// power-of-two scale per 128-element group (exact for the group's top eight
+// binades, rounded by at most 2^-15 of the group maximum below that), every
+// product and sum of a group is exact in 32-bit integers, and the scale, zero
+// point and activation scale are applied once per (row, group) in binary32.
+// FP4 codes are not integers (E2M1); they decode exactly to binary16 pairs
+// (cvt.rn.f16x2.e2m1x2) and meet binary16 activations, scaled exactly by a
+// power of two per 32-element unit, in the mixed-precision FMA.
 #pragma once
 
 #include "common.cuh"
@@ -44,30 +49,39 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-// Exponent e with 2^e <= max|x| < 2^(e+1) over 32 BF16 values (as bits); a
-// unit of zeros gives 14.  Clamped so that 2^(14-e) and 2^(e-14) stay normal
-// binary32 numbers.
-__device__ __forceinline__ int unit_exponent(const uint32_t (&xb)[16]) {
+// Largest |x| bit pattern over 32 BF16 values held as 16 words of pairs.
+__device__ __forceinline__ uint32_t unit_absmax_bits(const uint32_t (&xb)[16]) {
     uint32_t m2 = 0;  // two packed 16-bit maxima of |x| bit patterns
 #pragma unroll
     for (int i = 0; i < 16; ++i) m2 = __vmaxu2(m2, xb[i] & 0x7FFF7FFFu);
-    const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
-    int e = static_cast<int>(m >> 7) - 127;  // BF16 exponent (subnormals read as -127)
+    return max(m2 & 0xFFFFu, m2 >> 16);
+}
+
+// Exponent e with 2^e <= m < 2^(e+1) for the BF16 magnitude bit pattern m;
+// zero gives 14.  Clamped so that 2^(14-e) and 2^(e-14) stay normal binary32
+// numbers (subnormal BF16 values read as exponent -127).
+__device__ __forceinline__ int exponent_of_absmax(uint32_t m) {
+    int e = static_cast<int>(m >> 7) - 127;
     if (m == 0) e = 14;
     e = max(e, -100);
     e = min(e, 113);
     return e;
 }
 
+__device__ __forceinline__ int unit_exponent(const uint32_t (&xb)[16]) {
+    return exponent_of_absmax(unit_absmax_bits(xb));
+}
+
 __device__ __forceinline__ float pow2f(int e) { return __uint_as_float(static_cast<uint32_t>(e + 127) << 23); }
 
-// Load 32 BF16 activations (64 bytes, 16-byte aligned) as 16 words of packed
-// pairs: xb[i] = {x[2i], x[2i+1]}.
+// Load 32 BF16 activations (64 bytes, 16-byte aligned, global memory) as 16
+// words of packed pairs: xb[i] = {x[2i], x[2i+1]}.  A plain (coherent) load:
+// the activation may have been written by the previous kernel of the stream.
 __device__ __forceinline__ void load_x_unit(const uint16_t *x, uint32_t (&xb)[16]) {
     const uint4 *p = reinterpret_cast<const uint4 *>(x);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        const uint4 v = __ldg(p + q);
+        const uint4 v = p[q];
         xb[4 * q + 0] = v.x;
         xb[4 * q + 1] = v.y;
         xb[4 * q + 2] = v.z;
@@ -75,8 +89,73 @@ __device__ __forceinline__ void load_x_unit(const uint16_t *x, uint32_t (&xb)[16
     }
 }
 
+// Round |t| < 2^22 to the nearest integer (ties to even) with one FMA: adding
+// 1.5 * 2^23 leaves a binary32 number whose unit in the last place is 1, so
+// the sum's low mantissa bits are 2^22 + rint(t).
+__device__ __forceinline__ int rint_scaled(float x, float scale) {
+    const float r = fmaf(x, scale, 12582912.0f);
+    return static_cast<int>(__float_as_uint(r) - 0x4B400000u);
+}
+
 __device__ __forceinline__ float bf16_elem(const uint32_t (&xb)[16], int k) {
     return bf16_bits_to_f32((k & 1) ? (xb[k >> 1] >> 16) : (xb[k >> 1] & 0xFFFFu));
+}
+
+// d = c + a.lo16 * b.byte0 + a.hi16 * b.byte1   (a: two signed 16-bit values,
+// b: unsigned bytes; exact in 32-bit integers)
+__device__ __forceinline__ int dp2a_lo(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+// d = c + a.lo16 * b.byte2 + a.hi16 * b.byte3
+__device__ __forceinline__ int dp2a_hi(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t pack_i16x2(int lo, int hi) {
+    return (static_cast<uint32_t>(lo) & 0xFFFFu) | (static_cast<uint32_t>(hi) << 16);
+}
+
+// INT4 activation unit: 32 BF16 values (as 16 words of pairs) -> 16 words of
+// signed 16-bit pairs, x_int = rint(x * 2^(14-e)), in the order the integer
+// dot products meet them: for word m of a packed unit (codes 8m..8m+7; its
+// bytes hold codes (8m+2i, 8m+2i+1)), the even codes come as bytes
+// (c0, c2, c4, c6) and the odd ones as (16 c1, 16 c3, 16 c5, 16 c7), so the
+// pairs are (x0, x2), (x4, x6), (x1, x3), (x5, x7).  e is the exponent of the
+// largest |x| of the whole 128-element group, whose top binade therefore maps
+// exactly into [2^14, 2^15) (|x_int| <= 32640); only values below 2^(e-7)
+// are rounded, by at most 2^-15 of the group's maximum.  Returns sum x_int.
+__device__ __forceinline__ int int4_x_unit(const uint32_t (&xb)[16], int e, uint32_t (&xr)[16]) {
+    const float inv = pow2f(14 - e);
+    int sum = 0;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        int v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            v[q] = rint_scaled(bf16_elem(xb, 8 * m + q), inv);  // x * inv is exact
+            sum += v[q];
+        }
+        xr[4 * m + 0] = pack_i16x2(v[0], v[2]);
+        xr[4 * m + 1] = pack_i16x2(v[4], v[6]);
+        xr[4 * m + 2] = pack_i16x2(v[1], v[3]);
+        xr[4 * m + 3] = pack_i16x2(v[5], v[7]);
+    }
+    return sum;
+}
+
+// FP4 activation unit: 32 BF16 values -> 16 f16x2 natural pairs (x[2i],
+// x[2i+1]) scaled exactly by 2^(14-e) (binary16 holds every BF16 value of the
+// unit's top 28 binades exactly); returns pw = 2^(e-14).
+__device__ __forceinline__ float fp4_x_unit(const uint32_t (&xb)[16], uint32_t (&xr)[16]) {
+    const int e = unit_exponent(xb);
+    const float inv = pow2f(14 - e);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) xr[q] = pack_half2(bf16_elem(xb, 2 * q) * inv, bf16_elem(xb, 2 * q + 1) * inv);
+    return pow2f(e - 14);
 }
 
 // Sum of R per-row partials over the 32 lanes of a warp, R in {1, 2, 4}.

@@ -23,6 +23,7 @@ cudaError_t launch_gemv_int4(const uint16_t *x, const uint8_t *qw, const uint16_
     a.rows_per_slot = N;
     a.V = N;
     a.E = 1;
+    a.sz_total = N * (K / 128) * 2;
     a.K = static_cast<int>(K);
     a.G = static_cast<int>(K / 128);
     return gemv_dispatch<false>(a, st, dev.device, dev.num_sms, dev.max_smem_optin);

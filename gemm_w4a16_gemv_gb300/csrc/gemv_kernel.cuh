@@ -4,23 +4,26 @@
 //   INT4: y[v]       = sum_k x[k] * (q[v,k] - z[v,k/128]) * s[v,k/128]
 //   FP4 : y[i*N + n] = sum_k x[k] * e2m1(q[ids[i],n,k]) * s[ids[i],n,k/32]
 //
-// One persistent CTA per SM.  Warp CW is the producer: it walks this CTA's
-// output rows ("virtual rows" v; for FP4 v = i*N + n) in blocks of at most RB
-// rows that never cross an expert boundary, and for each block issues one
-// cp.async.bulk of the block's packed rows (one contiguous range of the
-// row-major matrix) plus 4-byte cp.async copies of the block's scale (and
-// zero) rows, all completing on the stage's "full" mbarrier.  A ring of
-// `stages` shared-memory stages keeps up to ~150 KB of weights in flight.
+// One persistent CTA per SM, launched with programmatic stream serialisation
+// so that it can start while the previous kernel of the stream drains.
 //
-// Warps 0..CW-1 consume.  The activation vector is converted once per CTA,
-// cooperatively, into f16x2 pairs with an exact power-of-two scale per
-// 32-element unit (gemv_common.cuh) and parked in shared memory; each thread
-// then keeps the pairs of its own units in registers.  Threads form teams of
-// TT threads; a team owns RPT rows of every stage and each of its threads
-// owns UPT 32-code units of those rows.  Per-row partials are reduced across
-// the warp with a transposed butterfly and across the team's warps by the
-// producer, in a fixed order (so results are bitwise reproducible), when it
-// recycles the stage; it then writes the BF16 outputs.  All waits are bounded.
+// Warp CW is the producer.  Before the previous kernel has finished it only
+// warms L2 with the first weights of its range (an L2 prefetch cannot hide a
+// later write); after griddepcontrol.wait it walks this CTA's output rows
+// ("virtual rows" v; for FP4 v = i*N + n) in blocks of at most RB rows that
+// never cross an expert boundary, and per block issues three bulk copies into
+// a ring stage -- the block's packed rows (contiguous in the row-major
+// matrix) and the 16-byte-aligned ranges enclosing its scale and zero rows --
+// all completing on the stage's "full" mbarrier.  When a stage comes back it
+// sums the consumers' per-warp partials of each row in a fixed order (results
+// are bitwise reproducible) and writes the BF16 outputs.
+//
+// Warps 0..CW-1 consume.  They convert the activation once per CTA into
+// shared memory (INT4: signed 16-bit integers with a power-of-two scale per
+// 128-element group, for exact DP2A integer dot products; FP4: binary16
+// pairs with a scale per 32-element unit, for the mixed-precision FMA), then
+// keep the part each thread owns in registers and work through the stages.
+// All waits are bounded.
 #pragma once
 
 #include "common.cuh"
@@ -43,10 +46,11 @@ struct GemvParams {
     int64_t V;              // virtual rows in total (INT4: N; FP4: topk * N)
     int64_t E;              // FP4: number of experts
     int K, G, UPR, RB, stages;
+    int64_t sz_total;       // bytes of the whole scale tensor (and of the zero tensor)
     int w_bytes;            // packed weights of a stage (RB * K/2)
-    int sz_bytes;           // one scale (or zero) region of a stage, 16-aligned
+    int sz_bytes;           // one scale (or zero) region of a stage, 16-aligned, with slack
+    int x_off;              // byte offset of the converted activation units (K/32 * 72 bytes)
     int stage_bytes;        // 128-aligned
-    int x_off;              // byte offset of the staged activations
     int stage_off;          // byte offset of stage 0
 };
 
@@ -54,6 +58,8 @@ struct StageMeta {
     long long vrow;  // first virtual row of the block
     int rows;
     int valid;       // FP4: expert id in range
+    int soff;        // half-words between the stage's s/z region start and the block's first group
+    int pad;
 };
 
 template <int CW, int RPT>
@@ -64,10 +70,6 @@ struct GemvHeader {
     float psum[kGemvMaxStages][2][CW][RPT];  // per-warp row partials, by phase parity
 };
 
-// Per-unit constants: INT4 bias sum, effective activation sum; scale undo.
-struct UnitConst {
-    float c, xs, pw, pad;
-};
 
 __device__ __forceinline__ int64_t gemv_even_floor(int64_t v) { return v & ~int64_t(1); }
 
@@ -120,29 +122,40 @@ __device__ __forceinline__ void gemv_producer(const GemvParams &a, GemvHeader<CW
         unsigned char *st = stage0 + slot * a.stage_bytes;
         uint16_t *ss = reinterpret_cast<uint16_t *>(st + a.w_bytes);
         uint16_t *sz = reinterpret_cast<uint16_t *>(st + a.w_bytes + a.sz_bytes);
-        const uint16_t *gs = a.s + src_row * a.G;
-        const uint16_t *gz = FP4 ? nullptr : a.z + src_row * a.G;
-        const int nsz = rows * a.G;
+        // The block's scale (and zero) rows are one contiguous byte range
+        // [b0, b1) of their tensor; copy its enclosing 16-byte-aligned range,
+        // except past the tensor's end, where the last < 16 bytes are copied
+        // by plain loads.
+        const uint64_t b0 = static_cast<uint64_t>(src_row) * a.G * 2;
+        const uint64_t b1 = b0 + static_cast<uint64_t>(rows) * a.G * 2;
+        const uint64_t lo16 = b0 & ~uint64_t(15);
+        uint64_t hi16 = (b1 + 15) & ~uint64_t(15);
+        if (hi16 > static_cast<uint64_t>(a.sz_total)) hi16 = b1 & ~uint64_t(15);
+        const uint32_t nb = static_cast<uint32_t>(hi16 - lo16);
         if (lane == 0) {
             if (!ok) atomicOr(a.status, kDevBadExpert);
             h.meta[slot].vrow = v;
             h.meta[slot].rows = rows;
             h.meta[slot].valid = ok ? 1 : 0;
-            if (!FP4 && (nsz & 1)) {  // odd tail: one half-word copied synchronously
-                ss[nsz - 1] = gs[nsz - 1];
-                sz[nsz - 1] = gz[nsz - 1];
+            h.meta[slot].soff = static_cast<int>((b0 - lo16) >> 1);
+            if (ok) {
+                for (uint64_t o = hi16; o < b1; o += 2) {  // ragged end of the tensor
+                    ss[(o - lo16) >> 1] = a.s[o >> 1];
+                    if (!FP4) sz[(o - lo16) >> 1] = a.z[o >> 1];
+                }
             }
             const uint32_t wb = ok ? static_cast<uint32_t>(rows) * half_k : 0u;
-            mbar_arrive_expect_tx(&h.full[slot], wb);
-            if (ok) bulk_g2s(st, a.qw + src_row * half_k, wb, &h.full[slot], pol);
-        }
-        if (ok) {
-            for (int i = lane; i < (nsz >> 1); i += 32) {
-                cp_async_4(ss + 2 * i, gs + 2 * i);
-                if (!FP4) cp_async_4(sz + 2 * i, gz + 2 * i);
+            const uint32_t sb = ok ? nb * (FP4 ? 1u : 2u) : 0u;
+            mbar_arrive_expect_tx(&h.full[slot], wb + sb);
+            if (ok) {
+                bulk_g2s(st, a.qw + src_row * half_k, wb, &h.full[slot], pol);
+                if (nb) {
+                    bulk_g2s(ss, reinterpret_cast<const unsigned char *>(a.s) + lo16, nb, &h.full[slot], pol);
+                    if (!FP4)
+                        bulk_g2s(sz, reinterpret_cast<const unsigned char *>(a.z) + lo16, nb, &h.full[slot], pol);
+                }
             }
         }
-        cp_async_arrive_noinc(&h.full[slot]);
         // the next copy is in flight; now finish the block this slot held
         if (recycle) finalize(slot, phase ^ 1, old);
         v += rows;
@@ -160,114 +173,207 @@ __device__ __forceinline__ void gemv_producer(const GemvParams &a, GemvHeader<CW
     }
 }
 
-// Cooperative activation staging: one thread per 32-element unit writes the
-// unit's 16 f16x2 pairs and its constants to shared memory.
-template <bool FP4>
-__device__ __forceinline__ void gemv_stage_x(const GemvParams &a, uint32_t *xh_s, UnitConst *xc_s, int tid,
-                                             int nthreads) {
-    for (int u = tid; u < a.UPR; u += nthreads) {
-        uint32_t xb[16];
-        load_x_unit(a.x + 32 * u, xb);
-        const int e = unit_exponent(xb);
-        const float inv = pow2f(14 - e);
-        UnitConst uc;
-        uc.pw = pow2f(e - 14);
-        uc.pad = 0.0f;
-        float c = 0.0f, xs = 0.0f;
-        uint32_t out[16];
-        if (FP4) {
-            // natural pairs (x[2i], x[2i+1]), matching the E2M1 byte decode
-#pragma unroll
-            for (int q = 0; q < 16; ++q)
-                out[q] = pack_half2(bf16_elem(xb, 2 * q) * inv, bf16_elem(xb, 2 * q + 1) * inv);
-        } else {
-            // INT4 unpack order for word m: (8m, 8m+4), (8m+1, 8m+5)/16,
-            // (8m+2, 8m+6), (8m+3, 8m+7)/16 -- the /16 pairs meet codes that
-            // the unpack leaves multiplied by 16
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float f = (q & 1) ? 0.0625f : 1.0f;
-                    const float v0 = bf16_elem(xb, 8 * m + q) * inv * f;
-                    const float v1 = bf16_elem(xb, 8 * m + q + 4) * inv * f;
-                    out[4 * m + q] = pack_half2(v0, v1);
-                    c += v0 + v1;                                   // times the 1024 bias below
-                    xs += (q & 1) ? 16.0f * (v0 + v1) : (v0 + v1);  // activation each product sees
-                }
-            }
-        }
-        uc.c = 1024.0f * c;
-        uc.xs = xs;
-        uint4 *dst = reinterpret_cast<uint4 *>(xh_s + 16 * u);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) dst[q] = make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
-        xc_s[u] = uc;
+// L2 prefetch of the first rows of this CTA's range (about one ring of
+// stages): packed codes, then the matching scale and zero rows, each range
+// trimmed inward to 16-byte boundaries so that it never leaves its tensor.
+__device__ __forceinline__ void gemv_prefetch_l2_range(const void *base, uint64_t lo, uint64_t hi) {
+    lo = (lo + 15) & ~uint64_t(15);
+    hi &= ~uint64_t(15);
+    const unsigned char *p = static_cast<const unsigned char *>(base);
+    for (uint64_t o = lo; o < hi; o += 32768) {
+        const uint64_t n = hi - o < 32768 ? hi - o : 32768;
+        prefetch_l2_bulk(p + o, static_cast<uint32_t>(n));
     }
 }
 
-template <bool FP4, int CW, int TT, int UPT, int RPT>
-__global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_stream_kernel(const GemvParams a) {
-    using Header = GemvHeader<CW, RPT>;
-    extern __shared__ __align__(1024) unsigned char smem[];
-    Header &h = *reinterpret_cast<Header *>(smem);
-    uint32_t *xh_s = reinterpret_cast<uint32_t *>(smem + a.x_off);                // [UPR][16]
-    UnitConst *xc_s = reinterpret_cast<UnitConst *>(smem + a.x_off + a.UPR * 64);  // [UPR]
-    unsigned char *stage0 = smem + a.stage_off;
+__device__ __forceinline__ void gemv_prefetch_l2(const GemvParams &a, int64_t begin, int64_t end) {
+    const int64_t half_k = a.K >> 1;
+    int64_t rows = static_cast<int64_t>(a.stages) * a.RB;
+    if (rows > end - begin) rows = end - begin;
+    if (rows <= 0) return;
+    gemv_prefetch_l2_range(a.qw, begin * half_k, (begin + rows) * half_k);
+    const uint64_t g0 = static_cast<uint64_t>(begin) * a.G * 2, g1 = static_cast<uint64_t>(begin + rows) * a.G * 2;
+    gemv_prefetch_l2_range(a.s, g0, g1);
+    gemv_prefetch_l2_range(a.z, g0, g1);
+}
 
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-
-    // This CTA's virtual rows.  INT4 ranges start on even rows, so every block
-    // start is even and the 4-byte copies of scale/zero rows stay aligned when
-    // K/128 is odd.
-    int64_t begin = blockIdx.x * a.V / gridDim.x;
-    int64_t end = (blockIdx.x + 1) * a.V / gridDim.x;
-    if (!FP4) {
-        begin = gemv_even_floor(begin);
-        end = (blockIdx.x + 1 == gridDim.x) ? a.V : gemv_even_floor(end);
-    }
-
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < a.stages; ++i) {
-            mbar_init(&h.full[i], 33);  // producer lane 0 (+tx) and 32 cp.async lanes
-            mbar_init(&h.empty[i], CW);
+// Activation conversion, once per CTA, one 32-element unit per consumer
+// thread (units u = K/32 of them).  Shared-memory layout at xs: [K/32][16]
+// words of converted pairs, then per scale block a float2 (xsum, pw).
+//  INT4: scale block = one 128-element group (4 units, 4 neighbouring lanes
+//        agree on the group exponent through shuffles; K % 128 == 0 makes
+//        every group whole); xsum = sum of the group's x_int.
+//  FP4:  scale block = the unit; (0, pw).
+template <bool FP4, int CW>
+__device__ __forceinline__ void gemv_convert_x(const GemvParams &a, unsigned char *xs, int warp, int lane) {
+    uint32_t *xw = reinterpret_cast<uint32_t *>(xs);
+    const int units = a.K >> 5;
+    float2 *xc = reinterpret_cast<float2 *>(xs + units * 64);
+    for (int u0 = warp * 32; u0 < units; u0 += CW * 32) {  // warp-uniform
+        const int u = u0 + lane;
+        const bool ok = u < units;
+        uint32_t xb[16], w[16];
+        if (ok) {
+            load_x_unit(a.x + 32 * u, xb);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) xb[i] = 0u;
         }
-        fence_barrier_init();
+        float2 c;
+        if constexpr (FP4) {
+            c = make_float2(0.0f, fp4_x_unit(xb, w));
+        } else {
+            uint32_t m = unit_absmax_bits(xb);
+            m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            const int e = exponent_of_absmax(m);
+            int sum = int4_x_unit(xb, e, w);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            c = make_float2(static_cast<float>(sum), pow2f(e - 14));  // |sum| < 2^23: exact
+        }
+        if (ok) {
+            uint4 *dst = reinterpret_cast<uint4 *>(xw + 16 * u);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+            if (FP4) xc[u] = c;
+            else if ((u & 3) == 0) xc[u >> 2] = c;
+        }
     }
-    __syncthreads();
+}
 
-    if (warp == CW) {
-        gemv_producer<FP4, CW, TT, UPT, RPT>(a, h, stage0, begin, end, lane);
-        return;
+// After a stage: reduce the per-row partials across the warp, park them for
+// the producer and release the stage.
+template <int CW, int RPT>
+__device__ __forceinline__ void gemv_release_stage(GemvHeader<CW, RPT> &h, const float (&part)[RPT], int slot,
+                                                   int phase, int warp, int lane) {
+    const float red = warp_reduce_rows<RPT>(part, lane);
+    if ((lane & (32 / RPT - 1)) == 0) h.psum[slot][phase][warp][reduced_row<RPT>(lane)] = red;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&h.empty[slot]);
+}
+
+// INT4 consumer.  A thread owns one 128-code group g of RPT rows per stage:
+// 64 bytes of packed codes per row, read as four 16-byte sub-units (u = 4g+s).
+// Lanes start at different sub-units (rotation by (j >> 1) & 3) so that the
+// eight lanes of each 128-byte shared-memory wavefront hit distinct banks;
+// the x registers are loaded in the same rotated order, so indexing stays
+// static.  Products are exact integer dot products (DP2A); per (row, group):
+//   y += s * 2^(e-14) * (dot - z * xsum).
+template <int CW, int TT, int RPT>
+__device__ __forceinline__ void gemv_consume_int4(const GemvParams &a, GemvHeader<CW, RPT> &h,
+                                                  const unsigned char *stage0, const unsigned char *xs,
+                                                  int64_t begin, int64_t end, int warp, int lane) {
+    const int team = threadIdx.x / TT;
+    const int g = threadIdx.x % TT;
+    const bool valid = g < a.G;
+    const int gs = valid ? g : 0;
+    const int rot = (g >> 1) & 3;
+    const uint32_t *xw = reinterpret_cast<const uint32_t *>(xs);
+    uint32_t xr[4][16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(xw + 16 * (4 * gs + ((q + rot) & 3)));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 v4 = src[i];
+            xr[q][4 * i] = v4.x;
+            xr[q][4 * i + 1] = v4.y;
+            xr[q][4 * i + 2] = v4.z;
+            xr[q][4 * i + 3] = v4.w;
+        }
     }
+    const float2 xc = reinterpret_cast<const float2 *>(xs + (a.K >> 5) * 64)[gs];
+    const float xsum = xc.x, pw = valid ? xc.y : 0.0f;
+    const int half_k = a.K >> 1;
 
-    gemv_stage_x<FP4>(a, xh_s, xc_s, threadIdx.x, CW * 32);
-    named_bar_sync(1, CW * 32);
+    const int rbase = team * RPT;
+    int slot = 0, phase = 0;
+    for (int64_t v = begin; v < end;) {
+        if (!mbar_wait(&h.full[slot], phase, a.status)) return;
+        const int rows = h.meta[slot].rows;
+        const int soff = h.meta[slot].soff;
+        const unsigned char *st = stage0 + slot * a.stage_bytes;
+        const uint16_t *ss = reinterpret_cast<const uint16_t *>(st + a.w_bytes) + soff;
+        const uint16_t *sz = reinterpret_cast<const uint16_t *>(st + a.w_bytes + a.sz_bytes) + soff;
+        float part[RPT];
+#pragma unroll
+        for (int rr = 0; rr < RPT; ++rr) part[rr] = 0.0f;
+        if (valid) {
+            int lo[RPT], hi[RPT];
+#pragma unroll
+            for (int rr = 0; rr < RPT; ++rr) lo[rr] = hi[rr] = 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int sub = (q + rot) & 3;
+                uint4 wv[RPT];
+#pragma unroll
+                for (int rr = 0; rr < RPT; ++rr)
+                    wv[rr] = *reinterpret_cast<const uint4 *>(st + static_cast<size_t>(rbase + rr) * half_k +
+                                                              64 * g + 16 * sub);
+#pragma unroll
+                for (int rr = 0; rr < RPT; ++rr) {
+                    const uint32_t words[4] = {wv[rr].x, wv[rr].y, wv[rr].z, wv[rr].w};
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        // even codes as bytes c (one logic op), odd codes as
+                        // bytes 16c (one logic op, no shift)
+                        const uint32_t ev = words[m] & 0x0F0F0F0Fu, od = words[m] & 0xF0F0F0F0u;
+                        lo[rr] = dp2a_lo(xr[q][4 * m + 0], ev, lo[rr]);
+                        lo[rr] = dp2a_hi(xr[q][4 * m + 1], ev, lo[rr]);
+                        hi[rr] = dp2a_lo(xr[q][4 * m + 2], od, hi[rr]);
+                        hi[rr] = dp2a_hi(xr[q][4 * m + 3], od, hi[rr]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int rr = 0; rr < RPT; ++rr) {
+                const int dot = lo[rr] + (hi[rr] >> 4);  // hi is a multiple of 16; |dot| < 2^24
+                const int gi = (rbase + rr) * a.G + g;
+                const float sf = f16_bits_to_f32(ss[gi]) * pw;
+                const float zf = f16_bits_to_f32(sz[gi]);
+                part[rr] = sf * fmaf(-zf, xsum, static_cast<float>(dot));
+            }
+        }
+        gemv_release_stage<CW, RPT>(h, part, slot, phase, warp, lane);
+        v += rows;
+        if (++slot == a.stages) {
+            slot = 0;
+            phase ^= 1;
+        }
+    }
+}
 
+// FP4 consumer.  A thread owns UPT 32-code units (u = j + i*TT) of RPT rows
+// per stage; codes decode exactly to binary16 pairs (cvt e2m1x2) and meet the
+// f16 activation pairs in the mixed-precision FMA; one scale per unit.
+template <int CW, int TT, int UPT, int RPT>
+__device__ __forceinline__ void gemv_consume_fp4(const GemvParams &a, GemvHeader<CW, RPT> &h,
+                                                 const unsigned char *stage0, const unsigned char *xs,
+                                                 int64_t begin, int64_t end, int warp, int lane) {
     const int team = threadIdx.x / TT;
     const int j = threadIdx.x % TT;
-    uint32_t xh[UPT][16];
-    float cu[UPT], xu[UPT], pw[UPT];
+    const int units = a.K >> 5;
+    const uint32_t *xw = reinterpret_cast<const uint32_t *>(xs);
+    const float2 *xc = reinterpret_cast<const float2 *>(xs + units * 64);
+    uint32_t xr[UPT][16];
+    float pw[UPT];
     bool valid[UPT];
 #pragma unroll
     for (int i = 0; i < UPT; ++i) {
         const int u = j + i * TT;
-        valid[i] = u < a.UPR;
+        valid[i] = u < units;
         const int us = valid[i] ? u : 0;
-        const uint4 *src = reinterpret_cast<const uint4 *>(xh_s + 16 * us);
+        const uint4 *src = reinterpret_cast<const uint4 *>(xw + 16 * us);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const uint4 t = src[q];
-            xh[i][4 * q] = t.x;
-            xh[i][4 * q + 1] = t.y;
-            xh[i][4 * q + 2] = t.z;
-            xh[i][4 * q + 3] = t.w;
+            const uint4 v4 = src[q];
+            xr[i][4 * q] = v4.x;
+            xr[i][4 * q + 1] = v4.y;
+            xr[i][4 * q + 2] = v4.z;
+            xr[i][4 * q + 3] = v4.w;
         }
-        const UnitConst uc = xc_s[us];
-        cu[i] = uc.c;
-        xu[i] = uc.xs;
-        pw[i] = valid[i] ? uc.pw : 0.0f;
+        pw[i] = valid[i] ? xc[us].y : 0.0f;
     }
 
     const int rbase = team * RPT;
@@ -275,9 +381,9 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_stream_kernel(const Gem
     for (int64_t v = begin; v < end;) {
         if (!mbar_wait(&h.full[slot], phase, a.status)) return;
         const int rows = h.meta[slot].rows;
+        const int soff = h.meta[slot].soff;
         const unsigned char *st = stage0 + slot * a.stage_bytes;
-        const uint16_t *ss = reinterpret_cast<const uint16_t *>(st + a.w_bytes);
-        const uint16_t *sz = reinterpret_cast<const uint16_t *>(st + a.w_bytes + a.sz_bytes);
+        const uint16_t *ss = reinterpret_cast<const uint16_t *>(st + a.w_bytes) + soff;
         float part[RPT];
 #pragma unroll
         for (int rr = 0; rr < RPT; ++rr) part[rr] = 0.0f;
@@ -288,51 +394,81 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_stream_kernel(const Gem
             uint4 wv[RPT];
 #pragma unroll
             for (int rr = 0; rr < RPT; ++rr)
-                wv[rr] = *reinterpret_cast<const uint4 *>(st + (static_cast<size_t>(rbase + rr) * a.UPR + u) * 16);
+                wv[rr] = *reinterpret_cast<const uint4 *>(st + (static_cast<size_t>(rbase + rr) * units + u) * 16);
 #pragma unroll
             for (int rr = 0; rr < RPT; ++rr) {
-                float lo = 0.0f, hi = 0.0f;
                 const uint32_t words[4] = {wv[rr].x, wv[rr].y, wv[rr].z, wv[rr].w};
+                float lo = 0.0f, hi = 0.0f;
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
                     const uint32_t w = words[m];
-                    if (FP4) {
-                        mfma_f16x2(e2m1x2_to_f16x2(w), xh[i][4 * m + 0], lo, hi);
-                        mfma_f16x2(e2m1x2_to_f16x2(w >> 8), xh[i][4 * m + 1], lo, hi);
-                        mfma_f16x2(e2m1x2_to_f16x2(w >> 16), xh[i][4 * m + 2], lo, hi);
-                        mfma_f16x2(e2m1x2_to_f16x2(w >> 24), xh[i][4 * m + 3], lo, hi);
-                    } else {
-                        // two codes per logic op: binary16 1024 + q and 1024 + 16q
-                        const uint32_t w8 = w >> 8;
-                        mfma_f16x2((w & 0x000F000Fu) | 0x64006400u, xh[i][4 * m + 0], lo, hi);
-                        mfma_f16x2((w & 0x00F000F0u) | 0x64006400u, xh[i][4 * m + 1], lo, hi);
-                        mfma_f16x2((w8 & 0x000F000Fu) | 0x64006400u, xh[i][4 * m + 2], lo, hi);
-                        mfma_f16x2((w8 & 0x00F000F0u) | 0x64006400u, xh[i][4 * m + 3], lo, hi);
-                    }
+                    mfma_f16x2(e2m1x2_to_f16x2(w), xr[i][4 * m + 0], lo, hi);
+                    mfma_f16x2(e2m1x2_to_f16x2(w >> 8), xr[i][4 * m + 1], lo, hi);
+                    mfma_f16x2(e2m1x2_to_f16x2(w >> 16), xr[i][4 * m + 2], lo, hi);
+                    mfma_f16x2(e2m1x2_to_f16x2(w >> 24), xr[i][4 * m + 3], lo, hi);
                 }
-                if (FP4) {
-                    const float sf = f16_bits_to_f32(ss[(rbase + rr) * a.G + u]) * pw[i];  // one scale per unit
-                    part[rr] = fmaf(sf, lo + hi, part[rr]);
-                } else {
-                    const int g = (rbase + rr) * a.G + (u >> 2);
-                    const float sf = f16_bits_to_f32(ss[g]) * pw[i];
-                    const float zf = f16_bits_to_f32(sz[g]);
-                    float t = (lo + hi) - cu[i];
-                    t = fmaf(-zf, xu[i], t);
-                    part[rr] = fmaf(sf, t, part[rr]);
-                }
+                const float sf = f16_bits_to_f32(ss[(rbase + rr) * a.G + u]) * pw[i];
+                part[rr] = fmaf(sf, lo + hi, part[rr]);
             }
         }
-        const float red = warp_reduce_rows<RPT>(part, lane);
-        if ((lane & (32 / RPT - 1)) == 0) h.psum[slot][phase][warp][reduced_row<RPT>(lane)] = red;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&h.empty[slot]);
+        gemv_release_stage<CW, RPT>(h, part, slot, phase, warp, lane);
         v += rows;
         if (++slot == a.stages) {
             slot = 0;
             phase ^= 1;
         }
     }
+}
+
+template <bool FP4, int CW, int TT, int UPT, int RPT>
+__global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_stream_kernel(const GemvParams a) {
+    using Header = GemvHeader<CW, RPT>;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    Header &h = *reinterpret_cast<Header *>(smem);
+    unsigned char *stage0 = smem + a.stage_off;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // This CTA's contiguous range of virtual rows.
+    const int64_t begin = blockIdx.x * a.V / gridDim.x;
+    const int64_t end = (blockIdx.x + 1) * a.V / gridDim.x;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < a.stages; ++i) {
+            mbar_init(&h.full[i], 1);  // producer lane 0, plus the stage's transaction bytes
+            mbar_init(&h.empty[i], CW);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    // The next launch of the stream may now be scheduled: its CTAs take the
+    // SMs this grid frees and warm L2 with their first weights while this
+    // grid drains.
+    pdl_launch_dependents();
+
+    if (warp == CW) {
+        // The packed weights, scales and zeros are read-only for the whole
+        // stream; only the L2 prefetch runs before the previous kernel ends.
+        if (!FP4 && lane == 0) gemv_prefetch_l2(a, begin, end);
+        // The weights copied into shared memory, the expert ids and the
+        // output follow the stream order.
+        pdl_wait();
+        gemv_producer<FP4, CW, TT, UPT, RPT>(a, h, stage0, begin, end, lane);
+        return;
+    }
+
+    // The activation follows the stream order too.  The consumers convert it
+    // once per CTA into shared memory (plain loads: the bulk-copy engine is
+    // busy with weights), then each thread copies the part it owns into
+    // registers.
+    pdl_wait();
+    gemv_convert_x<FP4, CW>(a, smem + a.x_off, warp, lane);
+    named_bar_sync(1, CW * 32);
+    if constexpr (FP4)
+        gemv_consume_fp4<CW, TT, UPT, RPT>(a, h, stage0, smem + a.x_off, begin, end, warp, lane);
+    else
+        gemv_consume_int4<CW, TT, RPT>(a, h, stage0, smem + a.x_off, begin, end, warp, lane);
 }
 
 // Host side: pick the team shape for K, size the stages, launch one CTA per SM.
@@ -370,8 +506,7 @@ cudaError_t gemv_launch(GemvParams a, cudaStream_t st, int device, int num_sms, 
     auto kern = gemv_stream_kernel<FP4, CW, TT, UPT, RPT>;
     const int header = (static_cast<int>(sizeof(GemvHeader<CW, RPT>)) + 127) & ~127;
     a.x_off = header;
-    const int x_bytes = a.UPR * 64 + a.UPR * static_cast<int>(sizeof(UnitConst));
-    a.stage_off = (a.x_off + x_bytes + 1023) & ~1023;
+    a.stage_off = (a.x_off + (a.K / 32) * 72 + 1023) & ~1023;  // converted units: 64 B of pairs + (xsum, pw)
     int stages = (max_smem - a.stage_off) / a.stage_bytes;
     if (stages > kGemvMaxStages) stages = kGemvMaxStages;
     if (stages < 2) return cudaErrorInvalidValue;
@@ -388,32 +523,70 @@ cudaError_t gemv_launch(GemvParams a, cudaStream_t st, int device, int num_sms, 
     const int64_t max_ctas = (a.V + 1) / 2;  // at least two rows each
     if (ctas > max_ctas) ctas = max_ctas;
     if (ctas < 1) ctas = 1;
-    kern<<<static_cast<unsigned>(ctas), (CW + 1) * 32, smem, st>>>(a);
-    return cudaGetLastError();
+    // Programmatic stream serialisation: this launch may begin while the
+    // previous kernel of the stream finishes; the kernel waits for it
+    // (griddepcontrol.wait) before touching x, y or the expert ids.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+    cfg.blockDim = dim3((CW + 1) * 32);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 // Fill the stage geometry of `a` for K and launch the matching instance.
+//  INT4: a thread owns one 128-code group: TT = the smallest warp multiple
+//        covering K/128 groups; RPT = 2 rows per thread while a stage stays
+//        within the stage target, else 1.
+//  FP4:  TT threads x UPT units of 32 codes cover a row (gemv_choose_shape).
 template <bool FP4>
 cudaError_t gemv_dispatch(GemvParams a, cudaStream_t st, int device, int num_sms, int max_smem) {
-    a.UPR = a.K / 32;
     const int row_bytes = a.K / 2;
-    const GemvShape sh = gemv_choose_shape(kGemvCW, a.UPR, row_bytes, kGemvStageTarget);
+    GemvShape sh = {0, 0, 0};
+    if (FP4) {
+        a.UPR = a.K / 32;
+        sh = gemv_choose_shape(kGemvCW, a.UPR, row_bytes, kGemvStageTarget);
+    } else {
+        a.UPR = a.G;
+        for (int tt = 32; tt <= 128 && sh.TT == 0; tt *= 2)
+            if (tt >= a.G) sh = {tt, 1, 0};
+        if (sh.TT != 0) {
+            const int teams = kGemvCW * 32 / sh.TT;
+            sh.RPT = (teams * 2 * row_bytes <= kGemvStageTarget && teams * 2 <= kGemvMaxRB) ? 2 : 1;
+        }
+    }
     if (sh.TT == 0) return cudaErrorInvalidValue;
-    a.RB = (kGemvCW * 32 / sh.TT) * sh.RPT;  // even: RPT is 2 or 4
+    a.RB = (kGemvCW * 32 / sh.TT) * sh.RPT;
     if (a.RB > kGemvMaxRB) return cudaErrorInvalidValue;
     a.w_bytes = a.RB * row_bytes;
-    a.sz_bytes = ((a.RB * a.G * 2) + 15) & ~15;
+    a.sz_bytes = ((a.RB * a.G * 2) + 32 + 15) & ~15;  // + slack for the 16-byte-aligned superset
     a.stage_bytes = (a.w_bytes + (FP4 ? 1 : 2) * a.sz_bytes + 127) & ~127;
+    if constexpr (FP4) {
 #define W4_GEMV_CASE(TT_, UPT_)                                                                   \
     if (sh.TT == TT_ && sh.UPT == UPT_)                                                           \
-        return sh.RPT == 4 ? gemv_launch<FP4, TT_, UPT_, 4>(a, st, device, num_sms, max_smem)     \
-                           : gemv_launch<FP4, TT_, UPT_, 2>(a, st, device, num_sms, max_smem);
-    W4_GEMV_CASE(32, 2)
-    W4_GEMV_CASE(64, 2)
-    W4_GEMV_CASE(128, 2)
-    W4_GEMV_CASE(256, 2)
-    W4_GEMV_CASE(32, 1)
+        return sh.RPT == 4 ? gemv_launch<true, TT_, UPT_, 4>(a, st, device, num_sms, max_smem)    \
+                           : gemv_launch<true, TT_, UPT_, 2>(a, st, device, num_sms, max_smem);
+        W4_GEMV_CASE(32, 2)
+        W4_GEMV_CASE(64, 2)
+        W4_GEMV_CASE(128, 2)
+        W4_GEMV_CASE(256, 2)
+        W4_GEMV_CASE(32, 1)
 #undef W4_GEMV_CASE
+    } else {
+#define W4_GEMV_CASE(TT_)                                                                         \
+    if (sh.TT == TT_)                                                                             \
+        return sh.RPT == 2 ? gemv_launch<false, TT_, 1, 2>(a, st, device, num_sms, max_smem)      \
+                           : gemv_launch<false, TT_, 1, 1>(a, st, device, num_sms, max_smem);
+        W4_GEMV_CASE(32)
+        W4_GEMV_CASE(64)
+        W4_GEMV_CASE(128)
+#undef W4_GEMV_CASE
+    }
     return cudaErrorInvalidValue;
 }
 

@@ -25,6 +25,7 @@ cudaError_t launch_moe_fp4(const uint16_t *x, const uint8_t *qw, const uint16_t 
     a.rows_per_slot = N;
     a.V = static_cast<int64_t>(topk) * N;
     a.E = E;
+    a.sz_total = E * N * (K / 32) * 2;
     a.K = static_cast<int>(K);
     a.G = static_cast<int>(K / 32);
     return gemv_dispatch<true>(a, st, dev.device, dev.num_sms, dev.max_smem_optin);

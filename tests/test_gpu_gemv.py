@@ -103,3 +103,36 @@ def test_gemv_rejects_bad_arguments_without_launch():
                       torch.zeros(16 * 128, dtype=torch.float16, device="cuda"),
                       torch.zeros(16 * 128, dtype=torch.float16, device="cuda"))
     assert e.value.status == 3
+
+
+def test_gemv_stream_order_with_early_launch():
+    """The GEMV may start before the previous kernel of the stream ends
+    (programmatic dependent launch): it must still see an activation, weights
+    and output buffer that the previous kernels wrote, with no host sync in
+    between.  Chain: torch writes x, up GEMV, down GEMV on the up output,
+    torch rewrites the weights and poisons y, GEMV again."""
+    torch, w4 = cuda_or_skip()
+    up = synth.int4_problem(15360, 3840, seed=21)
+    dn = synth.int4_problem(3840, 15360, seed=22)
+    qu, su, zu = (dev_tensor(up["qw"], torch.uint8), dev_tensor(up["s"], torch.float16),
+                  dev_tensor(up["z"], torch.float16))
+    qd, sd, zd = (dev_tensor(dn["qw"], torch.uint8), dev_tensor(dn["s"], torch.float16),
+                  dev_tensor(dn["z"], torch.float16))
+    x0 = dev_tensor(up["x"], torch.bfloat16).view(-1)
+    torch.cuda.synchronize()
+    x = x0 * 2.0                              # written by a kernel just before the GEMV
+    y_up = w4.w4a16_gemv(x, qu, su, zu)
+    y_dn = w4.w4a16_gemv(y_up, qd, sd, zd)    # consumes the previous launch's output
+    qd2 = torch.flip(qd, dims=[0]).contiguous()  # weights written just before use
+    y2 = torch.full((3840,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    w4.w4a16_gemv(y_up, qd2, sd, zd, y2)
+    torch.cuda.synchronize()
+    xh = host_bits16(x)
+    ref_up = oracle.gemv_int4(xh, up["qw"], up["s"], up["z"], K=3840)
+    yu = host_bits16(y_up)
+    assert_close(yu, ref_up, "chained up")
+    ref_dn = oracle.gemv_int4(yu, dn["qw"], dn["s"], dn["z"], K=15360)
+    assert_close(host_bits16(y_dn), ref_dn, "chained down")
+    ref_2 = oracle.gemv_int4(yu, dn["qw"][::-1].copy(), dn["s"], dn["z"], K=15360)
+    assert_close(host_bits16(y2), ref_2, "rewritten weights")
+    assert w4.w4a16_check_device_error() == 0
