@@ -140,6 +140,12 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// Prefetch the 128-byte line holding p into L2 (through the load/store unit,
+// not the bulk-copy engine).
+__device__ __forceinline__ void prefetch_l2_line(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
+}
+
 // Programmatic dependent launch.  launch_dependents lets the next kernel of
 // the stream (launched with programmatic stream serialisation) be scheduled
 // before this grid ends; wait blocks the calling thread until every grid this

@@ -7,9 +7,9 @@
 // One persistent CTA per SM, launched with programmatic stream serialisation
 // so that it can start while the previous kernel of the stream drains.
 //
-// Warp CW is the producer.  Before the previous kernel has finished it only
-// warms L2 with the first weights of its range (an L2 prefetch cannot hide a
-// later write); after griddepcontrol.wait it walks this CTA's output rows
+// Until the previous kernel has finished, the CTA only warms L2 with the first
+// weights of its range (an L2 prefetch cannot hide a later write).  Then warp
+// CW, the producer, walks this CTA's output rows
 // ("virtual rows" v; for FP4 v = i*N + n) in blocks of at most RB rows that
 // never cross an expert boundary, and per block issues three bulk copies into
 // a ring stage -- the block's packed rows (contiguous in the row-major
@@ -33,6 +33,10 @@ namespace w4 {
 
 constexpr int kGemvMaxStages = 8;
 constexpr int kGemvMaxRB = 32;
+// Stages' worth of weights prefetched into L2 before the previous kernel
+// ends: enough to start the stream at once, little enough not to queue the
+// activation reads behind a burst of misses.
+constexpr int kGemvPrefetchStages = 2;
 
 struct GemvParams {
     const uint16_t *x;
@@ -45,11 +49,13 @@ struct GemvParams {
     int64_t rows_per_slot;  // FP4: N (one expert's rows); INT4: N
     int64_t V;              // virtual rows in total (INT4: N; FP4: topk * N)
     int64_t E;              // FP4: number of experts
+    int64_t rows_q;         // V / grid (rows per CTA) ...
+    int64_t rows_r;         // ... and V % grid (CTAs with one row more)
     int K, G, UPR, RB, stages;
     int64_t sz_total;       // bytes of the whole scale tensor (and of the zero tensor)
     int w_bytes;            // packed weights of a stage (RB * K/2)
     int sz_bytes;           // one scale (or zero) region of a stage, 16-aligned, with slack
-    int x_off;              // byte offset of the converted activation units (K/32 * 72 bytes)
+    int x_off;              // byte offset of the converted activation (K/32 * 72 + 256 bytes)
     int stage_bytes;        // 128-aligned
     int stage_off;          // byte offset of stage 0
 };
@@ -73,15 +79,6 @@ struct GemvHeader {
 
 __device__ __forceinline__ int64_t gemv_even_floor(int64_t v) { return v & ~int64_t(1); }
 
-// Rows of the block starting at virtual row v (this CTA's range ends at end).
-__device__ __forceinline__ int gemv_block_rows(int64_t v, int64_t end, int64_t per_slot, int RB) {
-    const int64_t boundary = (v / per_slot + 1) * per_slot;
-    int64_t r = end - v;
-    if (boundary - v < r) r = boundary - v;
-    if (RB < r) r = RB;
-    return static_cast<int>(r);
-}
-
 template <bool FP4, int CW, int TT, int UPT, int RPT>
 __device__ __forceinline__ void gemv_producer(const GemvParams &a, GemvHeader<CW, RPT> &h,
                                               unsigned char *stage0, int64_t begin, int64_t end,
@@ -102,6 +99,10 @@ __device__ __forceinline__ void gemv_producer(const GemvParams &a, GemvHeader<CW
         }
     };
     int slot = 0, phase = 0, issued = 0;
+    // Expert slot (FP4; INT4 has one slot of N rows) holding row `begin`.
+    int64_t i_slot = FP4 ? begin / a.rows_per_slot : 0;
+    int64_t slot_end = FP4 ? (i_slot + 1) * a.rows_per_slot : end;
+    int64_t expert = FP4 && begin < end ? a.ids[i_slot] : 0;
     for (int64_t v = begin; v < end; ++issued) {
         const bool recycle = issued >= a.stages;
         StageMeta old{};
@@ -110,55 +111,58 @@ __device__ __forceinline__ void gemv_producer(const GemvParams &a, GemvHeader<CW
             old = h.meta[slot];
             __syncwarp();
         }
-        const int rows = gemv_block_rows(v, end, a.rows_per_slot, a.RB);
+        // The block: at most RB rows, not past this CTA's range nor the
+        // current expert slot (no 64-bit division in this loop: a single
+        // thread's division costs hundreds of nanoseconds here).
+        int64_t lim = end - v;
+        if (slot_end - v < lim) lim = slot_end - v;
+        const int rows = static_cast<int>(lim < a.RB ? lim : a.RB);
         int64_t src_row = v;
         bool ok = true;
         if (FP4) {
-            const int64_t i_slot = v / a.rows_per_slot;
-            const int64_t e = a.ids[i_slot];
-            ok = (e >= 0 && e < a.E);
-            src_row = (ok ? e : 0) * a.rows_per_slot + (v - i_slot * a.rows_per_slot);
+            ok = (expert >= 0 && expert < a.E);
+            src_row = (ok ? expert : 0) * a.rows_per_slot + (v - (slot_end - a.rows_per_slot));
         }
         unsigned char *st = stage0 + slot * a.stage_bytes;
         uint16_t *ss = reinterpret_cast<uint16_t *>(st + a.w_bytes);
         uint16_t *sz = reinterpret_cast<uint16_t *>(st + a.w_bytes + a.sz_bytes);
         // The block's scale (and zero) rows are one contiguous byte range
-        // [b0, b1) of their tensor; copy its enclosing 16-byte-aligned range,
-        // except past the tensor's end, where the last < 16 bytes are copied
-        // by plain loads.
+        // [b0, b1) of their tensor.  Its enclosing 16-byte-aligned chunks go
+        // by 16-byte cp.async from the warp's lanes (keeping the bulk-copy
+        // queue for the weights); a chunk that would pass the tensor's end
+        // reads only the bytes before it and zero-fills the rest.
         const uint64_t b0 = static_cast<uint64_t>(src_row) * a.G * 2;
         const uint64_t b1 = b0 + static_cast<uint64_t>(rows) * a.G * 2;
         const uint64_t lo16 = b0 & ~uint64_t(15);
-        uint64_t hi16 = (b1 + 15) & ~uint64_t(15);
-        if (hi16 > static_cast<uint64_t>(a.sz_total)) hi16 = b1 & ~uint64_t(15);
-        const uint32_t nb = static_cast<uint32_t>(hi16 - lo16);
         if (lane == 0) {
             if (!ok) atomicOr(a.status, kDevBadExpert);
             h.meta[slot].vrow = v;
             h.meta[slot].rows = rows;
             h.meta[slot].valid = ok ? 1 : 0;
             h.meta[slot].soff = static_cast<int>((b0 - lo16) >> 1);
-            if (ok) {
-                for (uint64_t o = hi16; o < b1; o += 2) {  // ragged end of the tensor
-                    ss[(o - lo16) >> 1] = a.s[o >> 1];
-                    if (!FP4) sz[(o - lo16) >> 1] = a.z[o >> 1];
-                }
-            }
             const uint32_t wb = ok ? static_cast<uint32_t>(rows) * half_k : 0u;
-            const uint32_t sb = ok ? nb * (FP4 ? 1u : 2u) : 0u;
-            mbar_arrive_expect_tx(&h.full[slot], wb + sb);
-            if (ok) {
-                bulk_g2s(st, a.qw + src_row * half_k, wb, &h.full[slot], pol);
-                if (nb) {
-                    bulk_g2s(ss, reinterpret_cast<const unsigned char *>(a.s) + lo16, nb, &h.full[slot], pol);
-                    if (!FP4)
-                        bulk_g2s(sz, reinterpret_cast<const unsigned char *>(a.z) + lo16, nb, &h.full[slot], pol);
-                }
+            mbar_arrive_expect_tx(&h.full[slot], wb);
+            if (ok) bulk_g2s(st, a.qw + src_row * half_k, wb, &h.full[slot], pol);
+        }
+        if (ok) {
+            const unsigned char *gs = reinterpret_cast<const unsigned char *>(a.s);
+            const unsigned char *gz = reinterpret_cast<const unsigned char *>(a.z);
+            for (uint64_t o = lo16 + 16 * static_cast<uint64_t>(lane); o < b1; o += 16 * 32) {
+                const uint64_t left = static_cast<uint64_t>(a.sz_total) - o;
+                const uint32_t n = left < 16 ? static_cast<uint32_t>(left) : 16u;
+                cp_async_16_zfill(reinterpret_cast<unsigned char *>(ss) + (o - lo16), gs + o, n);
+                if (!FP4) cp_async_16_zfill(reinterpret_cast<unsigned char *>(sz) + (o - lo16), gz + o, n);
             }
         }
+        cp_async_arrive_noinc(&h.full[slot]);
         // the next copy is in flight; now finish the block this slot held
         if (recycle) finalize(slot, phase ^ 1, old);
         v += rows;
+        if (FP4 && v == slot_end && v < end) {
+            ++i_slot;
+            slot_end += a.rows_per_slot;
+            expert = a.ids[i_slot];
+        }
         if (++slot == a.stages) {
             slot = 0;
             phase ^= 1;
@@ -173,45 +177,70 @@ __device__ __forceinline__ void gemv_producer(const GemvParams &a, GemvHeader<CW
     }
 }
 
-// L2 prefetch of the first rows of this CTA's range (about one ring of
-// stages): packed codes, then the matching scale and zero rows, each range
-// trimmed inward to 16-byte boundaries so that it never leaves its tensor.
-__device__ __forceinline__ void gemv_prefetch_l2_range(const void *base, uint64_t lo, uint64_t hi) {
-    lo = (lo + 15) & ~uint64_t(15);
-    hi &= ~uint64_t(15);
-    const unsigned char *p = static_cast<const unsigned char *>(base);
-    for (uint64_t o = lo; o < hi; o += 32768) {
-        const uint64_t n = hi - o < 32768 ? hi - o : 32768;
-        prefetch_l2_bulk(p + o, static_cast<uint32_t>(n));
+// L2 prefetch of the first kGemvPrefetchStages blocks of this CTA's range:
+// the packed codes by bulk prefetch (from the producer lane, ahead of its own
+// stage copies), the scale and zero rows one 32-byte sector per instruction
+// from the consumer threads (idle until the previous kernel ends).  Ranges
+// are rounded inward to 16 bytes, so no address leaves its tensor.
+__device__ __forceinline__ int64_t gemv_prefetch_rows(const GemvParams &a, int64_t begin, int64_t end) {
+    int64_t rows = static_cast<int64_t>(kGemvPrefetchStages) * a.RB;
+    return rows < end - begin ? rows : end - begin;
+}
+
+__device__ __forceinline__ void gemv_prefetch_codes(const GemvParams &a, int64_t begin, int64_t end) {
+    const int64_t rows = gemv_prefetch_rows(a, begin, end);
+    const int64_t half_k = a.K >> 1;
+    const unsigned char *p = a.qw + begin * half_k;
+    for (int64_t o = 0; o < rows * half_k; o += 32768) {
+        const int64_t n = rows * half_k - o < 32768 ? rows * half_k - o : 32768;
+        prefetch_l2_bulk(p + o, static_cast<uint32_t>(n));  // half_k % 64 == 0: aligned, whole
     }
 }
 
-__device__ __forceinline__ void gemv_prefetch_l2(const GemvParams &a, int64_t begin, int64_t end) {
-    const int64_t half_k = a.K >> 1;
-    int64_t rows = static_cast<int64_t>(a.stages) * a.RB;
-    if (rows > end - begin) rows = end - begin;
-    if (rows <= 0) return;
-    gemv_prefetch_l2_range(a.qw, begin * half_k, (begin + rows) * half_k);
+__device__ __forceinline__ void gemv_prefetch_range(const void *base, uint64_t lo, uint64_t hi, int tid,
+                                                    int nthreads) {
+    lo = (lo + 15) & ~uint64_t(15);
+    hi &= ~uint64_t(15);
+    const unsigned char *p = static_cast<const unsigned char *>(base);
+    for (uint64_t o = lo + static_cast<uint64_t>(tid) * 32; o < hi; o += static_cast<uint64_t>(nthreads) * 32)
+        prefetch_l2_line(p + o);
+}
+
+__device__ __forceinline__ void gemv_prefetch_groups(const GemvParams &a, int64_t begin, int64_t end, int tid,
+                                                     int nthreads) {
+    const int64_t rows = gemv_prefetch_rows(a, begin, end);
     const uint64_t g0 = static_cast<uint64_t>(begin) * a.G * 2, g1 = static_cast<uint64_t>(begin + rows) * a.G * 2;
-    gemv_prefetch_l2_range(a.s, g0, g1);
-    gemv_prefetch_l2_range(a.z, g0, g1);
+    gemv_prefetch_range(a.s, g0, g1, tid, nthreads);
+    gemv_prefetch_range(a.z, g0, g1, tid, nthreads);
 }
 
 // Activation conversion, once per CTA, one 32-element unit per consumer
-// thread (units u = K/32 of them).  Shared-memory layout at xs: [K/32][16]
-// words of converted pairs, then per scale block a float2 (xsum, pw).
-//  INT4: scale block = one 128-element group (4 units, 4 neighbouring lanes
-//        agree on the group exponent through shuffles; K % 128 == 0 makes
-//        every group whole); xsum = sum of the group's x_int.
-//  FP4:  scale block = the unit; (0, pw).
+// thread (U = K/32 units; INT4 has U % 4 == 0).  Shared-memory layout at xs, as uint4 "planes" laid
+// out so that the threads' later register loads are free of bank conflicts:
+//  INT4: plane p = 4s + i (s: unit within the 128-element group, i: quarter
+//        of the unit's 16 words) holds Gp = G rounded up to even entries, one
+//        per group; per group a float2 (xsum, pw) follows at xs + 64U + 256.
+//        Four neighbouring lanes (the group's units; K % 128 == 0 keeps every
+//        group whole) agree on the group exponent through shuffles.
+//  FP4:  plane i holds U entries, one per unit; per unit a float2 (0, pw).
+__device__ __forceinline__ int gemv_x_gp(int G) { return (G + 1) & ~1; }
+__device__ __forceinline__ int gemv_x_consts(int K) { return (K >> 5) * 64 + 256; }
+
 template <bool FP4, int CW>
 __device__ __forceinline__ void gemv_convert_x(const GemvParams &a, unsigned char *xs, int warp, int lane) {
-    uint32_t *xw = reinterpret_cast<uint32_t *>(xs);
+    uint4 *xw = reinterpret_cast<uint4 *>(xs);
     const int units = a.K >> 5;
-    float2 *xc = reinterpret_cast<float2 *>(xs + units * 64);
+    const int gp = gemv_x_gp(a.G);
+    float2 *xc = reinterpret_cast<float2 *>(xs + gemv_x_consts(a.K));
+    // Every CTA reads the same few KB at the same moment; starting each CTA at
+    // a different group (a rotation by whole groups, so that the four lanes
+    // of a group stay together) spreads the requests over the L2 slices.
+    const int rot = FP4 ? static_cast<int>((blockIdx.x * 7u) % static_cast<unsigned>(units))
+                        : 4 * static_cast<int>((blockIdx.x * 7u) % static_cast<unsigned>(units >> 2));
     for (int u0 = warp * 32; u0 < units; u0 += CW * 32) {  // warp-uniform
-        const int u = u0 + lane;
-        const bool ok = u < units;
+        const bool ok = u0 + lane < units;
+        int u = u0 + lane + rot;
+        if (u >= units) u -= units;
         uint32_t xb[16], w[16];
         if (ok) {
             load_x_unit(a.x + 32 * u, xb);
@@ -233,9 +262,12 @@ __device__ __forceinline__ void gemv_convert_x(const GemvParams &a, unsigned cha
             c = make_float2(static_cast<float>(sum), pow2f(e - 14));  // |sum| < 2^23: exact
         }
         if (ok) {
-            uint4 *dst = reinterpret_cast<uint4 *>(xw + 16 * u);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+            for (int i = 0; i < 4; ++i) {
+                const uint4 q4 = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                if (FP4) xw[i * units + u] = q4;
+                else xw[(4 * (u & 3) + i) * gp + (u >> 2)] = q4;
+            }
             if (FP4) xc[u] = c;
             else if ((u & 3) == 0) xc[u >> 2] = c;
         }
@@ -269,21 +301,21 @@ __device__ __forceinline__ void gemv_consume_int4(const GemvParams &a, GemvHeade
     const bool valid = g < a.G;
     const int gs = valid ? g : 0;
     const int rot = (g >> 1) & 3;
-    const uint32_t *xw = reinterpret_cast<const uint32_t *>(xs);
+    const uint4 *xw = reinterpret_cast<const uint4 *>(xs);
+    const int gp = gemv_x_gp(a.G);
     uint32_t xr[4][16];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(xw + 16 * (4 * gs + ((q + rot) & 3)));
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const uint4 v4 = src[i];
+            const uint4 v4 = xw[(4 * ((q + rot) & 3) + i) * gp + gs];
             xr[q][4 * i] = v4.x;
             xr[q][4 * i + 1] = v4.y;
             xr[q][4 * i + 2] = v4.z;
             xr[q][4 * i + 3] = v4.w;
         }
     }
-    const float2 xc = reinterpret_cast<const float2 *>(xs + (a.K >> 5) * 64)[gs];
+    const float2 xc = reinterpret_cast<const float2 *>(xs + gemv_x_consts(a.K))[gs];
     const float xsum = xc.x, pw = valid ? xc.y : 0.0f;
     const int half_k = a.K >> 1;
 
@@ -354,8 +386,8 @@ __device__ __forceinline__ void gemv_consume_fp4(const GemvParams &a, GemvHeader
     const int team = threadIdx.x / TT;
     const int j = threadIdx.x % TT;
     const int units = a.K >> 5;
-    const uint32_t *xw = reinterpret_cast<const uint32_t *>(xs);
-    const float2 *xc = reinterpret_cast<const float2 *>(xs + units * 64);
+    const uint4 *xw = reinterpret_cast<const uint4 *>(xs);
+    const float2 *xc = reinterpret_cast<const float2 *>(xs + gemv_x_consts(a.K));
     uint32_t xr[UPT][16];
     float pw[UPT];
     bool valid[UPT];
@@ -364,10 +396,9 @@ __device__ __forceinline__ void gemv_consume_fp4(const GemvParams &a, GemvHeader
         const int u = j + i * TT;
         valid[i] = u < units;
         const int us = valid[i] ? u : 0;
-        const uint4 *src = reinterpret_cast<const uint4 *>(xw + 16 * us);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const uint4 v4 = src[q];
+            const uint4 v4 = xw[q * units + us];
             xr[i][4 * q] = v4.x;
             xr[i][4 * q + 1] = v4.y;
             xr[i][4 * q + 2] = v4.z;
@@ -430,13 +461,15 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_stream_kernel(const Gem
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // This CTA's contiguous range of virtual rows.
-    const int64_t begin = blockIdx.x * a.V / gridDim.x;
-    const int64_t end = (blockIdx.x + 1) * a.V / gridDim.x;
+    // This CTA's contiguous range of virtual rows: V = q * grid + r rows,
+    // the first r CTAs take one more (q and r come from the host).
+    const int64_t b = blockIdx.x;
+    const int64_t begin = b * a.rows_q + (b < a.rows_r ? b : a.rows_r);
+    const int64_t end = begin + a.rows_q + (b < a.rows_r ? 1 : 0);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < a.stages; ++i) {
-            mbar_init(&h.full[i], 1);  // producer lane 0, plus the stage's transaction bytes
+            mbar_init(&h.full[i], 33);  // producer lane 0 (+ weight bytes) and its 32 cp.async lanes
             mbar_init(&h.empty[i], CW);
         }
         fence_barrier_init();
@@ -448,9 +481,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_stream_kernel(const Gem
     pdl_launch_dependents();
 
     if (warp == CW) {
-        // The packed weights, scales and zeros are read-only for the whole
-        // stream; only the L2 prefetch runs before the previous kernel ends.
-        if (!FP4 && lane == 0) gemv_prefetch_l2(a, begin, end);
+        if (!FP4 && lane == 0) gemv_prefetch_codes(a, begin, end);
         // The weights copied into shared memory, the expert ids and the
         // output follow the stream order.
         pdl_wait();
@@ -458,10 +489,12 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_stream_kernel(const Gem
         return;
     }
 
-    // The activation follows the stream order too.  The consumers convert it
-    // once per CTA into shared memory (plain loads: the bulk-copy engine is
-    // busy with weights), then each thread copies the part it owns into
-    // registers.
+    // Until the previous kernel ends only the L2 prefetch of this CTA's first
+    // weights may run (it cannot hide a later write: L2 is the point of
+    // coherence).  The activation follows the stream order: the consumers
+    // convert it once per CTA into shared memory, then each thread copies the
+    // part it owns into registers.
+    if (!FP4) gemv_prefetch_groups(a, begin, end, threadIdx.x, CW * 32);
     pdl_wait();
     gemv_convert_x<FP4, CW>(a, smem + a.x_off, warp, lane);
     named_bar_sync(1, CW * 32);
@@ -506,7 +539,7 @@ cudaError_t gemv_launch(GemvParams a, cudaStream_t st, int device, int num_sms, 
     auto kern = gemv_stream_kernel<FP4, CW, TT, UPT, RPT>;
     const int header = (static_cast<int>(sizeof(GemvHeader<CW, RPT>)) + 127) & ~127;
     a.x_off = header;
-    a.stage_off = (a.x_off + (a.K / 32) * 72 + 1023) & ~1023;  // converted units: 64 B of pairs + (xsum, pw)
+    a.stage_off = (a.x_off + (a.K / 32) * 72 + 256 + 1023) & ~1023;  // converted x: planes, then (xsum, pw)
     int stages = (max_smem - a.stage_off) / a.stage_bytes;
     if (stages > kGemvMaxStages) stages = kGemvMaxStages;
     if (stages < 2) return cudaErrorInvalidValue;
@@ -523,6 +556,8 @@ cudaError_t gemv_launch(GemvParams a, cudaStream_t st, int device, int num_sms, 
     const int64_t max_ctas = (a.V + 1) / 2;  // at least two rows each
     if (ctas > max_ctas) ctas = max_ctas;
     if (ctas < 1) ctas = 1;
+    a.rows_q = a.V / ctas;
+    a.rows_r = a.V % ctas;
     // Programmatic stream serialisation: this launch may begin while the
     // previous kernel of the stream finishes; the kernel waits for it
     // (griddepcontrol.wait) before touching x, y or the expert ids.
