@@ -83,9 +83,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // false (and records kDevTimeout) if it did not complete within the limit, or
 // at once if some wait of this device already timed out, so that a failing
 // launch winds down quickly instead of sitting out one limit per wait.
+// A barrier check is a dependent shared-memory round trip of roughly 150 SM
+// cycles even when the phase has completed, so the common case is a single
+// try_wait ahead of the loop.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
                                           unsigned int *status) {
     const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait(a, parity)) return true;
     // try_wait suspends the thread until the phase completes or a short
     // hardware time slice ends, so polling it costs no memory traffic; the
     // clock and the status word are consulted only between batches.
@@ -101,6 +105,32 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
         if (status && (*reinterpret_cast<volatile unsigned int *>(status) & kDevTimeout)) return false;
         if (global_timer_ns() - t0 > kWaitLimitNs) {
             if (status) atomicOr(status, kDevTimeout);
+            return false;
+        }
+    }
+}
+
+// Warp-wide bounded wait on up to 32 barriers at once: each lane names its
+// own barrier (or none, bar == nullptr) and parity, and every lane returns
+// once all of them have completed -- one barrier round trip for the whole
+// set instead of one per barrier.  All 32 lanes must call it together.
+// Returns false on timeout (every lane alike).
+__device__ __forceinline__ bool mbar_wait_lanes(uint64_t *bar, uint32_t parity, unsigned int *status) {
+    const uint32_t a = bar ? smem_u32(bar) : 0u;
+    bool done = (bar == nullptr) || mbar_try_wait(a, parity);
+    if (__all_sync(0xffffffffu, done)) return true;
+    const unsigned long long t0 = global_timer_ns();
+#pragma unroll 1
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 256; ++i) {
+            if (!done) done = mbar_try_wait(a, parity);
+            if (__all_sync(0xffffffffu, done)) return true;
+        }
+        const bool stop = (status && (*reinterpret_cast<volatile unsigned int *>(status) & kDevTimeout)) ||
+                          global_timer_ns() - t0 > kWaitLimitNs;
+        if (__any_sync(0xffffffffu, stop)) {
+            if (status && (threadIdx.x & 31) == 0) atomicOr(status, kDevTimeout);
             return false;
         }
     }

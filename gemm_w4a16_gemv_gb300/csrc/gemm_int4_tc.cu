@@ -155,26 +155,38 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
+        // the whole warp waits (one lane per barrier); lane 0 issues
+        const uint64_t pol = policy_evict_first();
         if (lane == 0) {
             tma_prefetch_desc(&tmW);
             tma_prefetch_desc(&tmX);
-            const uint64_t pol = policy_evict_first();
             const uint32_t szb = static_cast<uint32_t>(rows_n) * a.G * 2;
             mbar_arrive_expect_tx(&bar.szfull, 2 * szb);
             if (szb) {
                 bulk_g2s(smem + a.off_sz, a.s + static_cast<size_t>(n0) * a.G, szb, &bar.szfull, pol);
                 bulk_g2s(smem + a.off_sz + a.sz_bytes, a.z + static_cast<size_t>(n0) * a.G, szb, &bar.szfull, pol);
             }
-            int xs = 0, xph = 0;  // X stage and its phase
-            for (int g = 0; g < ngroups; ++g) {
-                if ((g & 1) == 0) {
-                    const int wb = g >> 1, ws = wb & 1;
-                    if (wb >= WS && !mbar_wait(&bar.wempty[ws], ((wb >> 1) - 1) & 1, a.status)) break;
+        }
+        int xs = 0, xph = 0;  // X stage and its phase
+        for (int g = 0; g < ngroups; ++g) {
+            const bool wload = (g & 1) == 0;
+            const int wb = g >> 1, ws = wb % WS;
+            uint64_t *wb_bar = nullptr;
+            uint32_t par = 0;
+            if (lane == 0 && wload && wb >= WS) {
+                wb_bar = &bar.wempty[ws];
+                par = ((wb / WS) - 1) & 1;
+            } else if (lane == 1 && g >= XP) {
+                wb_bar = &bar.xempty[xs];
+                par = xph ^ 1;
+            }
+            if (!mbar_wait_lanes(wb_bar, par, a.status)) break;
+            if (lane == 0) {
+                if (wload) {
                     mbar_arrive_expect_tx(&bar.wfull[ws], W_BYTES);
                     // rows past N (last and padding tiles) read as zeros
                     tma_load_2d(smem + a.off_w + ws * W_BYTES, &tmW, wb * 128, n0, &bar.wfull[ws]);
                 }
-                if (g >= XP && !mbar_wait(&bar.xempty[xs], xph ^ 1, a.status)) break;
                 mbar_arrive_expect_tx(&bar.xfull[xs], 2 * X_BYTES);  // both boxes, from all slices
                 unsigned char *dst = smem + OFF_X + xs * 2 * X_BYTES + static_cast<int>(crank) * xrows * 128;
                 const int row = m0 + static_cast<int>(crank) * xrows;
@@ -184,29 +196,40 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                     else
                         tma_load_2d(dst + h * X_BYTES, &tmX, g * GK + h * BK, row, &bar.xfull[xs]);
                 }
-                if (++xs == XP) {
-                    xs = 0;
-                    xph ^= 1;
-                }
+            }
+            __syncwarp();
+            if (++xs == XP) {
+                xs = 0;
+                xph ^= 1;
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_kind_f16(128, BM, 1u);  // BF16, M = 128 lanes, N = 128 rows of X
-            bool ok = true;
-            int xs = 0, xph = 0, db = 0, dph = 0;
-            for (int g = 0; g < ngroups; ++g) {
-                const int ap = g % AP;
-                if (g >= DB && !mbar_wait(&bar.accempty[db], dph ^ 1, a.status)) {
-                    ok = false;
-                    break;
-                }
-                if (!mbar_wait(&bar.aready[ap], (g / AP) & 1, a.status) || !mbar_wait(&bar.xfull[xs], xph, a.status)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
+        // the whole warp waits for the group's three conditions at once (one
+        // lane per barrier); lane 0 issues
+        constexpr uint32_t idesc = idesc_kind_f16(128, BM, 1u);  // BF16, M = 128 lanes, N = 128 rows of X
+        bool ok = true;
+        int xs = 0, xph = 0, db = 0, dph = 0;
+        for (int g = 0; g < ngroups; ++g) {
+            const int ap = g % AP;
+            uint64_t *wbar = nullptr;
+            uint32_t par = 0;
+            if (lane == 0) {
+                wbar = &bar.aready[ap];
+                par = (g / AP) & 1;
+            } else if (lane == 1) {
+                wbar = &bar.xfull[xs];
+                par = xph;
+            } else if (lane == 2 && g >= DB) {
+                wbar = &bar.accempty[db];
+                par = dph ^ 1;
+            }
+            if (!mbar_wait_lanes(wbar, par, a.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (lane == 0) {
                 const uint32_t t_acc = tmem + db * 128;
                 const uint32_t a_t = tmem + TM_A + ap * 64;
                 const uint32_t b_addr = smem_u32(smem + OFF_X + xs * 2 * X_BYTES);
@@ -219,19 +242,20 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                 else
                     umma_commit(&bar.xempty[xs]);
                 umma_commit(&bar.accfull[db]);
-                if (++xs == XP) {
-                    xs = 0;
-                    xph ^= 1;
-                }
-                if (++db == DB) {
-                    db = 0;
-                    dph ^= 1;
-                }
             }
-            // Only after a timeout: one more commit so that the epilogue's wait
-            // also ends once the MMAs already issued have completed.
-            if (!ok) umma_commit(&bar.accfull[db]);
+            __syncwarp();
+            if (++xs == XP) {
+                xs = 0;
+                xph ^= 1;
+            }
+            if (++db == DB) {
+                db = 0;
+                dph ^= 1;
+            }
         }
+        // Only after a timeout: one more commit so that the epilogue's wait
+        // also ends once the MMAs already issued have completed.
+        if (!ok && lane == 0) umma_commit(&bar.accfull[db]);
         __syncwarp();
         mbar_wait(&bar.done, 0, a.status);
         tc_fence_after();
@@ -244,16 +268,23 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         const uint32_t t_lane = static_cast<uint32_t>(q * 32) << 16;
         for (int g = 0; g < ngroups; ++g) {
             const int ap = g % AP;
-            const int wb = g >> 1, ws = wb & 1, half = g & 1;
-            if (half == 0 && !mbar_wait(&bar.wfull[ws], (wb >> 1) & 1, a.status)) break;
-            // operand stage ap is free once the MMAs of group g - AP are done,
-            // which that group's X "empty" barrier records (it cannot run a
-            // phase ahead: its next phase needs this builder's stage for group
+            const int wb = g >> 1, ws = wb % WS, half = g & 1;
+            // lane 0: the packed codes (every other group); lane 1: operand
+            // stage ap is free once the MMAs of group g - AP are done, which
+            // that group's X "empty" barrier records (it cannot run a phase
+            // ahead: its next phase needs this builder's stage for group
             // g - AP + XP >= g)
-            if (g >= AP) {
+            uint64_t *wbar = nullptr;
+            uint32_t par = 0;
+            if (lane == 0 && half == 0) {
+                wbar = &bar.wfull[ws];
+                par = (wb / WS) & 1;
+            } else if (lane == 1 && g >= AP) {
                 const int pg = g - AP;
-                if (!mbar_wait(&bar.xempty[pg % XP], (pg / XP) & 1, a.status)) break;
+                wbar = &bar.xempty[pg % XP];
+                par = (pg / XP) & 1;
             }
+            if (!mbar_wait_lanes(wbar, par, a.status)) break;
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 uint32_t cols[32];
