@@ -32,8 +32,9 @@
 //    L2 serves every X tile C times fewer; the grid is padded to a multiple
 //    of C with CTAs that carry no weight rows (they only share the loads);
 //  * warp 0 (one lane): one bulk copy each of the tile's scale and zero rows;
-//    per group its X rows (two TMA boxes, 128-byte swizzle, multicast); every
-//    two groups the packed codes of the tile's rows, 128 bytes each (TMA);
+//    per group its X rows (two TMA boxes, 128-byte swizzle, multicast);
+//  * warp 2 (one lane): every two groups the packed codes of the tile's rows,
+//    128 bytes each (TMA), on a ring of its own;
 //  * warps 8-11 (TMEM lane quarters 0-3): per group, thread (q, i) turns the
 //    128 codes of weight row 28 q + i into 64 columns of BF16 pairs 128 + q
 //    (byte permutes) and stores them into the group's TMEM operand stage;
@@ -64,7 +65,7 @@ constexpr int BM = 128;               // X rows per tile (the MMA's N)
 constexpr int BK = 64;                // one TMA box of X (128 bytes of BF16 per row)
 constexpr int GK = 128;               // K per group = per hand-off
 constexpr int MAX_XP = 5;             // X ring depth in groups (runtime, from shared memory)
-constexpr int WS = 2;                 // packed-code ring (each load: two groups)
+constexpr int WS = 3;                 // packed-code ring (each load: two groups)
 constexpr int AP = 2;                 // TMEM operand stages (64 columns each)
 constexpr int DB = 3;                 // TMEM accumulators (128 columns each)
 constexpr int X_BYTES = BM * BK * 2;  // 16 KB: one box; a group takes two
@@ -169,24 +170,8 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         }
         int xs = 0, xph = 0;  // X stage and its phase
         for (int g = 0; g < ngroups; ++g) {
-            const bool wload = (g & 1) == 0;
-            const int wb = g >> 1, ws = wb % WS;
-            uint64_t *wb_bar = nullptr;
-            uint32_t par = 0;
-            if (lane == 0 && wload && wb >= WS) {
-                wb_bar = &bar.wempty[ws];
-                par = ((wb / WS) - 1) & 1;
-            } else if (lane == 1 && g >= XP) {
-                wb_bar = &bar.xempty[xs];
-                par = xph ^ 1;
-            }
-            if (!mbar_wait_lanes(wb_bar, par, a.status)) break;
+            if (g >= XP && !mbar_wait(&bar.xempty[xs], xph ^ 1, a.status)) break;
             if (lane == 0) {
-                if (wload) {
-                    mbar_arrive_expect_tx(&bar.wfull[ws], W_BYTES);
-                    // rows past N (last and padding tiles) read as zeros
-                    tma_load_2d(smem + a.off_w + ws * W_BYTES, &tmW, wb * 128, n0, &bar.wfull[ws]);
-                }
                 mbar_arrive_expect_tx(&bar.xfull[xs], 2 * X_BYTES);  // both boxes, from all slices
                 unsigned char *dst = smem + OFF_X + xs * 2 * X_BYTES + static_cast<int>(crank) * xrows * 128;
                 const int row = m0 + static_cast<int>(crank) * xrows;
@@ -201,6 +186,20 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             if (++xs == XP) {
                 xs = 0;
                 xph ^= 1;
+            }
+        }
+    } else if (warp == 2) {
+        // ---------------------------------------- packed-code TMA producer
+        // its own ring, so the codes (from HBM) are requested as early as the
+        // ring allows, independently of the X ring's pace
+        if (lane == 0) {
+            const int nwb = (ngroups + 1) / 2;
+            for (int wb = 0; wb < nwb; ++wb) {
+                const int ws = wb % WS;
+                if (wb >= WS && !mbar_wait(&bar.wempty[ws], ((wb / WS) - 1) & 1, a.status)) break;
+                mbar_arrive_expect_tx(&bar.wfull[ws], W_BYTES);
+                // rows past N (last and padding tiles) read as zeros
+                tma_load_2d(smem + a.off_w + ws * W_BYTES, &tmW, wb * 128, n0, &bar.wfull[ws]);
             }
         }
     } else if (warp == 1) {
