@@ -11,9 +11,10 @@
 
 namespace {
 
-// Sticky per-device status word.  A __device__ variable exists once per
-// device context; its address is looked up per device at first use.
-__device__ unsigned int g_status;
+// Per-device control block (see common.cuh): sticky status word, test-only
+// injection flags, wait limit.  A __device__ variable exists once per device
+// context; its address is looked up per device at first use.
+__device__ __align__(16) unsigned int g_status[4];
 
 thread_local char g_err[512] = "";
 
@@ -173,17 +174,28 @@ int w4a16_check_device_error(void *stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(W4A16_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
     unsigned int v = 0;
-    e = cudaMemcpyFromSymbol(&v, g_status, sizeof v);
+    e = cudaMemcpyFromSymbol(&v, g_status, sizeof v, 0);
     if (e != cudaSuccess) return fail(W4A16_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
     if (v != 0) {
         const unsigned int zero = 0;
-        e = cudaMemcpyToSymbol(g_status, &zero, sizeof zero);
+        e = cudaMemcpyToSymbol(g_status, &zero, sizeof zero, 0);
         if (e != cudaSuccess) return fail(W4A16_ERR_CUDA, "status clear: %s", cudaGetErrorString(e));
     }
     if (v & w4::kDevTimeout) return fail(W4A16_ERR_TIMEOUT, "a device pipeline wait timed out");
     if (v & w4::kDevBadExpert) return fail(W4A16_ERR_DEVICE, "an expert id was outside [0, E)");
-    if (v & w4::kDevRange)
-        return fail(W4A16_ERR_DEVICE, "a w4a16_gemm activation was outside the FP16 range (|x| >= 65520)");
+    return ok();
+}
+
+int w4a16_debug_inject(unsigned int flags, unsigned long long wait_limit_ns) {
+    w4::DeviceInfo dev;
+    unsigned int *status;
+    if (int r = device_state(dev, status)) return r;
+    cudaError_t e = cudaDeviceSynchronize();  // no launch of this device may still read the block
+    if (e != cudaSuccess) return fail(W4A16_ERR_CUDA, "device synchronize: %s", cudaGetErrorString(e));
+    unsigned int v[3] = {flags, static_cast<unsigned int>(wait_limit_ns & 0xFFFFFFFFull),
+                         static_cast<unsigned int>(wait_limit_ns >> 32)};
+    e = cudaMemcpyToSymbol(g_status, v, sizeof v, sizeof(unsigned int));
+    if (e != cudaSuccess) return fail(W4A16_ERR_CUDA, "control write: %s", cudaGetErrorString(e));
     return ok();
 }
 

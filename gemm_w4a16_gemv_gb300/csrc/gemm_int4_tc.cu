@@ -171,7 +171,9 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         int xs = 0, xph = 0;  // X stage and its phase
         for (int g = 0; g < ngroups; ++g) {
             if (g >= XP && !mbar_wait(&bar.xempty[xs], xph ^ 1, a.status)) break;
-            if (lane == 0) {
+            // test-only injection: leave the first X stage unsignalled, so that
+            // the waits run out and the launch ends with the timeout status
+            if (lane == 0 && !(g == 0 && injected(a.status, kInjectSkipFirstStage))) {
                 mbar_arrive_expect_tx(&bar.xfull[xs], 2 * X_BYTES);  // both boxes, from all slices
                 unsigned char *dst = smem + OFF_X + xs * 2 * X_BYTES + static_cast<int>(crank) * xrows * 128;
                 const int row = m0 + static_cast<int>(crank) * xrows;

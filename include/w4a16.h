@@ -125,6 +125,20 @@ int w4a16_dequant(int fmt, const uint8_t *qw, const uint16_t *s,
  */
 int w4a16_check_device_error(void *stream);
 
+/*
+ * Test-only failure injection (the library's bounded-wait path, exercised
+ * without faulting the GPU).  Synchronises the device, then sets for this
+ * device:
+ *   flags          0: normal operation;  1: every w4a16_gemv, fp4_moe_gemv and
+ *                  w4a16_gemm launch leaves the first stage of its pipeline
+ *                  unsignalled, so its waits run out; the launch returns
+ *                  early with a garbage output and w4a16_check_device_error
+ *                  reports W4A16_ERR_TIMEOUT (the context stays usable);
+ *   wait_limit_ns  limit of every pipeline wait (0: the default, 2 s).
+ * Not for production use.  Returns W4A16_OK or W4A16_ERR_CUDA.
+ */
+int w4a16_debug_inject(unsigned int flags, unsigned long long wait_limit_ns);
+
 /* Message for the last failed call on this host thread ("" if none). */
 const char *w4a16_last_error_string(void);
 

@@ -29,7 +29,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("w4a16_gemv", "w4a16_gemm", "fp4_moe_gemv", "w4a16_dequant",
-              "w4a16_check_device_error", "w4a16_last_error_string", "w4a16_version"):
+              "w4a16_check_device_error", "w4a16_last_error_string", "w4a16_version",
+              "w4a16_debug_inject"):
         assert n in names
 
 
