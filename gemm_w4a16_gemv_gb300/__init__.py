@@ -21,7 +21,7 @@ import torch
 __all__ = [
     "w4a16_gemv", "w4a16_gemm", "fp4_moe_gemv", "w4a16_dequant",
     "w4a16_check_device_error", "w4a16_last_error_string", "w4a16_version",
-    "w4a16_debug_inject", "INJECT_SKIP_FIRST_STAGE",
+    "w4a16_debug_inject", "INJECT_STALL_PIPELINE",
     "library_path", "W4A16Error", "STATUS", "FMT_INT4", "FMT_FP4",
     "OUT_F32", "OUT_BF16",
 ]
@@ -46,7 +46,7 @@ SIGNATURES = {
     "fp4_moe_gemv": ([_P, _P, _P, _P, _INT, _P, _I64, _I64, _I64, _INT, _P], _INT),
     "w4a16_dequant": ([_INT, _P, _P, _P, _P, _INT, _I64, _I64, _INT, _P], _INT),
     "w4a16_check_device_error": ([_P], _INT),
-    "w4a16_debug_inject": ([ctypes.c_uint, ctypes.c_ulonglong], _INT),
+    "w4a16_debug_inject": ([ctypes.c_uint], _INT),
     "w4a16_last_error_string": ([], ctypes.c_char_p),
     "w4a16_version": ([], _INT),
 }
@@ -185,15 +185,15 @@ def w4a16_check_device_error(stream=None) -> int:
     return int(lib().w4a16_check_device_error(_stream(stream)))
 
 
-INJECT_SKIP_FIRST_STAGE = 1
+INJECT_STALL_PIPELINE = 1
 
 
-def w4a16_debug_inject(flags: int = 0, wait_limit_ns: int = 0) -> None:
-    """Test-only: make every later GEMV/MoE/GEMM launch on this device skip the
-    first stage of its pipeline (flags=1), so that its bounded waits run out
-    after wait_limit_ns (0: the 2 s default) and the device status reports a
-    timeout; flags=0 restores normal operation."""
-    _check(lib().w4a16_debug_inject(int(flags), int(wait_limit_ns)))
+def w4a16_debug_inject(flags: int = 0) -> None:
+    """Test-only: make every later GEMV/MoE/GEMM launch on this device issue
+    no stage of its pipeline (flags=1), so that its bounded waits run out
+    (after about 2 s) and the device status reports a timeout; flags=0
+    restores normal operation."""
+    _check(lib().w4a16_debug_inject(int(flags)))
 
 
 def w4a16_last_error_string() -> str:

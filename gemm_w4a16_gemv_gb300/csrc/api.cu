@@ -11,10 +11,10 @@
 
 namespace {
 
-// Per-device control block (see common.cuh): sticky status word, test-only
-// injection flags, wait limit.  A __device__ variable exists once per device
-// context; its address is looked up per device at first use.
-__device__ __align__(16) unsigned int g_status[4];
+// Sticky per-device status word (bits in common.cuh).  A __device__ variable
+// exists once per device context; its address is looked up per device at
+// first use.
+__device__ unsigned int g_status;
 
 thread_local char g_err[512] = "";
 
@@ -35,13 +35,13 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 struct DevCache {
     bool ready;
-    w4::DeviceInfo info;
+    w4::DeviceInfo info;  // info.inject: this device's injection flags
     unsigned int *status;
 };
 DevCache g_dev[64];
 
 // Current device's info and status-word address (looked up once per device).
-int device_state(w4::DeviceInfo &info, unsigned int *&status) {
+int device_state(w4::DeviceInfo &info, unsigned int *&status, DevCache **cache = nullptr) {
     int d = 0;
     cudaError_t e = cudaGetDevice(&d);
     if (e != cudaSuccess) return fail(W4A16_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
@@ -62,6 +62,7 @@ int device_state(w4::DeviceInfo &info, unsigned int *&status) {
     }
     info = c.info;
     status = c.status;
+    if (cache) *cache = &c;
     return W4A16_OK;
 }
 
@@ -174,11 +175,11 @@ int w4a16_check_device_error(void *stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(W4A16_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
     unsigned int v = 0;
-    e = cudaMemcpyFromSymbol(&v, g_status, sizeof v, 0);
+    e = cudaMemcpyFromSymbol(&v, g_status, sizeof v);
     if (e != cudaSuccess) return fail(W4A16_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
     if (v != 0) {
         const unsigned int zero = 0;
-        e = cudaMemcpyToSymbol(g_status, &zero, sizeof zero, 0);
+        e = cudaMemcpyToSymbol(g_status, &zero, sizeof zero);
         if (e != cudaSuccess) return fail(W4A16_ERR_CUDA, "status clear: %s", cudaGetErrorString(e));
     }
     if (v & w4::kDevTimeout) return fail(W4A16_ERR_TIMEOUT, "a device pipeline wait timed out");
@@ -186,16 +187,16 @@ int w4a16_check_device_error(void *stream) {
     return ok();
 }
 
-int w4a16_debug_inject(unsigned int flags, unsigned long long wait_limit_ns) {
+int w4a16_debug_inject(unsigned int flags) {
     w4::DeviceInfo dev;
     unsigned int *status;
-    if (int r = device_state(dev, status)) return r;
-    cudaError_t e = cudaDeviceSynchronize();  // no launch of this device may still read the block
-    if (e != cudaSuccess) return fail(W4A16_ERR_CUDA, "device synchronize: %s", cudaGetErrorString(e));
-    unsigned int v[3] = {flags, static_cast<unsigned int>(wait_limit_ns & 0xFFFFFFFFull),
-                         static_cast<unsigned int>(wait_limit_ns >> 32)};
-    e = cudaMemcpyToSymbol(g_status, v, sizeof v, sizeof(unsigned int));
-    if (e != cudaSuccess) return fail(W4A16_ERR_CUDA, "control write: %s", cudaGetErrorString(e));
+    DevCache *c = nullptr;
+    if (int r = device_state(dev, status, &c)) return r;
+    if (flags & ~static_cast<unsigned int>(w4::kInjectStallPipeline))
+        return fail(W4A16_ERR_INVALID_ARG, "unknown injection flags 0x%x", flags);
+    // the flags travel as a kernel argument of later launches: the normal
+    // path reads no memory for them
+    c->info.inject = flags;
     return ok();
 }
 

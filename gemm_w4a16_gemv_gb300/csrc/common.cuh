@@ -9,33 +9,20 @@
 
 namespace w4 {
 
-// Per-device control block that every kernel receives as `status`
-// (unsigned int[4], 16-byte aligned):
-//   status[0]     sticky status bits written by kernels (never by traps);
-//   status[1]     test-only injection flags (normally 0);
-//   status[2..3]  wait limit in ns as a 64-bit value (0: the default).
+// Bits of the per-device status word written by kernels (never by traps).
 enum : unsigned int {
     kDevTimeout = 1u,    // a pipeline wait exceeded its time limit
     kDevBadExpert = 2u,  // an expert id outside [0, E)
 };
-// Injection flags (status[1]): the pipelines skip their first stage, so that
-// their waits run out -- the bounded-wait path, exercised without a fault.
+// Test-only injection flags, passed to the kernels as an argument: with
+// kInjectStallPipeline the producers issue nothing, so that the waits on
+// them run out -- the bounded-wait path, exercised without a fault.
 enum : unsigned int {
-    kInjectSkipFirstStage = 1u,
+    kInjectStallPipeline = 1u,
 };
 
-// Default wait limit for every mbarrier spin, in nanoseconds of %globaltimer.
+// Wait limit for every mbarrier spin, in nanoseconds of %globaltimer.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
-
-__device__ __forceinline__ unsigned long long wait_limit_ns(const unsigned int *status) {
-    if (!status) return kWaitLimitNs;
-    const unsigned long long v = *reinterpret_cast<const volatile unsigned long long *>(status + 2);
-    return v ? v : kWaitLimitNs;
-}
-
-__device__ __forceinline__ bool injected(const unsigned int *status, unsigned int flag) {
-    return status && (*reinterpret_cast<const volatile unsigned int *>(status + 1) & flag);
-}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -115,14 +102,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
     for (int i = 0; i < 1024; ++i)
         if (mbar_try_wait(a, parity)) return true;
     const unsigned long long t0 = global_timer_ns();
-    const unsigned long long limit = wait_limit_ns(status);
 #pragma unroll 1
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 1024; ++i)
             if (mbar_try_wait(a, parity)) return true;
         if (status && (*reinterpret_cast<volatile unsigned int *>(status) & kDevTimeout)) return false;
-        if (global_timer_ns() - t0 > limit) {
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
             if (status) atomicOr(status, kDevTimeout);
             return false;
         }
@@ -139,7 +125,6 @@ __device__ __forceinline__ bool mbar_wait_lanes(uint64_t *bar, uint32_t parity, 
     bool done = (bar == nullptr) || mbar_try_wait(a, parity);
     if (__all_sync(0xffffffffu, done)) return true;
     const unsigned long long t0 = global_timer_ns();
-    const unsigned long long limit = wait_limit_ns(status);
 #pragma unroll 1
     while (true) {
 #pragma unroll 1
@@ -148,7 +133,7 @@ __device__ __forceinline__ bool mbar_wait_lanes(uint64_t *bar, uint32_t parity, 
             if (__all_sync(0xffffffffu, done)) return true;
         }
         const bool stop = (status && (*reinterpret_cast<volatile unsigned int *>(status) & kDevTimeout)) ||
-                          global_timer_ns() - t0 > limit;
+                          global_timer_ns() - t0 > kWaitLimitNs;
         if (__any_sync(0xffffffffu, stop)) {
             if (status && (threadIdx.x & 31) == 0) atomicOr(status, kDevTimeout);
             return false;

@@ -20,6 +20,7 @@ cudaError_t launch_gemv_int4(const uint16_t *x, const uint8_t *qw, const uint16_
     a.ids = nullptr;
     a.y = y;
     a.status = status;
+    a.inject = dev.inject;
     a.rows_per_slot = N;
     a.V = N;
     a.E = 1;

@@ -58,6 +58,7 @@ struct GemvParams {
     int x_off;              // byte offset of the converted activation (K/32 * 72 + 256 bytes)
     int stage_bytes;        // 128-aligned
     int stage_off;          // byte offset of stage 0
+    unsigned int inject;    // test-only injection flags (0 normally), kept last
 };
 
 struct StageMeta {
@@ -134,10 +135,7 @@ __device__ __forceinline__ void gemv_producer(const GemvParams &a, GemvHeader<CW
         const uint64_t b0 = static_cast<uint64_t>(src_row) * a.G * 2;
         const uint64_t b1 = b0 + static_cast<uint64_t>(rows) * a.G * 2;
         const uint64_t lo16 = b0 & ~uint64_t(15);
-        // test-only injection: leave the first stage unsignalled, so that the
-        // consumers' waits run out and the launch ends with the timeout status
-        const bool skip = issued == 0 && injected(a.status, kInjectSkipFirstStage);
-        if (lane == 0 && !skip) {
+        if (lane == 0) {
             if (!ok) atomicOr(a.status, kDevBadExpert);
             h.meta[slot].vrow = v;
             h.meta[slot].rows = rows;
@@ -147,7 +145,7 @@ __device__ __forceinline__ void gemv_producer(const GemvParams &a, GemvHeader<CW
             mbar_arrive_expect_tx(&h.full[slot], wb);
             if (ok) bulk_g2s(st, a.qw + src_row * half_k, wb, &h.full[slot], pol);
         }
-        if (ok && !skip) {
+        if (ok) {
             const unsigned char *gs = reinterpret_cast<const unsigned char *>(a.s);
             const unsigned char *gz = reinterpret_cast<const unsigned char *>(a.z);
             for (uint64_t o = lo16 + 16 * static_cast<uint64_t>(lane); o < b1; o += 16 * 32) {
@@ -157,7 +155,7 @@ __device__ __forceinline__ void gemv_producer(const GemvParams &a, GemvHeader<CW
                 if (!FP4) cp_async_16_zfill(reinterpret_cast<unsigned char *>(sz) + (o - lo16), gz + o, n);
             }
         }
-        if (!skip) cp_async_arrive_noinc(&h.full[slot]);
+        cp_async_arrive_noinc(&h.full[slot]);
         // the next copy is in flight; now finish the block this slot held
         if (recycle) finalize(slot, phase ^ 1, old);
         v += rows;
@@ -488,7 +486,10 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_stream_kernel(const Gem
         // The weights copied into shared memory, the expert ids and the
         // output follow the stream order.
         pdl_wait();
-        gemv_producer<FP4, CW, TT, UPT, RPT>(a, h, stage0, begin, end, lane);
+        // test-only injection: no stage is ever issued, so the consumers'
+        // first waits run out and the launch ends with the timeout status
+        if (!(a.inject & kInjectStallPipeline))
+            gemv_producer<FP4, CW, TT, UPT, RPT>(a, h, stage0, begin, end, lane);
         return;
     }
 

@@ -11,6 +11,7 @@ struct DeviceInfo {
     int device;
     int num_sms;
     int max_smem_optin;
+    unsigned int inject;  // test-only injection flags (w4a16_debug_inject), normally 0
 };
 
 cudaError_t launch_dequant(int fmt, const uint8_t *qw, const uint16_t *s,

@@ -22,6 +22,7 @@ cudaError_t launch_moe_fp4(const uint16_t *x, const uint8_t *qw, const uint16_t 
     a.ids = ids;
     a.y = y;
     a.status = status;
+    a.inject = dev.inject;
     a.rows_per_slot = N;
     a.V = static_cast<int64_t>(topk) * N;
     a.E = E;

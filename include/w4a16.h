@@ -127,17 +127,19 @@ int w4a16_check_device_error(void *stream);
 
 /*
  * Test-only failure injection (the library's bounded-wait path, exercised
- * without faulting the GPU).  Synchronises the device, then sets for this
- * device:
- *   flags          0: normal operation;  1: every w4a16_gemv, fp4_moe_gemv and
- *                  w4a16_gemm launch leaves the first stage of its pipeline
- *                  unsignalled, so its waits run out; the launch returns
- *                  early with a garbage output and w4a16_check_device_error
- *                  reports W4A16_ERR_TIMEOUT (the context stays usable);
- *   wait_limit_ns  limit of every pipeline wait (0: the default, 2 s).
- * Not for production use.  Returns W4A16_OK or W4A16_ERR_CUDA.
+ * without faulting the GPU).  Sets this device's injection flags:
+ *   0  normal operation;
+ *   1  every later w4a16_gemv, fp4_moe_gemv and w4a16_gemm launch issues no
+ *      stage of its pipeline (the weight stages of the GEMVs, the activation
+ *      stages of the GEMM), so its waits run out after their limit (about
+ *      2 s); the launch then returns with an unspecified output and
+ *      w4a16_check_device_error reports W4A16_ERR_TIMEOUT (the context stays
+ *      usable).
+ * The flags are a host-side setting passed to each later launch (a CUDA
+ * graph keeps the flags it was captured with).  Not for production use.
+ * Returns W4A16_OK, or W4A16_ERR_INVALID_ARG for an unknown flag.
  */
-int w4a16_debug_inject(unsigned int flags, unsigned long long wait_limit_ns);
+int w4a16_debug_inject(unsigned int flags);
 
 /* Message for the last failed call on this host thread ("" if none). */
 const char *w4a16_last_error_string(void);
