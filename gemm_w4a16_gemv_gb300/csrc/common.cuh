@@ -84,6 +84,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread may sleep up to hint_ns
+// (woken when the phase completes) instead of returning after the default
+// short time slice, so a waiting warp leaves its issue slots to the others.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+template <uint32_t HINT>
+__device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity) {
+    return HINT ? mbar_try_wait_hint(bar, parity, HINT) : mbar_try_wait(bar, parity);
+}
+
 // Bounded wait for the phase with the given parity to complete.  Returns
 // false (and records kDevTimeout) if it did not complete within the limit, or
 // at once if some wait of this device already timed out, so that a failing
@@ -91,6 +111,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // A barrier check is a dependent shared-memory round trip of roughly 150 SM
 // cycles even when the phase has completed, so the common case is a single
 // try_wait ahead of the loop.
+// HINT (ns, 0: none) is the suspend-time hint of the polls after the first.
+template <uint32_t HINT = 0>
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
                                           unsigned int *status) {
     const uint32_t a = smem_u32(bar);
@@ -100,13 +122,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
     // clock and the status word are consulted only between batches.
 #pragma unroll 1
     for (int i = 0; i < 1024; ++i)
-        if (mbar_try_wait(a, parity)) return true;
+        if (mbar_poll<HINT>(a, parity)) return true;
     const unsigned long long t0 = global_timer_ns();
 #pragma unroll 1
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 1024; ++i)
-            if (mbar_try_wait(a, parity)) return true;
+            if (mbar_poll<HINT>(a, parity)) return true;
         if (status && (*reinterpret_cast<volatile unsigned int *>(status) & kDevTimeout)) return false;
         if (global_timer_ns() - t0 > kWaitLimitNs) {
             if (status) atomicOr(status, kDevTimeout);
@@ -120,6 +142,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
 // once all of them have completed -- one barrier round trip for the whole
 // set instead of one per barrier.  All 32 lanes must call it together.
 // Returns false on timeout (every lane alike).
+template <uint32_t HINT = 0>
 __device__ __forceinline__ bool mbar_wait_lanes(uint64_t *bar, uint32_t parity, unsigned int *status) {
     const uint32_t a = bar ? smem_u32(bar) : 0u;
     bool done = (bar == nullptr) || mbar_try_wait(a, parity);
@@ -129,7 +152,7 @@ __device__ __forceinline__ bool mbar_wait_lanes(uint64_t *bar, uint32_t parity, 
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 256; ++i) {
-            if (!done) done = mbar_try_wait(a, parity);
+            if (!done) done = mbar_poll<HINT>(a, parity);
             if (__all_sync(0xffffffffu, done)) return true;
         }
         const bool stop = (status && (*reinterpret_cast<volatile unsigned int *>(status) & kDevTimeout)) ||

@@ -5,22 +5,26 @@
 // dequantised weight tile never leaves the SM, so HBM sees only packed codes).
 //
 // The dequantisation is split into an exact part that feeds the tensor cores
-// and an affine part applied per group to the accumulator:
-//   sum_{k in g} X[m,k] (q - z) s = s * A_g[n,m] - s * (128 + z) * S_g[m]
-//   A_g[n,m] = sum_{k in g} (128 + q[n,k]) * X[m,k]    (BF16 x BF16 MMA)
+// and an affine part applied per group to the accumulator.  With
+// z_i = clamp(rint(z), 0, 15) and the residual z_r = z - z_i (zero whenever
+// z is an integer code, as GPTQ zero points are):
+//   sum_{k in g} X[m,k] (q - z) s = s * A_g[n,m] - s * z_r * S_g[m]
+//   A_g[n,m] = sum_{k in g} (q[n,k] - z_i) * X[m,k]    (BF16 x BF16 MMA)
 //   S_g[m]   = sum_{k in g} X[m,k]                      (same MMA: rows of ones)
-// 128 + q is an integer of at most 8 significant bits, so the weight operand
-// is an exact BF16 number and X enters as loaded; every product is exact and
-// all sums are binary32.
+// q - z_i is an integer in [-15, 15], so the weight operand is an exact BF16
+// number and X enters as loaded; every product is exact and all sums are
+// binary32.  When every z_r of a warp's rows is zero for a group (the
+// common case) the epilogue is one multiply-add per element; otherwise it
+// also folds in S_g.
 //
 // Operand placement.  The weights are the MMA's A operand and live in tensor
 // memory: in each 32-lane quarter of the 128 TMEM lanes, lanes 0-27 hold 28
 // weight rows and lanes 28-31 BF16 ones, whose accumulator rows give S_g (so
-// every epilogue warp finds S_g in its own lane 28 and broadcasts it with a
-// shuffle).  The activation tile is the B operand (N = 128 rows m of X) in
-// shared memory, loaded by TMA.  So shared memory carries only the X tiles
-// (written by TMA, read by the MMA) and the packed codes; the dequantised
-// weights go straight from registers to TMEM (tcgen05.st).
+// an epilogue warp that needs S_g finds it in its own lane 28 and broadcasts
+// it with a shuffle).  The activation tile is the B operand (N = 128 rows m
+// of X) in shared memory, loaded by TMA.  So shared memory carries only the X
+// tiles (written by TMA, read by the MMA) and the packed codes; the
+// dequantised weights go straight from registers to TMEM (tcgen05.st).
 //
 // Every hand-off is per group (128 K, two TMA boxes of 64): an mbarrier wait
 // costs about 200 SM cycles of latency on this part even when the phase has
@@ -36,20 +40,23 @@
 //  * warp 2 (one lane): every two groups the packed codes of the tile's rows,
 //    128 bytes each (TMA), on a ring of its own;
 //  * warps 8-11 (TMEM lane quarters 0-3): per group, thread (q, i) turns the
-//    128 codes of weight row 28 q + i into 64 columns of BF16 pairs 128 + q
-//    (byte permutes) and stores them into the group's TMEM operand stage;
-//    lanes 28-31 store ones;
-//  * warp 1 (one lane): per group waits for the operand stage and the X
-//    tile, issues 8 x tcgen05.mma (M=128, N=128, K=16, A from TMEM) into one
-//    of three accumulators and commits twice: to the X stage's barrier in
-//    every CTA of the cluster (which also frees the operand stage: its
-//    builders watch that barrier) and to the accumulator's;
-//  * warps 4-7 and 12-15: per group read the accumulator (warp w: TMEM lanes
-//    32 (w mod 4) .. +31, one half of the 128 columns), release it and fold
-//    y += s A_g - s (128 + z) S_g into registers; at the end round to BF16
-//    and store Y.
+//    128 codes of weight row 28 q + i into 64 columns of BF16 pairs q - z_i
+//    (byte permutes and one BF16 pair subtraction) and stores them into the
+//    group's TMEM operand stage; lanes 28-31 store ones;
+//  * warps 1 and 3 (one lane each) issue the MMAs of the even and the odd
+//    groups, so that one warp's barrier checks overlap the other's issue and
+//    the tensor pipe sees a steady stream: per group wait for the operand
+//    stage (one of four), the X tile and a free accumulator (one of two),
+//    issue 8 x tcgen05.mma (M=128, N=128, K=16, A from TMEM) and commit
+//    three times: to the X stage's barrier in every CTA of the cluster, to
+//    the operand stage's (local) and to the accumulator's;
+//  * warps 4-7 and 12-15: per group load the accumulator (warp w: TMEM lanes
+//    32 (w mod 4) .. +31, one half of the 128 columns) into registers,
+//    release it at once and fold y += s A_g (- s z_r S_g) into registers;
+//    at the end round to BF16 and store Y.
 // Every wait is bounded; on timeout the status word is set, each role still
-// performs the arrivals the others wait for, and TMEM is always released.
+// performs the arrivals the others wait for, and TMEM is released only after
+// every MMA issued has completed.
 #include <mutex>
 
 #include "common.cuh"
@@ -66,14 +73,20 @@ constexpr int BK = 64;                // one TMA box of X (128 bytes of BF16 per
 constexpr int GK = 128;               // K per group = per hand-off
 constexpr int MAX_XP = 5;             // X ring depth in groups (runtime, from shared memory)
 constexpr int WS = 3;                 // packed-code ring (each load: two groups)
-constexpr int AP = 2;                 // TMEM operand stages (64 columns each)
-constexpr int DB = 3;                 // TMEM accumulators (128 columns each)
+constexpr int AP = 4;                 // TMEM operand stages (64 columns each)
+constexpr int DB = 2;                 // TMEM accumulators (128 columns each)
 constexpr int X_BYTES = BM * BK * 2;  // 16 KB: one box; a group takes two
 constexpr int W_BYTES = BNW * 128;    // 14 KB packed codes, two groups
-constexpr int THREADS = 512;          // 16 warps (2-3 idle)
-constexpr int PREP_WARPS = 4;         // warps 8-11
+constexpr int THREADS = 640;          // 20 warps, five warpgroups
+constexpr int PREP_WARPS = 8;         // warps 8-11 and 16-19
 constexpr int EPI_WARPS = 8;          // warps 4-7, 12-15
 constexpr uint32_t TMEM_COLS = 512;
+constexpr int kRegSplit = 128 * (40 + 152 + 64 + 152 + 64);  // registers after the per-role split
+// Suspend-time hints (ns) of the waits' polls, per role (0: plain polls).
+constexpr uint32_t kHintProd = 0;     // X and packed-code producers
+constexpr uint32_t kHintMma = 0;      // MMA issuers
+constexpr uint32_t kHintBuild = 0;    // operand builders
+constexpr uint32_t kHintEpi = 0;      // epilogue
 constexpr uint32_t TM_A = DB * 128;   // operand stages after the accumulators
 constexpr uint32_t ONES = 0x3F803F80u;  // two BF16 1.0
 // layout: [X ring][W ring][s tile][z tile][barriers]
@@ -101,10 +114,12 @@ struct Barriers {
     uint64_t wfull[WS];       // packed codes landed (TMA tx bytes)
     uint64_t wempty[WS];      // packed codes read (operand builders)
     uint64_t aready[AP];      // TMEM operand stage written (operand builders)
+    uint64_t aempty[AP];      // MMAs done with the operand stage (commit, local)
     uint64_t accfull[DB];     // group accumulator complete (commit)
     uint64_t accempty[DB];    // group accumulator read (epilogue warps)
     uint64_t szfull;          // scale/zero tiles landed
-    uint64_t done;            // epilogue finished with TMEM
+    uint64_t done;            // epilogue and operand builders finished with TMEM
+    uint64_t drained;         // every MMA of both issuing warps completed (commits)
     uint32_t tmem_holder;
 };
 
@@ -135,13 +150,17 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             mbar_init(&bar.wfull[i], 1);
             mbar_init(&bar.wempty[i], PREP_WARPS);
         }
-        for (int i = 0; i < AP; ++i) mbar_init(&bar.aready[i], PREP_WARPS);
+        for (int i = 0; i < AP; ++i) {
+            mbar_init(&bar.aready[i], PREP_WARPS);
+            mbar_init(&bar.aempty[i], 1);
+        }
         for (int i = 0; i < DB; ++i) {
             mbar_init(&bar.accfull[i], 1);
             mbar_init(&bar.accempty[i], EPI_WARPS);
         }
         mbar_init(&bar.szfull, 1);
-        mbar_init(&bar.done, EPI_WARPS);
+        mbar_init(&bar.done, EPI_WARPS + PREP_WARPS);
+        mbar_init(&bar.drained, 2);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -157,7 +176,15 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     const uint16_t cmask = static_cast<uint16_t>((1u << a.csize) - 1u);
     const int xrows = BM / a.csize;  // X rows this CTA loads for the cluster
 
+    // Registers per warpgroup, set at the top of each role: the producers and
+    // MMA issuers (warps 0-3) need few; each epilogue thread (warps 4-7,
+    // 12-15) holds 64 running sums and a 64-column accumulator slice; the
+    // operand builders (8-11, 16-19) a 32-column slice.  128 threads x (40 +
+    // 152 + 64 + 152 + 64) = kRegSplit registers: the launcher checks that the
+    // block is launched with at least that many (a shortfall would leave
+    // setmaxnreg.inc waiting).
     if (warp == 0) {
+        reg_release<40>();
         // ------------------------------------------------------ TMA producer
         // the whole warp waits (one lane per barrier); lane 0 issues
         const uint64_t pol = policy_evict_first();
@@ -176,7 +203,7 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         // run out and the launch ends with the timeout status
         const int xgroups = (a.inject & kInjectStallPipeline) ? 0 : ngroups;
         for (int g = 0; g < xgroups; ++g) {
-            if (g >= XP && !mbar_wait(&bar.xempty[xs], xph ^ 1, a.status)) break;
+            if (g >= XP && !mbar_wait<kHintProd>(&bar.xempty[xs], xph ^ 1, a.status)) break;
             if (lane == 0) {
                 mbar_arrive_expect_tx(&bar.xfull[xs], 2 * X_BYTES);  // both boxes, from all slices
                 unsigned char *dst = smem + OFF_X + xs * 2 * X_BYTES + static_cast<int>(crank) * xrows * 128;
@@ -195,6 +222,7 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             }
         }
     } else if (warp == 2) {
+        reg_release<40>();
         // ---------------------------------------- packed-code TMA producer
         // its own ring, so the codes (from HBM) are requested as early as the
         // ring allows, independently of the X ring's pace
@@ -202,34 +230,48 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             const int nwb = (ngroups + 1) / 2;
             for (int wb = 0; wb < nwb; ++wb) {
                 const int ws = wb % WS;
-                if (wb >= WS && !mbar_wait(&bar.wempty[ws], ((wb / WS) - 1) & 1, a.status)) break;
+                if (wb >= WS && !mbar_wait<kHintProd>(&bar.wempty[ws], ((wb / WS) - 1) & 1, a.status)) break;
                 mbar_arrive_expect_tx(&bar.wfull[ws], W_BYTES);
                 // rows past N (last and padding tiles) read as zeros
                 tma_load_2d(smem + a.off_w + ws * W_BYTES, &tmW, wb * 128, n0, &bar.wfull[ws]);
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------- MMA issuer
-        // the whole warp waits for the group's three conditions at once (one
-        // lane per barrier); lane 0 issues
+    } else if (warp == 1 || warp == 3) {
+        reg_release<40>();
+        // ------------------------------------------------------ MMA issuers
+        // warp 1 takes the even groups, warp 3 the odd ones.  The whole warp
+        // waits for its group's three conditions at once (one lane per
+        // barrier); lane 0 issues.  Ring positions advance two groups per
+        // step (XP >= 3, DB = 2, AP = 4: at most one wrap each).
+        //
+        // A parity wait passes at once if its barrier is still in the phase
+        // before the awaited one, so no wait may run two phases ahead.  The
+        // accumulators (DB = 2) and operand stages (AP = 4) belong to one
+        // issuer each; an X stage's previous group g - XP belongs to the same
+        // issuer when XP is even, and when XP >= DB + 2 it was released (its
+        // MMAs done) before this issuer's accumulator wait for group g - 2
+        // ended.  With XP = 3 (the largest K) the X stage is awaited only
+        // after the accumulator, in a second round.
         constexpr uint32_t idesc = idesc_kind_f16(128, BM, 1u);  // BF16, M = 128 lanes, N = 128 rows of X
+        const bool x_second = (XP & 1) && XP < DB + 2;
+        const int g0 = warp == 1 ? 0 : 1;
         bool ok = true;
-        int xs = 0, xph = 0, db = 0, dph = 0;
-        for (int g = 0; g < ngroups; ++g) {
-            const int ap = g % AP;
+        int xs = g0, xph = 0, db = g0, dph = 0, ap = g0, aph = 0;
+        for (int g = g0; g < ngroups; g += 2) {
             uint64_t *wbar = nullptr;
             uint32_t par = 0;
             if (lane == 0) {
                 wbar = &bar.aready[ap];
-                par = (g / AP) & 1;
-            } else if (lane == 1) {
+                par = aph;
+            } else if (lane == 1 && !x_second) {
                 wbar = &bar.xfull[xs];
                 par = xph;
             } else if (lane == 2 && g >= DB) {
                 wbar = &bar.accempty[db];
                 par = dph ^ 1;
             }
-            if (!mbar_wait_lanes(wbar, par, a.status)) {
+            if (!mbar_wait_lanes<kHintMma>(wbar, par, a.status) ||
+                (x_second && !mbar_wait_lanes<kHintMma>(lane == 1 ? &bar.xfull[xs] : nullptr, xph, a.status))) {
                 ok = false;
                 break;
             }
@@ -246,81 +288,109 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                     umma_commit_multicast(&bar.xempty[xs], cmask);
                 else
                     umma_commit(&bar.xempty[xs]);
+                umma_commit(&bar.aempty[ap]);
                 umma_commit(&bar.accfull[db]);
             }
             __syncwarp();
-            if (++xs == XP) {
-                xs = 0;
+            xs += 2;
+            if (xs >= XP) {
+                xs -= XP;
                 xph ^= 1;
             }
-            if (++db == DB) {
-                db = 0;
+            db += 2;
+            if (db >= DB) {
+                db -= DB;
                 dph ^= 1;
+            }
+            ap += 2;
+            if (ap >= AP) {
+                ap -= AP;
+                aph ^= 1;
             }
         }
         // Only after a timeout: one more commit so that the epilogue's wait
-        // also ends once the MMAs already issued have completed.
+        // for this warp's group also ends once the MMAs already issued have
+        // completed.
         if (!ok && lane == 0) umma_commit(&bar.accfull[db]);
+        // `drained` fires once every MMA of both warps has completed
+        if (lane == 0) umma_commit(&bar.drained);
         __syncwarp();
-        mbar_wait(&bar.done, 0, a.status);
-        tc_fence_after();
-        tmem_dealloc(tmem, TMEM_COLS);
-    } else if (warp >= 8 && warp < 12) {
+        if (warp == 1) {
+            // MMAs always complete, so this wait ignores the status word: TMEM
+            // is never released under an MMA still in flight
+            mbar_wait<kHintMma>(&bar.drained, 0, nullptr);
+            mbar_wait<kHintMma>(&bar.done, 0, a.status);
+            __syncwarp();
+            tc_fence_after();
+            tmem_dealloc(tmem, TMEM_COLS);
+        }
+    } else if ((warp >= 8 && warp < 12) || warp >= 16) {
         // ---------------------------------------------- TMEM operand builders
+        // two warps per lane quarter, one half of the group's 64 columns each
+        // (a single warp converts too slowly: latency, not issue, bounds it)
+        reg_release<64>();
         const int q = warp & 3;
+        const int part = warp >= 16 ? 1 : 0;
         const int n = q * RQ + lane;  // weight row of this thread (lanes < 28)
         const bool wrow_ok = lane < RQ;
         const uint32_t t_lane = static_cast<uint32_t>(q * 32) << 16;
-        for (int g = 0; g < ngroups; ++g) {
+        const bool zrow = wrow_ok && n < rows_n;  // rows with loaded zero points
+        // warp-uniform waits throughout (one lane per barrier)
+        const bool okb = mbar_wait_lanes<kHintBuild>(lane == 0 ? &bar.szfull : nullptr, 0, a.status);
+        for (int g = 0; okb && g < ngroups; ++g) {
             const int ap = g % AP;
             const int wb = g >> 1, ws = wb % WS, half = g & 1;
             // lane 0: the packed codes (every other group); lane 1: operand
-            // stage ap is free once the MMAs of group g - AP are done, which
-            // that group's X "empty" barrier records (it cannot run a phase
-            // ahead: its next phase needs this builder's stage for group
-            // g - AP + XP >= g)
+            // stage ap is free once the MMAs of group g - AP are done (their
+            // commit to the stage's own barrier)
             uint64_t *wbar = nullptr;
             uint32_t par = 0;
             if (lane == 0 && half == 0) {
                 wbar = &bar.wfull[ws];
                 par = (wb / WS) & 1;
             } else if (lane == 1 && g >= AP) {
-                const int pg = g - AP;
-                wbar = &bar.xempty[pg % XP];
-                par = (pg / XP) & 1;
+                wbar = &bar.aempty[ap];
+                par = ((g - AP) / AP) & 1;
             }
-            if (!mbar_wait_lanes(wbar, par, a.status)) break;
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            if (!mbar_wait_lanes<kHintBuild>(wbar, par, a.status)) break;
+            // 128 + z_i as a BF16 pair (z_i = clamp(rint(z), 0, 15); a NaN z
+            // gives z_i = 0 and reaches the output through the residual)
+            uint32_t zpair = 0x43004300u;
+            if (zrow) {
+                const float zi = fminf(fmaxf(rintf(f16_bits_to_f32(z_tile[n * a.G + g])), 0.0f), 15.0f);
+                const uint32_t zb = 0x4300u + static_cast<uint32_t>(zi);
+                zpair = zb | (zb << 16);
+            }
+            {
                 uint32_t cols[32];
                 if (wrow_ok) {
-                    // 32 bytes (64 codes) of row n: 16-byte chunks 4 half + 2c
+                    // 32 bytes (64 codes) of row n: 16-byte chunks 4 half + 2 part
                     // and + 1 of the swizzled packed stage (chunk j at j ^ (n mod 8))
                     const unsigned char *wrow = smem + a.off_w + ws * W_BYTES + n * 128;
-                    const int j0 = 4 * half + 2 * c;
+                    const int j0 = 4 * half + 2 * part;
                     const uint4 p0 = *reinterpret_cast<const uint4 *>(wrow + ((j0 ^ (n & 7)) << 4));
                     const uint4 p1 = *reinterpret_cast<const uint4 *>(wrow + (((j0 + 1) ^ (n & 7)) << 4));
                     const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        // codes 8j..8j+7 (code i at bits 4i..4i+3) -> BF16 128 + q,
-                        // the byte q under the byte 0x43; column 4j + i holds
-                        // codes (8j + 2i, 8j + 2i + 1)
+                        // codes 8j..8j+7 (code i at bits 4i..4i+3) -> BF16 128 + q
+                        // (the byte q under the byte 0x43) -> q - z_i, exact;
+                        // column 4j + i holds codes (8j + 2i, 8j + 2i + 1)
                         const uint32_t w = words[j];
                         const uint32_t lo = w & 0x0F0F0F0Fu;         // q0 q2 q4 q6
                         const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;  // q1 q3 q5 q7
                         const uint32_t q0123 = __byte_perm(lo, hi, 0x5140);
                         const uint32_t q4567 = __byte_perm(lo, hi, 0x7362);
-                        cols[4 * j + 0] = __byte_perm(q0123, 0x43434343u, 0x4140);
-                        cols[4 * j + 1] = __byte_perm(q0123, 0x43434343u, 0x4342);
-                        cols[4 * j + 2] = __byte_perm(q4567, 0x43434343u, 0x4140);
-                        cols[4 * j + 3] = __byte_perm(q4567, 0x43434343u, 0x4342);
+                        cols[4 * j + 0] = bf16x2_sub(__byte_perm(q0123, 0x43434343u, 0x4140), zpair);
+                        cols[4 * j + 1] = bf16x2_sub(__byte_perm(q0123, 0x43434343u, 0x4342), zpair);
+                        cols[4 * j + 2] = bf16x2_sub(__byte_perm(q4567, 0x43434343u, 0x4140), zpair);
+                        cols[4 * j + 3] = bf16x2_sub(__byte_perm(q4567, 0x43434343u, 0x4342), zpair);
                     }
                 } else {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) cols[j] = ONES;  // lanes 28-31: S_g rows
                 }
-                tmem_st_32x32b_x32(tmem + t_lane + TM_A + ap * 64 + 32 * c, cols);
+                tmem_st_32x32b_x32(tmem + t_lane + TM_A + ap * 64 + 32 * part, cols);
             }
             tmem_st_wait();
             tc_fence_before();
@@ -330,7 +400,12 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                 if (half == 1 || g == ngroups - 1) mbar_arrive(&bar.wempty[ws]);
             }
         }
+        // this warp's TMEM stores are complete (waited above, or none issued
+        // since the last wait): TMEM may be released as far as it is concerned
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar.done);
     } else if (warp >= 4) {
+        reg_acquire<152>();
         // ------------------------------------------------ group epilogue
         const int q = warp & 3;                // TMEM lane quarter
         const int hc = warp >= 12 ? 1 : 0;     // column half: rows m of X
@@ -339,34 +414,50 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         float y[64];
 #pragma unroll
         for (int j = 0; j < 64; ++j) y[j] = 0.0f;
-        bool ok = mbar_wait(&bar.szfull, 0, a.status);
+        // warp-uniform waits (one lane per barrier): the shuffles and votes
+        // below need the whole warp
+        bool ok = mbar_wait_lanes<kHintEpi>(lane == 0 ? &bar.szfull : nullptr, 0, a.status);
         const bool row_ok = lane < RQ && n < rows_n;
         int db = 0, dph = 0;
         for (int g = 0; ok && g < ngroups; ++g) {
-            if (!mbar_wait(&bar.accfull[db], dph, a.status)) {
+            if (!mbar_wait_lanes<kHintEpi>(lane == 0 ? &bar.accfull[db] : nullptr, dph, a.status)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             const float sf = row_ok ? f16_bits_to_f32(s_tile[n * a.G + g]) : 0.0f;
-            const float zf = row_ok ? f16_bits_to_f32(z_tile[n * a.G + g]) : 0.0f;
-            const float sc = -sf * (128.0f + zf);
-            const uint32_t t_acc = tmem + t_lane + db * 128 + hc * 64;
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(t_acc + 32 * c, r);
-                tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    // lane 28 of every quarter accumulated the row of ones: S_g[m]
-                    const float sg = __shfl_sync(0xffffffffu, __uint_as_float(r[j]), RQ);
-                    y[32 * c + j] = fmaf(sf, __uint_as_float(r[j]), fmaf(sc, sg, y[32 * c + j]));
-                }
+            float zr = 0.0f;  // residual z - z_i (the operand holds q - z_i)
+            if (row_ok) {
+                const float zf = f16_bits_to_f32(z_tile[n * a.G + g]);
+                zr = zf - fminf(fmaxf(rintf(zf), 0.0f), 15.0f);
             }
+            // warp-uniform: fold S_g in only if some row of this warp needs it
+            const bool fold_sg = __any_sync(0xffffffffu, zr != 0.0f);
+            const float sc = -sf * zr;
+            const uint32_t t_acc = tmem + t_lane + db * 128 + hc * 64;
+            // both halves into registers, then release the accumulator at
+            // once: the MMAs of group g + DB need it, the arithmetic does not
+            uint32_t r[2][32];
+            tmem_ld_32x32b_x32(t_acc, r[0]);
+            tmem_ld_32x32b_x32(t_acc + 32, r[1]);
+            tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar.accempty[db]);
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                if (fold_sg) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        // lane 28 of every quarter accumulated the row of ones: S_g[m]
+                        const float sg = __shfl_sync(0xffffffffu, __uint_as_float(r[c][j]), RQ);
+                        y[32 * c + j] = fmaf(sf, __uint_as_float(r[c][j]), fmaf(sc, sg, y[32 * c + j]));
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) y[32 * c + j] = fmaf(sf, __uint_as_float(r[c][j]), y[32 * c + j]);
+                }
+            }
             if (++db == DB) {
                 db = 0;
                 dph ^= 1;
@@ -451,18 +542,27 @@ cudaError_t launch_gemm_int4(const uint16_t *X, const uint8_t *qw, const uint16_
     a.K = static_cast<int>(K);
     a.G = static_cast<int>(K / 128);
     a.sz_bytes = (BNW * a.G * 2 + 15) & ~15;
-    // as many X stages (groups) as shared memory allows (AP + 1 .. MAX_XP):
-    // the operand builders rely on XP >= AP
+    // as many X stages (groups) as shared memory allows (3 .. MAX_XP; the MMA
+    // issuers step their ring positions by two groups and order their waits
+    // by the ring depth)
     const int tail = WS * W_BYTES + 2 * a.sz_bytes + static_cast<int>(sizeof(Barriers));
     int xp = (dev.max_smem_optin - 1024 - tail) / (2 * X_BYTES);
     if (xp > MAX_XP) xp = MAX_XP;
-    if (xp < AP + 1) return cudaErrorNotSupported;
+    if (xp < 3) return cudaErrorNotSupported;
     a.xp = xp;
     a.off_w = OFF_X + xp * 2 * X_BYTES;  // 1024-aligned (X_BYTES is)
     a.off_sz = a.off_w + WS * W_BYTES;   // W_BYTES = 14 KB keeps 1024 alignment
     const int smem = 1024 + a.off_sz + 2 * a.sz_bytes + static_cast<int>(sizeof(Barriers));
     static int configured[64] = {0};
     const int d = dev.device & 63;
+    if (configured[d] == 0) {
+        // the per-role register split (setmaxnreg) must fit in what the block
+        // is launched with, or the growing warpgroups would wait for ever
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, gemm_int4_tc_kernel);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs * THREADS < kRegSplit) return cudaErrorNotSupported;
+    }
     if (configured[d] < smem) {
         cudaError_t e = cudaFuncSetAttribute(gemm_int4_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;

@@ -164,4 +164,23 @@ __device__ __forceinline__ void umma_commit_multicast(uint64_t *bar, uint16_t ma
         : "memory");
 }
 
+// a - b for two BF16 pairs in one fused multiply-add (a * 1 + (-b), a single
+// rounding: exact whenever the difference is a BF16 number).
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(0x3F803F80u), "r"(b ^ 0x80008000u));
+    return d;
+}
+
+// Per-warpgroup register budget (all four warps of a warpgroup execute the
+// same one): release down to R, or grow to R once the block's pool has room.
+template <uint32_t R>
+__device__ __forceinline__ void reg_release() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
+}
+template <uint32_t R>
+__device__ __forceinline__ void reg_acquire() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
+}
+
 }  // namespace w4
