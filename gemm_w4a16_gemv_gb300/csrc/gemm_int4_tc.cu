@@ -39,10 +39,11 @@
 //    per group its X rows (two TMA boxes, 128-byte swizzle, multicast);
 //  * warp 2 (one lane): every two groups the packed codes of the tile's rows,
 //    128 bytes each (TMA), on a ring of its own;
-//  * warps 8-11 (TMEM lane quarters 0-3): per group, thread (q, i) turns the
-//    128 codes of weight row 28 q + i into 64 columns of BF16 pairs q - z_i
-//    (byte permutes and one BF16 pair subtraction) and stores them into the
-//    group's TMEM operand stage; lanes 28-31 store ones;
+//  * warps 8-11 (even groups) and 16-19 (odd groups), TMEM lane quarters
+//    0-3: per group, thread (q, i) turns the 128 codes of weight row 28 q + i
+//    into 64 columns of BF16 pairs q - z_i (byte permutes and one BF16 pair
+//    subtraction) and stores them into the group's TMEM operand stage; lanes
+//    28-31 store ones;
 //  * warps 1 and 3 (one lane each) issue the MMAs of the even and the odd
 //    groups, so that one warp's barrier checks overlap the other's issue and
 //    the tensor pipe sees a steady stream: per group wait for the operand
@@ -78,7 +79,8 @@ constexpr int DB = 2;                 // TMEM accumulators (128 columns each)
 constexpr int X_BYTES = BM * BK * 2;  // 16 KB: one box; a group takes two
 constexpr int W_BYTES = BNW * 128;    // 14 KB packed codes, two groups
 constexpr int THREADS = 640;          // 20 warps, five warpgroups
-constexpr int PREP_WARPS = 8;         // warps 8-11 and 16-19
+constexpr int PREP_WARPS = 8;         // warps 8-11 (even groups) and 16-19 (odd groups)
+constexpr int PREP_PER_GROUP = 4;     // one builder warp per lane quarter builds a group
 constexpr int EPI_WARPS = 8;          // warps 4-7, 12-15
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int kRegSplit = 128 * (40 + 152 + 64 + 152 + 64);  // registers after the per-role split
@@ -151,7 +153,7 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             mbar_init(&bar.wempty[i], PREP_WARPS);
         }
         for (int i = 0; i < AP; ++i) {
-            mbar_init(&bar.aready[i], PREP_WARPS);
+            mbar_init(&bar.aready[i], PREP_PER_GROUP);
             mbar_init(&bar.aempty[i], 1);
         }
         for (int i = 0; i < DB; ++i) {
@@ -179,10 +181,10 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     // Registers per warpgroup, set at the top of each role: the producers and
     // MMA issuers (warps 0-3) need few; each epilogue thread (warps 4-7,
     // 12-15) holds 64 running sums and a 64-column accumulator slice; the
-    // operand builders (8-11, 16-19) a 32-column slice.  128 threads x (40 +
-    // 152 + 64 + 152 + 64) = kRegSplit registers: the launcher checks that the
-    // block is launched with at least that many (a shortfall would leave
-    // setmaxnreg.inc waiting).
+    // operand builders (8-11, 16-19) convert 32 columns at a time.  128
+    // threads x (40 + 152 + 64 + 152 + 64) = kRegSplit registers: the launcher
+    // checks that the block is launched with at least that many (a shortfall
+    // would leave setmaxnreg.inc waiting).
     if (warp == 0) {
         reg_release<40>();
         // ------------------------------------------------------ TMA producer
@@ -326,26 +328,31 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         }
     } else if ((warp >= 8 && warp < 12) || warp >= 16) {
         // ---------------------------------------------- TMEM operand builders
-        // two warps per lane quarter, one half of the group's 64 columns each
-        // (a single warp converts too slowly: latency, not issue, bounds it)
+        // two warps per lane quarter: warps 8-11 build the even groups, 16-19
+        // the odd ones, so each has two group periods for its chain of
+        // waits, loads, conversion and stores (one warp per group is bound by
+        // that chain's latency, not by issue)
         reg_release<64>();
         const int q = warp & 3;
-        const int part = warp >= 16 ? 1 : 0;
+        const int gpar = warp >= 16 ? 1 : 0;
         const int n = q * RQ + lane;  // weight row of this thread (lanes < 28)
         const bool wrow_ok = lane < RQ;
         const uint32_t t_lane = static_cast<uint32_t>(q * 32) << 16;
         const bool zrow = wrow_ok && n < rows_n;  // rows with loaded zero points
         // warp-uniform waits throughout (one lane per barrier)
         const bool okb = mbar_wait_lanes<kHintBuild>(lane == 0 ? &bar.szfull : nullptr, 0, a.status);
-        for (int g = 0; okb && g < ngroups; ++g) {
+        // Parity waits stay in phase: each operand stage belongs to one group
+        // parity (AP even), and both parities meet every packed-code box in
+        // order (one group of each box per parity).
+        for (int g = gpar; okb && g < ngroups; g += 2) {
             const int ap = g % AP;
             const int wb = g >> 1, ws = wb % WS, half = g & 1;
-            // lane 0: the packed codes (every other group); lane 1: operand
-            // stage ap is free once the MMAs of group g - AP are done (their
-            // commit to the stage's own barrier)
+            // lane 0: the packed codes; lane 1: operand stage ap is free once
+            // the MMAs of group g - AP are done (their commit to the stage's
+            // own barrier)
             uint64_t *wbar = nullptr;
             uint32_t par = 0;
-            if (lane == 0 && half == 0) {
+            if (lane == 0) {
                 wbar = &bar.wfull[ws];
                 par = (wb / WS) & 1;
             } else if (lane == 1 && g >= AP) {
@@ -361,13 +368,14 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                 const uint32_t zb = 0x4300u + static_cast<uint32_t>(zi);
                 zpair = zb | (zb << 16);
             }
-            {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
                 uint32_t cols[32];
                 if (wrow_ok) {
-                    // 32 bytes (64 codes) of row n: 16-byte chunks 4 half + 2 part
+                    // 32 bytes (64 codes) of row n: 16-byte chunks 4 half + 2c
                     // and + 1 of the swizzled packed stage (chunk j at j ^ (n mod 8))
                     const unsigned char *wrow = smem + a.off_w + ws * W_BYTES + n * 128;
-                    const int j0 = 4 * half + 2 * part;
+                    const int j0 = 4 * half + 2 * c;
                     const uint4 p0 = *reinterpret_cast<const uint4 *>(wrow + ((j0 ^ (n & 7)) << 4));
                     const uint4 p1 = *reinterpret_cast<const uint4 *>(wrow + (((j0 + 1) ^ (n & 7)) << 4));
                     const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
@@ -390,14 +398,16 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
 #pragma unroll
                     for (int j = 0; j < 32; ++j) cols[j] = ONES;  // lanes 28-31: S_g rows
                 }
-                tmem_st_32x32b_x32(tmem + t_lane + TM_A + ap * 64 + 32 * part, cols);
+                tmem_st_32x32b_x32(tmem + t_lane + TM_A + ap * 64 + 32 * c, cols);
             }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&bar.aready[ap]);
-                if (half == 1 || g == ngroups - 1) mbar_arrive(&bar.wempty[ws]);
+                // the box is free once both parities' builders are done with it
+                // (with an odd group count the last box is never awaited)
+                mbar_arrive(&bar.wempty[ws]);
             }
         }
         // this warp's TMEM stores are complete (waited above, or none issued
