@@ -83,7 +83,13 @@ constexpr int PREP_WARPS = 8;         // warps 8-11 (even groups) and 16-19 (odd
 constexpr int PREP_PER_GROUP = 4;     // one builder warp per lane quarter builds a group
 constexpr int EPI_WARPS = 8;          // warps 4-7, 12-15
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int kRegSplit = 128 * (40 + 152 + 64 + 152 + 64);  // registers after the per-role split
+// Registers per thread after the per-warpgroup split (setmaxnreg): the light
+// warps and the builders release down to theirs, the epilogue grows to its
+// own, so the launch count must lie between them (checked by the launcher).
+constexpr uint32_t kRegLight = 32;    // warps 0-3: producers and MMA issuers
+constexpr uint32_t kRegBuild = 80;    // warps 8-11, 16-19: operand builders
+constexpr uint32_t kRegEpi = 144;     // warps 4-7, 12-15: epilogue
+constexpr int kRegSplit = 128 * static_cast<int>(kRegLight + 2 * kRegEpi + 2 * kRegBuild);
 // Suspend-time hints (ns) of the waits' polls, per role (0: plain polls).
 constexpr uint32_t kHintProd = 0;     // X and packed-code producers
 constexpr uint32_t kHintMma = 0;      // MMA issuers
@@ -181,12 +187,14 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     // Registers per warpgroup, set at the top of each role: the producers and
     // MMA issuers (warps 0-3) need few; each epilogue thread (warps 4-7,
     // 12-15) holds 64 running sums and a 64-column accumulator slice; the
-    // operand builders (8-11, 16-19) convert 32 columns at a time.  128
-    // threads x (40 + 152 + 64 + 152 + 64) = kRegSplit registers: the launcher
-    // checks that the block is launched with at least that many (a shortfall
-    // would leave setmaxnreg.inc waiting).
+    // operand builders (8-11, 16-19) a group's 16 code words and 32 columns.
+    // 128 threads x (32 + 144 + 80 + 144 + 80) = kRegSplit registers.  The
+    // launcher checks that the block is launched with at least that many (a
+    // shortfall would leave setmaxnreg.inc waiting) and with a per-thread
+    // count between the released and the acquired ones (an increase below,
+    // or a decrease above, the current count is not a valid instruction).
     if (warp == 0) {
-        reg_release<40>();
+        reg_release<kRegLight>();
         // ------------------------------------------------------ TMA producer
         // the whole warp waits (one lane per barrier); lane 0 issues
         const uint64_t pol = policy_evict_first();
@@ -224,7 +232,7 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             }
         }
     } else if (warp == 2) {
-        reg_release<40>();
+        reg_release<kRegLight>();
         // ---------------------------------------- packed-code TMA producer
         // its own ring, so the codes (from HBM) are requested as early as the
         // ring allows, independently of the X ring's pace
@@ -239,7 +247,7 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             }
         }
     } else if (warp == 1 || warp == 3) {
-        reg_release<40>();
+        reg_release<kRegLight>();
         // ------------------------------------------------------ MMA issuers
         // warp 1 takes the even groups, warp 3 the odd ones.  The whole warp
         // waits for its group's three conditions at once (one lane per
@@ -332,7 +340,7 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         // the odd ones, so each has two group periods for its chain of
         // waits, loads, conversion and stores (one warp per group is bound by
         // that chain's latency, not by issue)
-        reg_release<64>();
+        reg_release<kRegBuild>();
         const int q = warp & 3;
         const int gpar = warp >= 16 ? 1 : 0;
         const int n = q * RQ + lane;  // weight row of this thread (lanes < 28)
@@ -360,6 +368,23 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                 par = ((g - AP) / AP) & 1;
             }
             if (!mbar_wait_lanes<kHintBuild>(wbar, par, a.status)) break;
+            // The group's 64 code bytes of row n (16-byte chunks 4 half + 0..3
+            // of the swizzled packed stage, chunk j at j ^ (n mod 8)) are
+            // loaded together: a shared-memory load waits several hundred
+            // cycles here (the TMA and the MMAs share the port), so both
+            // halves' loads must be in flight at once.
+            uint32_t wds[16];
+            if (wrow_ok) {
+                const unsigned char *wrow = smem + a.off_w + ws * W_BYTES + n * 128;
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    const uint4 p = *reinterpret_cast<const uint4 *>(wrow + (((4 * half + c4) ^ (n & 7)) << 4));
+                    wds[4 * c4 + 0] = p.x;
+                    wds[4 * c4 + 1] = p.y;
+                    wds[4 * c4 + 2] = p.z;
+                    wds[4 * c4 + 3] = p.w;
+                }
+            }
             // 128 + z_i as a BF16 pair (z_i = clamp(rint(z), 0, 15); a NaN z
             // gives z_i = 0 and reaches the output through the residual)
             uint32_t zpair = 0x43004300u;
@@ -372,19 +397,12 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             for (int c = 0; c < 2; ++c) {
                 uint32_t cols[32];
                 if (wrow_ok) {
-                    // 32 bytes (64 codes) of row n: 16-byte chunks 4 half + 2c
-                    // and + 1 of the swizzled packed stage (chunk j at j ^ (n mod 8))
-                    const unsigned char *wrow = smem + a.off_w + ws * W_BYTES + n * 128;
-                    const int j0 = 4 * half + 2 * c;
-                    const uint4 p0 = *reinterpret_cast<const uint4 *>(wrow + ((j0 ^ (n & 7)) << 4));
-                    const uint4 p1 = *reinterpret_cast<const uint4 *>(wrow + (((j0 + 1) ^ (n & 7)) << 4));
-                    const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        // codes 8j..8j+7 (code i at bits 4i..4i+3) -> BF16 128 + q
-                        // (the byte q under the byte 0x43) -> q - z_i, exact;
-                        // column 4j + i holds codes (8j + 2i, 8j + 2i + 1)
-                        const uint32_t w = words[j];
+                        // codes 8j..8j+7 of this half (code i at bits 4i..4i+3) ->
+                        // BF16 128 + q (the byte q under the byte 0x43) -> q - z_i,
+                        // exact; column 4j + i holds codes (8j + 2i, 8j + 2i + 1)
+                        const uint32_t w = wds[8 * c + j];
                         const uint32_t lo = w & 0x0F0F0F0Fu;         // q0 q2 q4 q6
                         const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;  // q1 q3 q5 q7
                         const uint32_t q0123 = __byte_perm(lo, hi, 0x5140);
@@ -415,7 +433,7 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar.done);
     } else if (warp >= 4) {
-        reg_acquire<152>();
+        reg_acquire<kRegEpi>();
         // ------------------------------------------------ group epilogue
         const int q = warp & 3;                // TMEM lane quarter
         const int hc = warp >= 12 ? 1 : 0;     // column half: rows m of X
@@ -571,7 +589,10 @@ cudaError_t launch_gemm_int4(const uint16_t *X, const uint8_t *qw, const uint16_
         cudaFuncAttributes fa;
         cudaError_t e = cudaFuncGetAttributes(&fa, gemm_int4_tc_kernel);
         if (e != cudaSuccess) return e;
-        if (fa.numRegs * THREADS < kRegSplit) return cudaErrorNotSupported;
+        const int launch_regs = fa.numRegs;
+        if (launch_regs * THREADS < kRegSplit || launch_regs < static_cast<int>(kRegBuild) ||
+            launch_regs < static_cast<int>(kRegLight) || launch_regs > static_cast<int>(kRegEpi))
+            return cudaErrorNotSupported;
     }
     if (configured[d] < smem) {
         cudaError_t e = cudaFuncSetAttribute(gemm_int4_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
