@@ -196,8 +196,11 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     if (warp == 0) {
         reg_release<kRegLight>();
         // ------------------------------------------------------ TMA producer
-        // the whole warp waits (one lane per barrier); lane 0 issues
+        // the whole warp waits (one lane per barrier); lane 0 issues.  X is
+        // kept in L2 (evict-last): every N tile reads it, and the streamed
+        // packed codes (evict-first) must not push it out.
         const uint64_t pol = policy_evict_first();
+        const uint64_t pol_x = policy_evict_last();
         if (lane == 0) {
             tma_prefetch_desc(&tmW);
             tma_prefetch_desc(&tmX);
@@ -220,9 +223,10 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                 const int row = m0 + static_cast<int>(crank) * xrows;
                 for (int h = 0; h < 2; ++h) {
                     if (a.csize > 1)
-                        tma_load_2d_multicast(dst + h * X_BYTES, &tmX, g * GK + h * BK, row, &bar.xfull[xs], cmask);
+                        tma_load_2d_multicast_hint(dst + h * X_BYTES, &tmX, g * GK + h * BK, row, &bar.xfull[xs],
+                                                   cmask, pol_x);
                     else
-                        tma_load_2d(dst + h * X_BYTES, &tmX, g * GK + h * BK, row, &bar.xfull[xs]);
+                        tma_load_2d_hint(dst + h * X_BYTES, &tmX, g * GK + h * BK, row, &bar.xfull[xs], pol_x);
                 }
             }
             __syncwarp();
@@ -235,15 +239,17 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         reg_release<kRegLight>();
         // ---------------------------------------- packed-code TMA producer
         // its own ring, so the codes (from HBM) are requested as early as the
-        // ring allows, independently of the X ring's pace
+        // ring allows, independently of the X ring's pace; streamed with the
+        // evict-first policy
         if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first();
             const int nwb = (ngroups + 1) / 2;
             for (int wb = 0; wb < nwb; ++wb) {
                 const int ws = wb % WS;
                 if (wb >= WS && !mbar_wait<kHintProd>(&bar.wempty[ws], ((wb / WS) - 1) & 1, a.status)) break;
                 mbar_arrive_expect_tx(&bar.wfull[ws], W_BYTES);
                 // rows past N (last and padding tiles) read as zeros
-                tma_load_2d(smem + a.off_w + ws * W_BYTES, &tmW, wb * 128, n0, &bar.wfull[ws]);
+                tma_load_2d_hint(smem + a.off_w + ws * W_BYTES, &tmW, wb * 128, n0, &bar.wfull[ws], pol_w);
             }
         }
     } else if (warp == 1 || warp == 3) {
