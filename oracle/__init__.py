@@ -13,6 +13,8 @@ What it computes (page titles as published):
   * "DeepSeek V4 Triton FP4 optimisation in practice", deep analysis item 2
     (even K column <-> low nibble) and the FP4 expert GEMMs;
   * the problem statement y = x W^T, W = (q - z) * s, FP16 s and z;
+  * symmetric INT4 (the symmetric GPTQ variant of "Quantisation correctness")
+    in GPTQ's form: z = None means the implicit zero point 8;
   * the OCP MX definition of E2M1 for the FP4 value table.
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against
@@ -91,6 +93,11 @@ def _ptr(a: np.ndarray):
     return ctypes.c_void_p(a.ctypes.data)
 
 
+def _zptr(z):
+    """Zero points or NULL (symmetric INT4)."""
+    return ctypes.c_void_p(None) if z is None else _ptr(z)
+
+
 # ----------------------------------------------------------------- formats
 
 def f16_to_f64(bits: int) -> float:
@@ -130,14 +137,15 @@ def e2m1_value(c: int) -> float:
 # -------------------------------------------------------------- dequantise
 
 def dequant_int4(qw, s, z, K: int, group: int = 128) -> np.ndarray:
-    """W[N, K] (float32) = ((float)q - (float)z) * (float)s per element."""
+    """W[N, K] (float32) = ((float)q - (float)z) * (float)s per element;
+    z=None: symmetric INT4 (z = 8 for every group)."""
     qw = _c(qw, np.uint8)
     s = _c(s, np.uint16)
-    z = _c(z, np.uint16)
+    z = None if z is None else _c(z, np.uint16)
     N = qw.size // (K // 2)
     _check_int4(qw, s, z, N, K, group)
     W = np.empty((N, K), dtype=np.float32)
-    _load().oracle_dequant_int4(_ptr(qw), _ptr(s), _ptr(z), N, K, group, _ptr(W))
+    _load().oracle_dequant_int4(_ptr(qw), _ptr(s), _zptr(z), N, K, group, _ptr(W))
     return W
 
 
@@ -159,23 +167,24 @@ def _check_int4(qw, s, z, N, K, group):
     if qw.size != N * (K // 2):
         raise ValueError("qw has %d bytes, expected %d" % (qw.size, N * (K // 2)))
     G = K // group
-    if s.size != N * G or z.size != N * G:
+    if s.size != N * G or (z is not None and z.size != N * G):
         raise ValueError("s/z must hold N*K/group values")
 
 
 # ---------------------------------------------------------------- products
 
 def gemm_int4(X, qw, s, z, K: int, group: int = 128) -> np.ndarray:
-    """Y[M, N] (float64) = X W^T with INT4 weights; X bfloat16 bits [M, K]."""
+    """Y[M, N] (float64) = X W^T with INT4 weights; X bfloat16 bits [M, K];
+    z=None: symmetric INT4 (z = 8)."""
     X = _c(np.asarray(X).reshape(-1, K), np.uint16)
     qw = _c(qw, np.uint8)
     s = _c(s, np.uint16)
-    z = _c(z, np.uint16)
+    z = None if z is None else _c(z, np.uint16)
     M = X.shape[0]
     N = qw.size // (K // 2)
     _check_int4(qw, s, z, N, K, group)
     Y = np.empty((M, N), dtype=np.float64)
-    _load().oracle_gemm_int4(_ptr(X), _ptr(qw), _ptr(s), _ptr(z), M, N, K,
+    _load().oracle_gemm_int4(_ptr(X), _ptr(qw), _ptr(s), _zptr(z), M, N, K,
                              group, _ptr(Y))
     return Y
 

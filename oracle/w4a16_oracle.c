@@ -18,6 +18,10 @@
  *  The problem statement fixes the remaining arithmetic:
  *          y[m,n] = sum_k x[m,k] * W[n,k],  W[n,k] = (q[n,k] - z[n,k/g]) * s[n,k/g]
  *          with q packed two per byte along K, low nibble = even k, s and z FP16.
+ *  Symmetric INT4 ([Lab5] "Quantisation correctness": symmetric GPTQ is the
+ *  variant the lab measured before settling on asymmetric) is taken in its
+ *  GPTQ form, the zero point being the code midpoint 2^(4-1) = 8: it is the
+ *  asymmetric formula with z = 8, selected by passing z = NULL.
  *  FP4 E2M1 values follow the OCP Microscaling (MX) format definition
  *  (1 sign, 2 exponent bits with bias 1, 1 mantissa bit, no inf/NaN); the
  *  pages name the format but print no table.
@@ -123,7 +127,8 @@ double oracle_e2m1_value(int code)
  * final configuration: bits 4, group_size g, symmetric false, FP16 scale;
  * problem statement: W = (q - z) * s).  One binary32 value per element:
  * (float)q - (float)z rounded, then times (float)s rounded.
- * qw: [N, K/2] bytes; s, z: [N, K/g] binary16; W: [N, K] binary32. */
+ * qw: [N, K/2] bytes; s, z: [N, K/g] binary16; W: [N, K] binary32.
+ * z == NULL: symmetric INT4, z = 8 for every group. */
 void oracle_dequant_int4(const uint8_t *qw, const uint16_t *s, const uint16_t *z,
                          int64_t N, int64_t K, int64_t g, float *W)
 {
@@ -131,7 +136,7 @@ void oracle_dequant_int4(const uint8_t *qw, const uint16_t *s, const uint16_t *z
     for (int64_t n = 0; n < N; ++n) {
         for (int64_t k = 0; k < K; ++k) {
             float q = (float)oracle_code(qw, K, n, k);
-            float zf = (float)oracle_f16_to_f64(z[n * G + k / g]);
+            float zf = z ? (float)oracle_f16_to_f64(z[n * G + k / g]) : 8.0f;
             float sf = (float)oracle_f16_to_f64(s[n * G + k / g]);
             float d = q - zf;
             float w = d * sf;
@@ -163,7 +168,8 @@ void oracle_dequant_fp4(const uint8_t *qw, const uint16_t *s, int64_t rows,
  * the weight is dequantised per element and dotted with the activation;
  * M = 1 is the decode GEMV, M > 1 the prefill GEMM).  Each W[n,k] is the
  * binary32 value of oracle_dequant_int4; the product and the running sum are
- * binary64, k ascending.  X: [M, K] bfloat16; Y: [M, N] binary64. */
+ * binary64, k ascending.  X: [M, K] bfloat16; Y: [M, N] binary64.
+ * z == NULL: symmetric INT4 (z = 8), as in oracle_dequant_int4. */
 void oracle_gemm_int4(const uint16_t *X, const uint8_t *qw, const uint16_t *s,
                       const uint16_t *z, int64_t M, int64_t N, int64_t K,
                       int64_t g, double *Y)
@@ -174,7 +180,7 @@ void oracle_gemm_int4(const uint16_t *X, const uint8_t *qw, const uint16_t *s,
             double acc = 0.0;
             for (int64_t k = 0; k < K; ++k) {
                 float q = (float)oracle_code(qw, K, n, k);
-                float zf = (float)oracle_f16_to_f64(z[n * G + k / g]);
+                float zf = z ? (float)oracle_f16_to_f64(z[n * G + k / g]) : 8.0f;
                 float sf = (float)oracle_f16_to_f64(s[n * G + k / g]);
                 float d = q - zf;
                 float w = d * sf;

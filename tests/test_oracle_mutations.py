@@ -4,7 +4,7 @@ Each case plants one mistake in a scratch copy of the oracle's C source (on
 the CPU only), rebuilds it, and runs the pin suite against it: the suite has
 to fail.  This is the evidence that the pins constrain every step of the
 oracle (unpacking, zero point, scale, sign, group and row indexing, operand
-order, E2M1 decoding, expert indirection)."""
+order, E2M1 decoding, expert indirection, the symmetric zero point)."""
 import os
 import shutil
 import subprocess
@@ -28,6 +28,8 @@ MUTATIONS = {
         "acc += (double)w * oracle_bf16_to_f64(X[m * K + k]);",
         "acc += (double)w * oracle_bf16_to_f64(X[m * K + (n % K)]);"),
     "activation_row": ("X[m * K + k]", "X[k]"),
+    "symmetric_zero_point": ("z ? (float)oracle_f16_to_f64(z[n * G + k / g]) : 8.0f;\n                float sf",
+                             "z ? (float)oracle_f16_to_f64(z[n * G + k / g]) : 7.0f;\n                float sf"),
     "fp4_scale_index": ("s[r * G + k / g]);\n            W[r * K + k] = v * sf;",
                         "s[r * G]);\n            W[r * K + k] = v * sf;"),
 }

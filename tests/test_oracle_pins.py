@@ -186,6 +186,44 @@ def test_code_equal_to_zero_point_gives_zero():
     assert np.all(y == 0.0)
 
 
+# Symmetric INT4 ("Lab 5", Quantisation correctness: the symmetric GPTQ
+# variant), taken in GPTQ's form with the implicit zero point 8 (z = None).
+
+def test_symmetric_midpoint_codes_give_zero():
+    rng = np.random.default_rng(15)
+    K = 384
+    qw = np.full((4, K // 2), 0x88, np.uint8)     # every code 8
+    s = f16_arr(rng.uniform(0.002, 0.02, size=(4, K // 128)))
+    y = oracle.gemv_int4(rand_bf16(rng, K), qw, s, None, K=K)
+    assert np.all(y == 0.0)
+    assert np.all(oracle.dequant_int4(qw, s, None, K=K) == 0.0)
+
+
+def test_symmetric_extreme_codes_closed_form():
+    # codes 15 -> +7 s, codes 0 -> -8 s (two's-complement-like range [-8, 7])
+    rng = np.random.default_rng(16)
+    K = 256
+    c = 5.0 / 512.0                        # exact in FP16
+    x = rand_bf16(rng, K)
+    sx = math.fsum(bf16_vals(x))
+    s = np.full((2, K // 128), f16(c), np.uint16)
+    top = oracle.gemv_int4(x, np.full((2, K // 2), 0xFF, np.uint8), s, None, K=K)
+    bot = oracle.gemv_int4(x, np.full((2, K // 2), 0x00, np.uint8), s, None, K=K)
+    assert np.allclose(top, 7.0 * c * sx, rtol=1e-12, atol=1e-12)
+    assert np.allclose(bot, -8.0 * c * sx, rtol=1e-12, atol=1e-12)
+
+
+def test_symmetric_equals_explicit_zero_point_eight():
+    rng = np.random.default_rng(17)
+    N, K = 5, 384
+    qw = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    s = f16_arr(rng.uniform(0.002, 0.02, size=(N, K // 128)))
+    z8 = np.full((N, K // 128), f16(8.0), np.uint16)
+    X = rand_bf16(rng, (2, K))
+    assert np.array_equal(oracle.gemm_int4(X, qw, s, None, K=K), oracle.gemm_int4(X, qw, s, z8, K=K))
+    assert np.array_equal(oracle.dequant_int4(qw, s, None, K=K), oracle.dequant_int4(qw, s, z8, K=K))
+
+
 def test_identity_weights_reproduce_activations():
     rng = np.random.default_rng(6)
     K = 128
