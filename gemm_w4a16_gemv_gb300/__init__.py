@@ -112,14 +112,15 @@ def _need(t: torch.Tensor, name: str, dtype, numel=None, device=None):
 
 
 def w4a16_gemv(x, qw, s, z, y=None, group: int = 128, stream=None):
-    """y[N] = x[K] W^T with INT4 weights qw [N, K/2], s/z [N, K/group]."""
+    """y[N] = x[K] W^T with INT4 weights qw [N, K/2], s/z [N, K/group];
+    z=None: symmetric INT4 (zero point 8)."""
     N = qw.shape[0]
     K = 2 * qw.shape[-1]
     dev = qw.device
     px = _need(x, "x", torch.bfloat16, K, dev)
     pq = _need(qw, "qw", torch.uint8, N * K // 2, dev)
     ps = _need(s, "s", torch.float16, N * (K // group), dev)
-    pz = _need(z, "z", torch.float16, N * (K // group), dev)
+    pz = _need(z, "z", torch.float16, N * (K // group), dev) if z is not None else None
     if y is None:
         y = torch.empty(N, dtype=torch.bfloat16, device=dev)
     py = _need(y, "y", torch.bfloat16, N, dev)
@@ -128,7 +129,8 @@ def w4a16_gemv(x, qw, s, z, y=None, group: int = 128, stream=None):
 
 
 def w4a16_gemm(X, qw, s, z, Y=None, group: int = 128, stream=None):
-    """Y[M, N] = X[M, K] W^T with INT4 weights qw [N, K/2], s/z [N, K/group]."""
+    """Y[M, N] = X[M, K] W^T with INT4 weights qw [N, K/2], s/z [N, K/group];
+    z=None: symmetric INT4 (zero point 8)."""
     N = qw.shape[0]
     K = 2 * qw.shape[-1]
     M = X.numel() // K
@@ -136,7 +138,7 @@ def w4a16_gemm(X, qw, s, z, Y=None, group: int = 128, stream=None):
     pX = _need(X, "X", torch.bfloat16, M * K, dev)
     pq = _need(qw, "qw", torch.uint8, N * K // 2, dev)
     ps = _need(s, "s", torch.float16, N * (K // group), dev)
-    pz = _need(z, "z", torch.float16, N * (K // group), dev)
+    pz = _need(z, "z", torch.float16, N * (K // group), dev) if z is not None else None
     if Y is None:
         Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
     pY = _need(Y, "Y", torch.bfloat16, M * N, dev)

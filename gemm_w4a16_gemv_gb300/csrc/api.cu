@@ -82,13 +82,13 @@ const char *w4a16_last_error_string(void) { return g_err; }
 int w4a16_gemv(const uint16_t *x, const uint8_t *qw, const uint16_t *s,
                const uint16_t *z, uint16_t *y, int64_t N, int64_t K,
                int group, void *stream) {
-    if (!x || !qw || !s || !z || !y) return fail(W4A16_ERR_INVALID_ARG, "w4a16_gemv: null pointer");
+    if (!x || !qw || !s || !y) return fail(W4A16_ERR_INVALID_ARG, "w4a16_gemv: null pointer");
     if (N < 1 || K < 1) return fail(W4A16_ERR_INVALID_ARG, "w4a16_gemv: N=%lld K=%lld must be >= 1", (long long)N, (long long)K);
     if (group != 128) return fail(W4A16_ERR_UNSUPPORTED, "w4a16_gemv: group %d (only 128)", group);
     if (K % 128 != 0) return fail(W4A16_ERR_INVALID_ARG, "w4a16_gemv: K=%lld not a multiple of the group", (long long)K);
     if (K > 16384) return fail(W4A16_ERR_UNSUPPORTED, "w4a16_gemv: K=%lld > 16384", (long long)K);
     if (N > (int64_t(1) << 31)) return fail(W4A16_ERR_UNSUPPORTED, "w4a16_gemv: N=%lld too large", (long long)N);
-    if (!aligned16(x) || !aligned16(qw) || !aligned16(s) || !aligned16(z) || !aligned16(y))
+    if (!aligned16(x) || !aligned16(qw) || !aligned16(s) || (z && !aligned16(z)) || !aligned16(y))
         return fail(W4A16_ERR_MISALIGNED, "w4a16_gemv: pointers must be 16-byte aligned");
     w4::DeviceInfo dev;
     unsigned int *status;
@@ -100,7 +100,7 @@ int w4a16_gemv(const uint16_t *x, const uint8_t *qw, const uint16_t *s,
 int w4a16_gemm(const uint16_t *X, const uint8_t *qw, const uint16_t *s,
                const uint16_t *z, uint16_t *Y, int64_t M, int64_t N,
                int64_t K, int group, void *stream) {
-    if (!X || !qw || !s || !z || !Y) return fail(W4A16_ERR_INVALID_ARG, "w4a16_gemm: null pointer");
+    if (!X || !qw || !s || !Y) return fail(W4A16_ERR_INVALID_ARG, "w4a16_gemm: null pointer");
     if (M < 1 || N < 1 || K < 1)
         return fail(W4A16_ERR_INVALID_ARG, "w4a16_gemm: M=%lld N=%lld K=%lld must be >= 1", (long long)M,
                     (long long)N, (long long)K);
@@ -110,7 +110,7 @@ int w4a16_gemm(const uint16_t *X, const uint8_t *qw, const uint16_t *s,
     if (K > 16384) return fail(W4A16_ERR_UNSUPPORTED, "w4a16_gemm: K=%lld > 16384", (long long)K);
     if (M > (int64_t(1) << 30) || N > (int64_t(1) << 30) || M * N > (int64_t(1) << 40))
         return fail(W4A16_ERR_UNSUPPORTED, "w4a16_gemm: sizes too large");
-    if (!aligned16(X) || !aligned16(qw) || !aligned16(s) || !aligned16(z) || !aligned16(Y))
+    if (!aligned16(X) || !aligned16(qw) || !aligned16(s) || (z && !aligned16(z)) || !aligned16(Y))
         return fail(W4A16_ERR_MISALIGNED, "w4a16_gemm: pointers must be 16-byte aligned");
     w4::DeviceInfo dev;
     unsigned int *status;
@@ -151,7 +151,6 @@ int w4a16_dequant(int fmt, const uint8_t *qw, const uint16_t *s,
     if (out_dtype != W4_OUT_F32 && out_dtype != W4_OUT_BF16)
         return fail(W4A16_ERR_INVALID_ARG, "w4a16_dequant: unknown output dtype %d", out_dtype);
     if (!qw || !s || !out) return fail(W4A16_ERR_INVALID_ARG, "w4a16_dequant: null pointer");
-    if (fmt == W4_FMT_INT4_ASYM && !z) return fail(W4A16_ERR_INVALID_ARG, "w4a16_dequant: INT4 needs z");
     if (fmt == W4_FMT_FP4_E2M1 && z) return fail(W4A16_ERR_INVALID_ARG, "w4a16_dequant: FP4 takes no z");
     if (rows < 1 || K < 1) return fail(W4A16_ERR_INVALID_ARG, "w4a16_dequant: rows, K must be >= 1");
     const int want = fmt == W4_FMT_INT4_ASYM ? 128 : 32;

@@ -35,7 +35,8 @@ dequant_kernel(const uint8_t *__restrict__ qw, const uint16_t *__restrict__ s,
         // 32 codes never straddle a group (group is 32 or 128)
         const int64_t gi = r * G + k0 / group;
         const float sf = f16_bits_to_f32(s[gi]);
-        const float zf = (FMT == 0) ? f16_bits_to_f32(z[gi]) : 0.0f;
+        // INT4 without zero points is symmetric: the midpoint code 8
+        const float zf = (FMT == 0) ? (z ? f16_bits_to_f32(z[gi]) : 8.0f) : 0.0f;
         float w[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {

@@ -131,6 +131,9 @@ struct Barriers {
     uint32_t tmem_holder;
 };
 
+// SYM: symmetric INT4 (no zero points, z = 8), its own instance so that the
+// asymmetric one carries no test for it.
+template <bool SYM>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                     const GemmArgs a) {
@@ -205,10 +208,11 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             tma_prefetch_desc(&tmW);
             tma_prefetch_desc(&tmX);
             const uint32_t szb = static_cast<uint32_t>(rows_n) * a.G * 2;
-            mbar_arrive_expect_tx(&bar.szfull, 2 * szb);
+            mbar_arrive_expect_tx(&bar.szfull, SYM ? szb : 2 * szb);  // symmetric: scales only
             if (szb) {
                 bulk_g2s(smem + a.off_sz, a.s + static_cast<size_t>(n0) * a.G, szb, &bar.szfull, pol);
-                bulk_g2s(smem + a.off_sz + a.sz_bytes, a.z + static_cast<size_t>(n0) * a.G, szb, &bar.szfull, pol);
+                if (!SYM)
+                    bulk_g2s(smem + a.off_sz + a.sz_bytes, a.z + static_cast<size_t>(n0) * a.G, szb, &bar.szfull, pol);
             }
         }
         int xs = 0, xph = 0;  // X stage and its phase
@@ -352,7 +356,7 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         const int n = q * RQ + lane;  // weight row of this thread (lanes < 28)
         const bool wrow_ok = lane < RQ;
         const uint32_t t_lane = static_cast<uint32_t>(q * 32) << 16;
-        const bool zrow = wrow_ok && n < rows_n;  // rows with loaded zero points
+        const bool zrow = !SYM && wrow_ok && n < rows_n;  // rows with loaded zero points
         // warp-uniform waits throughout (one lane per barrier)
         const bool okb = mbar_wait_lanes<kHintBuild>(lane == 0 ? &bar.szfull : nullptr, 0, a.status);
         // Parity waits stay in phase: each operand stage belongs to one group
@@ -393,7 +397,7 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             }
             // 128 + z_i as a BF16 pair (z_i = clamp(rint(z), 0, 15); a NaN z
             // gives z_i = 0 and reaches the output through the residual)
-            uint32_t zpair = 0x43004300u;
+            uint32_t zpair = SYM ? 0x43084308u : 0x43004300u;  // symmetric INT4: z = 8
             if (zrow) {
                 const float zi = fminf(fmaxf(rintf(f16_bits_to_f32(z_tile[n * a.G + g])), 0.0f), 15.0f);
                 const uint32_t zb = 0x4300u + static_cast<uint32_t>(zi);
@@ -460,8 +464,8 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             }
             tc_fence_after();
             const float sf = row_ok ? f16_bits_to_f32(s_tile[n * a.G + g]) : 0.0f;
-            float zr = 0.0f;  // residual z - z_i (the operand holds q - z_i)
-            if (row_ok) {
+            float zr = 0.0f;  // residual z - z_i (the operand holds q - z_i; 0 when symmetric)
+            if (!SYM && row_ok) {
                 const float zf = f16_bits_to_f32(z_tile[n * a.G + g]);
                 zr = zf - fminf(fmaxf(rintf(zf), 0.0f), 15.0f);
             }
@@ -587,23 +591,26 @@ cudaError_t launch_gemm_int4(const uint16_t *X, const uint8_t *qw, const uint16_
     a.off_w = OFF_X + xp * 2 * X_BYTES;  // 1024-aligned (X_BYTES is)
     a.off_sz = a.off_w + WS * W_BYTES;   // W_BYTES = 14 KB keeps 1024 alignment
     const int smem = 1024 + a.off_sz + 2 * a.sz_bytes + static_cast<int>(sizeof(Barriers));
-    static int configured[64] = {0};
+    // one instance per zero-point mode, each configured once per device
+    const int sym = z ? 0 : 1;
+    auto kern = sym ? gemm_int4_tc_kernel<true> : gemm_int4_tc_kernel<false>;
+    static int configured[2][64] = {{0}};
     const int d = dev.device & 63;
-    if (configured[d] == 0) {
+    if (configured[sym][d] == 0) {
         // the per-role register split (setmaxnreg) must fit in what the block
         // is launched with, or the growing warpgroups would wait for ever
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, gemm_int4_tc_kernel);
+        cudaError_t e = cudaFuncGetAttributes(&fa, kern);
         if (e != cudaSuccess) return e;
         const int launch_regs = fa.numRegs;
         if (launch_regs * THREADS < kRegSplit || launch_regs < static_cast<int>(kRegBuild) ||
             launch_regs < static_cast<int>(kRegLight) || launch_regs > static_cast<int>(kRegEpi))
             return cudaErrorNotSupported;
     }
-    if (configured[d] < smem) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_int4_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (configured[sym][d] < smem) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        configured[d] = smem;
+        configured[sym][d] = smem;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(gx, gy, 1);
@@ -617,7 +624,7 @@ cudaError_t launch_gemm_int4(const uint16_t *X, const uint8_t *qw, const uint16_
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_int4_tc_kernel, tmX, tmW, a);
+    return cudaLaunchKernelEx(&cfg, kern, tmX, tmW, a);
 }
 
 }  // namespace w4

@@ -1,5 +1,6 @@
-// M = 1 decode GEMV with INT4 asymmetric group-128 weights:
+// M = 1 decode GEMV with INT4 group-128 weights:
 //   y[n] = sum_k x[k] * (q[n,k] - z[n,k/128]) * s[n,k/128]
+// (asymmetric; symmetric INT4 passes no zero points and takes z = 8)
 // ("Lab 5: Gemma4 end-to-end inference optimisation", section "INT4 fused
 // GEMV": the packed weight is read once, unpacked in registers, scaled and
 // zero-shifted per group and dotted with the activation, never written back).
@@ -27,7 +28,8 @@ cudaError_t launch_gemv_int4(const uint16_t *x, const uint8_t *qw, const uint16_
     a.sz_total = N * (K / 128) * 2;
     a.K = static_cast<int>(K);
     a.G = static_cast<int>(K / 128);
-    return gemv_dispatch<false>(a, st, dev.device, dev.num_sms, dev.max_smem_optin);
+    return z ? gemv_dispatch<false, false>(a, st, dev.device, dev.num_sms, dev.max_smem_optin)
+             : gemv_dispatch<false, true>(a, st, dev.device, dev.num_sms, dev.max_smem_optin);
 }
 
 }  // namespace w4

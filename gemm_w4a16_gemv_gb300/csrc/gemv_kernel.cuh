@@ -42,7 +42,7 @@ struct GemvParams {
     const uint16_t *x;
     const uint8_t *qw;
     const uint16_t *s;
-    const uint16_t *z;      // INT4 only
+    const uint16_t *z;      // INT4 only; null: symmetric INT4 (zero point 8)
     const int32_t *ids;     // FP4 only
     uint16_t *y;
     unsigned int *status;
@@ -80,7 +80,7 @@ struct GemvHeader {
 
 __device__ __forceinline__ int64_t gemv_even_floor(int64_t v) { return v & ~int64_t(1); }
 
-template <bool FP4, int CW, int TT, int UPT, int RPT>
+template <bool FP4, int CW, int TT, int UPT, int RPT, bool SYM>
 __device__ __forceinline__ void gemv_producer(const GemvParams &a, GemvHeader<CW, RPT> &h,
                                               unsigned char *stage0, int64_t begin, int64_t end,
                                               int lane) {
@@ -152,7 +152,7 @@ __device__ __forceinline__ void gemv_producer(const GemvParams &a, GemvHeader<CW
                 const uint64_t left = static_cast<uint64_t>(a.sz_total) - o;
                 const uint32_t n = left < 16 ? static_cast<uint32_t>(left) : 16u;
                 cp_async_16_zfill(reinterpret_cast<unsigned char *>(ss) + (o - lo16), gs + o, n);
-                if (!FP4) cp_async_16_zfill(reinterpret_cast<unsigned char *>(sz) + (o - lo16), gz + o, n);
+                if (!FP4 && !SYM) cp_async_16_zfill(reinterpret_cast<unsigned char *>(sz) + (o - lo16), gz + o, n);
             }
         }
         cp_async_arrive_noinc(&h.full[slot]);
@@ -207,12 +207,13 @@ __device__ __forceinline__ void gemv_prefetch_range(const void *base, uint64_t l
         prefetch_l2_line(p + o);
 }
 
+template <bool SYM>
 __device__ __forceinline__ void gemv_prefetch_groups(const GemvParams &a, int64_t begin, int64_t end, int tid,
                                                      int nthreads) {
     const int64_t rows = gemv_prefetch_rows(a, begin, end);
     const uint64_t g0 = static_cast<uint64_t>(begin) * a.G * 2, g1 = static_cast<uint64_t>(begin + rows) * a.G * 2;
     gemv_prefetch_range(a.s, g0, g1, tid, nthreads);
-    gemv_prefetch_range(a.z, g0, g1, tid, nthreads);
+    if (!SYM) gemv_prefetch_range(a.z, g0, g1, tid, nthreads);
 }
 
 // Activation conversion, once per CTA, one 32-element unit per consumer
@@ -293,7 +294,7 @@ __device__ __forceinline__ void gemv_release_stage(GemvHeader<CW, RPT> &h, const
 // the x registers are loaded in the same rotated order, so indexing stays
 // static.  Products are exact integer dot products (DP2A); per (row, group):
 //   y += s * 2^(e-14) * (dot - z * xsum).
-template <int CW, int TT, int RPT>
+template <int CW, int TT, int RPT, bool SYM>
 __device__ __forceinline__ void gemv_consume_int4(const GemvParams &a, GemvHeader<CW, RPT> &h,
                                                   const unsigned char *stage0, const unsigned char *xs,
                                                   int64_t begin, int64_t end, int warp, int lane) {
@@ -364,7 +365,7 @@ __device__ __forceinline__ void gemv_consume_int4(const GemvParams &a, GemvHeade
                 const int dot = lo[rr] + (hi[rr] >> 4);  // hi is a multiple of 16; |dot| < 2^24
                 const int gi = (rbase + rr) * a.G + g;
                 const float sf = f16_bits_to_f32(ss[gi]) * pw;
-                const float zf = f16_bits_to_f32(sz[gi]);
+                const float zf = SYM ? 8.0f : f16_bits_to_f32(sz[gi]);  // symmetric: the midpoint 8
                 part[rr] = sf * fmaf(-zf, xsum, static_cast<float>(dot));
             }
         }
@@ -452,7 +453,7 @@ __device__ __forceinline__ void gemv_consume_fp4(const GemvParams &a, GemvHeader
     }
 }
 
-template <bool FP4, int CW, int TT, int UPT, int RPT>
+template <bool FP4, int CW, int TT, int UPT, int RPT, bool SYM>
 __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_stream_kernel(const GemvParams a) {
     using Header = GemvHeader<CW, RPT>;
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -489,7 +490,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_stream_kernel(const Gem
         // test-only injection: no stage is ever issued, so the consumers'
         // first waits run out and the launch ends with the timeout status
         if (!(a.inject & kInjectStallPipeline))
-            gemv_producer<FP4, CW, TT, UPT, RPT>(a, h, stage0, begin, end, lane);
+            gemv_producer<FP4, CW, TT, UPT, RPT, SYM>(a, h, stage0, begin, end, lane);
         return;
     }
 
@@ -498,14 +499,14 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_stream_kernel(const Gem
     // coherence).  The activation follows the stream order: the consumers
     // convert it once per CTA into shared memory, then each thread copies the
     // part it owns into registers.
-    if (!FP4) gemv_prefetch_groups(a, begin, end, threadIdx.x, CW * 32);
+    if (!FP4) gemv_prefetch_groups<SYM>(a, begin, end, threadIdx.x, CW * 32);
     pdl_wait();
     gemv_convert_x<FP4, CW>(a, smem + a.x_off, warp, lane);
     named_bar_sync(1, CW * 32);
     if constexpr (FP4)
         gemv_consume_fp4<CW, TT, UPT, RPT>(a, h, stage0, smem + a.x_off, begin, end, warp, lane);
     else
-        gemv_consume_int4<CW, TT, RPT>(a, h, stage0, smem + a.x_off, begin, end, warp, lane);
+        gemv_consume_int4<CW, TT, RPT, SYM>(a, h, stage0, smem + a.x_off, begin, end, warp, lane);
 }
 
 // Host side: pick the team shape for K, size the stages, launch one CTA per SM.
@@ -541,10 +542,10 @@ inline GemvShape gemv_choose_shape(int CW, int UPR, int row_bytes, int stage_tar
 constexpr int kGemvCW = 16;             // consumer warps per CTA
 constexpr int kGemvStageTarget = 32768; // packed weight bytes per stage (upper aim)
 
-template <bool FP4, int TT, int UPT, int RPT>
+template <bool FP4, int TT, int UPT, int RPT, bool SYM>
 cudaError_t gemv_launch(GemvParams a, cudaStream_t st, int device, int num_sms, int max_smem) {
     constexpr int CW = kGemvCW;
-    auto kern = gemv_stream_kernel<FP4, CW, TT, UPT, RPT>;
+    auto kern = gemv_stream_kernel<FP4, CW, TT, UPT, RPT, SYM>;
     const int header = (static_cast<int>(sizeof(GemvHeader<CW, RPT>)) + 127) & ~127;
     a.x_off = header;
     a.stage_off = (a.x_off + (a.K / 32) * 72 + 256 + 1023) & ~1023;  // converted x: planes, then (xsum, pw)
@@ -587,7 +588,9 @@ cudaError_t gemv_launch(GemvParams a, cudaStream_t st, int device, int num_sms, 
 //        covering K/128 groups; RPT = 2 rows per thread while a stage stays
 //        within the stage target, else 1.
 //  FP4:  TT threads x UPT units of 32 codes cover a row (gemv_choose_shape).
-template <bool FP4>
+// SYM: symmetric INT4 (no zero points), its own kernel instances so that the
+// asymmetric ones carry no test for it.
+template <bool FP4, bool SYM = false>
 cudaError_t gemv_dispatch(GemvParams a, cudaStream_t st, int device, int num_sms, int max_smem) {
     const int row_bytes = a.K / 2;
     GemvShape sh = {0, 0, 0};
@@ -612,8 +615,8 @@ cudaError_t gemv_dispatch(GemvParams a, cudaStream_t st, int device, int num_sms
     if constexpr (FP4) {
 #define W4_GEMV_CASE(TT_, UPT_)                                                                   \
     if (sh.TT == TT_ && sh.UPT == UPT_)                                                           \
-        return sh.RPT == 4 ? gemv_launch<true, TT_, UPT_, 4>(a, st, device, num_sms, max_smem)    \
-                           : gemv_launch<true, TT_, UPT_, 2>(a, st, device, num_sms, max_smem);
+        return sh.RPT == 4 ? gemv_launch<true, TT_, UPT_, 4, false>(a, st, device, num_sms, max_smem) \
+                           : gemv_launch<true, TT_, UPT_, 2, false>(a, st, device, num_sms, max_smem);
         W4_GEMV_CASE(32, 2)
         W4_GEMV_CASE(64, 2)
         W4_GEMV_CASE(128, 2)
@@ -623,8 +626,8 @@ cudaError_t gemv_dispatch(GemvParams a, cudaStream_t st, int device, int num_sms
     } else {
 #define W4_GEMV_CASE(TT_)                                                                         \
     if (sh.TT == TT_)                                                                             \
-        return sh.RPT == 2 ? gemv_launch<false, TT_, 1, 2>(a, st, device, num_sms, max_smem)      \
-                           : gemv_launch<false, TT_, 1, 1>(a, st, device, num_sms, max_smem);
+        return sh.RPT == 2 ? gemv_launch<false, TT_, 1, 2, SYM>(a, st, device, num_sms, max_smem) \
+                           : gemv_launch<false, TT_, 1, 1, SYM>(a, st, device, num_sms, max_smem);
         W4_GEMV_CASE(32)
         W4_GEMV_CASE(64)
         W4_GEMV_CASE(128)

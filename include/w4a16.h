@@ -63,7 +63,9 @@ typedef enum { W4_OUT_F32 = 0, W4_OUT_BF16 = 1 } w4_out_dtype;
  *   x  : bfloat16 [K]          activation
  *   qw : uint8    [N, K/2]     packed INT4 codes
  *   s  : binary16 [N, K/group] scales
- *   z  : binary16 [N, K/group] zero points
+ *   z  : binary16 [N, K/group] zero points, or NULL for symmetric INT4:
+ *        the zero point is then the code midpoint 8 for every group ("Lab 5",
+ *        section "Quantisation correctness": the symmetric GPTQ variant)
  *   y  : bfloat16 [N]          output (overwritten)
  * Requires group == 128, N >= 1, 128 <= K <= 16384, K % 128 == 0.
  */
@@ -76,7 +78,8 @@ int w4a16_gemv(const uint16_t *x, const uint8_t *qw, const uint16_t *s,
  * "INT4 fused GEMV", M = 128 prefill check; here fused: weight tiles are
  * dequantised into shared memory and fed to the tcgen05 tensor cores, so no
  * BF16 weight matrix is written to HBM).
- *   X : bfloat16 [M, K];  qw, s, z as for w4a16_gemv;  Y : bfloat16 [M, N].
+ *   X : bfloat16 [M, K];  qw, s, z as for w4a16_gemv (z may be NULL:
+ *       symmetric INT4);  Y : bfloat16 [M, N].
  * Requires group == 128, K % 128 == 0, 128 <= K <= 16384, N % 16 == 0.  Any
  * M >= 1 is accepted (rows past M in the last tile are masked).
  */
@@ -112,7 +115,8 @@ int fp4_moe_gemv(const uint16_t *x, const uint8_t *qw, const uint16_t *s,
  *   out_dtype W4_OUT_F32 writes binary32, W4_OUT_BF16 writes
  *   round-to-nearest-even bfloat16 of that binary32 value.
  *   qw : uint8 [rows, K/2];  s (and z for INT4) binary16 [rows, K/group];
- *   z must be NULL for FP4;  out : [rows, K] binary32 or bfloat16.
+ *   z must be NULL for FP4; for INT4 a NULL z means symmetric INT4 (z = 8);
+ *   out : [rows, K] binary32 or bfloat16.
  * group must be 128 (INT4) or 32 (FP4); K % group == 0; rows >= 1.
  */
 int w4a16_dequant(int fmt, const uint8_t *qw, const uint16_t *s,
