@@ -15,7 +15,9 @@ What it computes (page titles as published):
   * the problem statement y = x W^T, W = (q - z) * s, FP16 s and z;
   * symmetric INT4 (the symmetric GPTQ variant of "Quantisation correctness")
     in GPTQ's form: z = None means the implicit zero point 8;
-  * the OCP MX definition of E2M1 for the FP4 value table.
+  * the OCP MX definition of E2M1 for the FP4 value table;
+  * the dense BF16 product of the unfused two-pass path ("Triton dequant +
+    cuBLAS"), for the fusion ablation.
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against
 hand-written fixtures, closed forms, brute force and library routines.
@@ -78,6 +80,8 @@ def _load():
         lib.oracle_moe_fp4.argtypes = [P, P, P, P, I64, I64, I64, I64, I64, P,
                                        ctypes.POINTER(ctypes.c_int)]
         lib.oracle_moe_fp4.restype = None
+        lib.oracle_gemm_bf16.argtypes = [P, P, I64, I64, I64, P]
+        lib.oracle_gemm_bf16.restype = None
         _lib = lib
         return lib
 
@@ -211,3 +215,16 @@ def moe_fp4(x, qw, s, ids, E: int, N: int, K: int, group: int = 32):
     _load().oracle_moe_fp4(_ptr(x), _ptr(qw), _ptr(s), _ptr(ids), topk, E, N,
                            K, group, _ptr(Y), ctypes.byref(bad))
     return Y, int(bad.value)
+
+
+# ------------------------------------------------------ two-pass ablation
+
+def gemm_bf16(X, W, K: int) -> np.ndarray:
+    """Y[M, N] (float64) = X W^T for bfloat16 bit arrays X [M, K], W [N, K]
+    (the dense second pass of the unfused dequantise-then-GEMM path)."""
+    X = _c(np.asarray(X).reshape(-1, K), np.uint16)
+    W = _c(np.asarray(W).reshape(-1, K), np.uint16)
+    M, N = X.shape[0], W.shape[0]
+    Y = np.empty((M, N), dtype=np.float64)
+    _load().oracle_gemm_bf16(_ptr(X), _ptr(W), M, N, K, _ptr(Y))
+    return Y

@@ -224,3 +224,23 @@ void oracle_moe_fp4(const uint16_t *x, const uint8_t *qw, const uint16_t *s,
         }
     }
 }
+
+/* ---------------------------------------------------- two-pass ablation */
+
+/* Dense product of bfloat16 matrices, the second pass of the unfused path
+ * ([Lab5] "Triton dequant + cuBLAS": dequantise to a BF16 weight matrix in
+ * memory, then a dense BF16 GEMM): Y[m, n] = sum_k X[m, k] * W[n, k], every
+ * product and the running sum in binary64, k ascending.
+ * X: [M, K] bfloat16; W: [N, K] bfloat16; Y: [M, N] binary64. */
+void oracle_gemm_bf16(const uint16_t *X, const uint16_t *W, int64_t M,
+                      int64_t N, int64_t K, double *Y)
+{
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += oracle_bf16_to_f64(X[m * K + k]) * oracle_bf16_to_f64(W[n * K + k]);
+            Y[m * N + n] = acc;
+        }
+    }
+}

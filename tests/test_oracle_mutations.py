@@ -30,6 +30,7 @@ MUTATIONS = {
     "activation_row": ("X[m * K + k]", "X[k]"),
     "symmetric_zero_point": ("z ? (float)oracle_f16_to_f64(z[n * G + k / g]) : 8.0f;\n                float sf",
                              "z ? (float)oracle_f16_to_f64(z[n * G + k / g]) : 7.0f;\n                float sf"),
+    "bf16_weight_transposed": ("oracle_bf16_to_f64(W[n * K + k])", "oracle_bf16_to_f64(W[k * N + n])"),
     "fp4_scale_index": ("s[r * G + k / g]);\n            W[r * K + k] = v * sf;",
                         "s[r * G]);\n            W[r * K + k] = v * sf;"),
 }

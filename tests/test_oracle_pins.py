@@ -345,3 +345,47 @@ def test_dequant_fp4_matches_table_for_every_byte_pair(byte):
                            group=32)
     assert np.all(W[0, 0::2] == table[byte & 15] * 0.5)
     assert np.all(W[0, 1::2] == table[byte >> 4] * 0.5)
+
+
+# Dense BF16 product (the unfused two-pass path's second pass, "Lab 5",
+# section "Triton dequant + cuBLAS").
+
+def test_gemm_bf16_matches_numpy_matmul_non_square():
+    rng = np.random.default_rng(21)
+    M, N, K = 3, 5, 96
+    X = rand_bf16(rng, (M, K))
+    W = rand_bf16(rng, (N, K))
+    Y = oracle.gemm_bf16(X, W, K=K)
+    ref = bf16_vals(X).reshape(M, K).astype(np.float64) @ bf16_vals(W).reshape(N, K).astype(np.float64).T
+    assert Y.shape == (M, N)
+    assert np.allclose(Y, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_gemm_bf16_identity_weights():
+    rng = np.random.default_rng(22)
+    K = 64
+    W = np.where(np.eye(K, dtype=bool), f16_bf16_one(), 0).astype(np.uint16)
+    X = rand_bf16(rng, (4, K))
+    assert np.array_equal(oracle.gemm_bf16(X, W, K=K), bf16_vals(X).reshape(4, K))
+
+
+def f16_bf16_one():
+    return 0x3F80  # bfloat16 1.0
+
+
+def test_two_pass_within_bf16_weight_rounding_of_fused():
+    # dequantise -> round W to BF16 -> dense product stays within the BF16
+    # rounding bound of the fused result: |d| <= 2^-9 * sum_k |x_k w_k|
+    rng = np.random.default_rng(23)
+    N, K = 6, 384
+    p_qw = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    s = f16_arr(rng.uniform(0.002, 0.02, size=(N, K // 128)))
+    z = f16_arr(rng.integers(0, 16, size=(N, K // 128)).astype(np.float64))
+    X = rand_bf16(rng, (2, K))
+    Wf = oracle.dequant_int4(p_qw, s, z, K=K)
+    Wb = oracle.round_bf16(Wf.astype(np.float64)).reshape(N, K)
+    two = oracle.gemm_bf16(X, Wb, K=K)
+    fused = oracle.gemm_int4(X, p_qw, s, z, K=K)
+    bound = 2.0 ** -9 * (np.abs(bf16_vals(X).reshape(2, K)) @ np.abs(Wf.astype(np.float64)).T)
+    assert np.all(np.abs(two - fused) <= bound + 1e-12)
+    assert np.any(two != fused)  # the rounding is real
