@@ -327,6 +327,33 @@ def per_config(torch, w4, synth, dev, stream, hbm_peak, tf_peak):
         except Exception as e:  # the tensor-core GEMM may be unavailable in this build
             out[name] = {"unavailable": str(e).splitlines()[0][:120]}
         torch.cuda.empty_cache()
+    # the unfused two-pass ablation: dequantise to BF16 weights in HBM, then
+    # the dense BF16 GEMM (both this library's kernels), at the same shapes
+    for M in (128, 2048):
+        name = "two_pass_m%d_15360x3840" % M
+        try:
+            N, K = 15360, 3840
+            sets, _ = make_gemv_sets(torch, synth, dev, N, K, seed=0, nsets=4)
+            Wb = [torch.empty(N, K, dtype=torch.bfloat16, device=dev) for _ in range(4)]
+            X = torch.randn(M, K, device=dev).to(torch.bfloat16)
+            Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+
+            def deq(i):
+                w4.w4a16_dequant(w4.FMT_INT4, sets[i % 4]["qw"], sets[i % 4]["s"], sets[i % 4]["z"],
+                                 out=Wb[i % 4], out_dtype=w4.OUT_BF16)
+
+            t_deq = time_launches(torch, deq, 20, stream)
+            t_mm = time_launches(torch, lambda i: w4.w4a16_bf16_gemm(X, Wb[i % 4], Y), 20, stream)
+            t_two = time_launches(torch, lambda i: (deq(i), w4.w4a16_bf16_gemm(X, Wb[i % 4], Y)), 20, stream)
+            fused = out.get("gemm_m%d_15360x3840" % M, {}).get("us")
+            out[name] = {"us": round(t_two * 1e6, 2), "dequant_us": round(t_deq * 1e6, 2),
+                         "bf16_gemm_us": round(t_mm * 1e6, 2),
+                         "bf16_gemm_TFLOP/s": round(2.0 * M * N * K / t_mm / 1e12, 1),
+                         "fused_speedup": round(t_two * 1e6 / fused, 2) if fused else None}
+            del sets, Wb
+        except Exception as e:
+            out[name] = {"unavailable": str(e).splitlines()[0][:120]}
+        torch.cuda.empty_cache()
     return out
 
 

@@ -19,7 +19,7 @@ import threading
 import torch
 
 __all__ = [
-    "w4a16_gemv", "w4a16_gemm", "fp4_moe_gemv", "w4a16_dequant",
+    "w4a16_gemv", "w4a16_gemm", "fp4_moe_gemv", "w4a16_dequant", "w4a16_bf16_gemm",
     "w4a16_check_device_error", "w4a16_last_error_string", "w4a16_version",
     "w4a16_debug_inject", "INJECT_STALL_PIPELINE",
     "library_path", "W4A16Error", "STATUS", "FMT_INT4", "FMT_FP4",
@@ -43,6 +43,7 @@ _INT = ctypes.c_int
 SIGNATURES = {
     "w4a16_gemv": ([_P, _P, _P, _P, _P, _I64, _I64, _INT, _P], _INT),
     "w4a16_gemm": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _INT, _P], _INT),
+    "w4a16_bf16_gemm": ([_P, _P, _P, _I64, _I64, _I64, _P], _INT),
     "fp4_moe_gemv": ([_P, _P, _P, _P, _INT, _P, _I64, _I64, _I64, _INT, _P], _INT),
     "w4a16_dequant": ([_INT, _P, _P, _P, _P, _INT, _I64, _I64, _INT, _P], _INT),
     "w4a16_check_device_error": ([_P], _INT),
@@ -143,6 +144,20 @@ def w4a16_gemm(X, qw, s, z, Y=None, group: int = 128, stream=None):
         Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
     pY = _need(Y, "Y", torch.bfloat16, M * N, dev)
     _check(lib().w4a16_gemm(pX, pq, ps, pz, pY, M, N, K, group, _stream(stream)))
+    return Y
+
+
+def w4a16_bf16_gemm(X, W, Y=None, stream=None):
+    """Y[M, N] = X[M, K] W[N, K]^T, dense BF16 (the unfused path's GEMM)."""
+    N, K = W.shape[0], W.shape[-1]
+    M = X.numel() // K
+    dev = W.device
+    pX = _need(X, "X", torch.bfloat16, M * K, dev)
+    pW = _need(W, "W", torch.bfloat16, N * K, dev)
+    if Y is None:
+        Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    pY = _need(Y, "Y", torch.bfloat16, M * N, dev)
+    _check(lib().w4a16_bf16_gemm(pX, pW, pY, M, N, K, _stream(stream)))
     return Y
 
 

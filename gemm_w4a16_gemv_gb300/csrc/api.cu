@@ -119,6 +119,24 @@ int w4a16_gemm(const uint16_t *X, const uint8_t *qw, const uint16_t *s,
                     "w4a16_gemm");
 }
 
+int w4a16_bf16_gemm(const uint16_t *X, const uint16_t *W, uint16_t *Y, int64_t M, int64_t N, int64_t K,
+                    void *stream) {
+    if (!X || !W || !Y) return fail(W4A16_ERR_INVALID_ARG, "w4a16_bf16_gemm: null pointer");
+    if (M < 1 || N < 1 || K < 1)
+        return fail(W4A16_ERR_INVALID_ARG, "w4a16_bf16_gemm: M=%lld N=%lld K=%lld must be >= 1", (long long)M,
+                    (long long)N, (long long)K);
+    if (K % 64 != 0) return fail(W4A16_ERR_INVALID_ARG, "w4a16_bf16_gemm: K=%lld not a multiple of 64", (long long)K);
+    if (K > (int64_t(1) << 20) || M > (int64_t(1) << 30) || N > (int64_t(1) << 30) || M * N > (int64_t(1) << 40))
+        return fail(W4A16_ERR_UNSUPPORTED, "w4a16_bf16_gemm: sizes too large");
+    if (!aligned16(X) || !aligned16(W) || !aligned16(Y))
+        return fail(W4A16_ERR_MISALIGNED, "w4a16_bf16_gemm: pointers must be 16-byte aligned");
+    w4::DeviceInfo dev;
+    unsigned int *status;
+    if (int r = device_state(dev, status)) return r;
+    return launched(w4::launch_bf16_gemm(X, W, Y, M, N, K, static_cast<cudaStream_t>(stream), status, dev),
+                    "w4a16_bf16_gemm");
+}
+
 int fp4_moe_gemv(const uint16_t *x, const uint8_t *qw, const uint16_t *s,
                  const int32_t *expert_ids, int topk, uint16_t *y, int64_t E,
                  int64_t N, int64_t K, int group, void *stream) {

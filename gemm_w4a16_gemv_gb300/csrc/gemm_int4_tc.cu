@@ -58,11 +58,10 @@
 // Every wait is bounded; on timeout the status word is set, each role still
 // performs the arrivals the others wait for, and TMEM is released only after
 // every MMA issued has completed.
-#include <mutex>
-
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_common.cuh"
+#include "tma_host.h"
 
 namespace w4 {
 namespace {
@@ -516,23 +515,6 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     cluster_sync();
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    return fn;
-}
 
 }  // namespace
 

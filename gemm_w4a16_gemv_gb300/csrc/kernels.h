@@ -35,4 +35,9 @@ cudaError_t launch_gemm_int4(const uint16_t *X, const uint8_t *qw,
                              int64_t M, int64_t N, int64_t K, cudaStream_t st,
                              unsigned int *status, const DeviceInfo &dev);
 
+// Dense BF16 GEMM Y = X W^T (the second pass of the unfused path).
+cudaError_t launch_bf16_gemm(const uint16_t *X, const uint16_t *W, uint16_t *Y,
+                             int64_t M, int64_t N, int64_t K, cudaStream_t st,
+                             unsigned int *status, const DeviceInfo &dev);
+
 }  // namespace w4

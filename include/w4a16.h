@@ -88,6 +88,19 @@ int w4a16_gemm(const uint16_t *X, const uint8_t *qw, const uint16_t *s,
                int64_t K, int group, void *stream);
 
 /*
+ * Dense BF16 GEMM, Y[m, n] = sum_k X[m, k] * W[n, k] on the tensor cores:
+ * the second pass of the unfused path ("Lab 5", section "Triton dequant +
+ * cuBLAS": dequantise to a BF16 weight matrix in memory, then a dense GEMM).
+ * With w4a16_dequant (W4_OUT_BF16) it forms the two-pass ablation of the
+ * fused w4a16_gemm, measuring what the fusion saves.
+ *   X : bfloat16 [M, K];  W : bfloat16 [N, K];  Y : bfloat16 [M, N]
+ *       (binary32 accumulation, round-to-nearest-even output).
+ * Requires K % 64 == 0, M, N >= 1.
+ */
+int w4a16_bf16_gemm(const uint16_t *X, const uint16_t *W, uint16_t *Y,
+                    int64_t M, int64_t N, int64_t K, void *stream);
+
+/*
  * Batched-expert FP4 GEMV for one token ("DeepSeek V4 Triton FP4
  * optimisation in practice": six routed experts per token; stacking the
  * experts on the host cost 20% end to end, so all experts run in one launch

@@ -28,7 +28,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("w4a16_gemv", "w4a16_gemm", "fp4_moe_gemv", "w4a16_dequant",
+    for n in ("w4a16_gemv", "w4a16_gemm", "fp4_moe_gemv", "w4a16_dequant", "w4a16_bf16_gemm",
               "w4a16_check_device_error", "w4a16_last_error_string", "w4a16_version",
               "w4a16_debug_inject"):
         assert n in names
@@ -71,6 +71,10 @@ def test_host_validation_codes(libw4):
     assert _call(libw4, "fp4_moe_gemv", A, A, A, A + 2, 2, A, 4, 8, 128, 32, None) == 3
     assert _call(libw4, "w4a16_dequant", 1, A, A, A, A, 0, 4, 128, 32, None) == 1
     assert _call(libw4, "w4a16_dequant", 0, A, A, A, A, 2, 4, 128, 128, None) == 1
+    assert _call(libw4, "w4a16_dequant", 0, A, A, A, A, 0, 4, 128, 64, None) == 2
+    assert _call(libw4, "w4a16_bf16_gemm", None, A, A, 4, 16, 128, None) == 1
+    assert _call(libw4, "w4a16_bf16_gemm", A, A, A, 4, 16, 96, None) == 1
+    assert _call(libw4, "w4a16_bf16_gemm", A, A + 4, A, 4, 16, 128, None) == 3
     assert _call(libw4, "w4a16_dequant", 0, A, A, A, A, 0, 4, 128, 64, None) == 2
     msg = _call(libw4, "w4a16_last_error_string").decode()
     assert "group" in msg
