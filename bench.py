@@ -297,6 +297,23 @@ def per_config(torch, w4, synth, dev, stream, hbm_peak, tf_peak):
         out[name] = {"us": round(t * 1e6, 2), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm_peak, 3)}
         del sets
         torch.cuda.empty_cache()
+    # decode-sized batches through w4a16_gemm: the M rows share one pass over
+    # the weights (bytes: weights + scales/zeros once, M activations/outputs)
+    N, K = UP
+    nsets = L2_SETS
+    sets, _ = make_gemv_sets(torch, synth, dev, N, K, seed=0, nsets=nsets)
+    for M in (2, 4):
+        X = torch.randn(M, K, device=dev).to(torch.bfloat16)
+        Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        t = time_launches(torch, lambda i: w4.w4a16_gemm(X, sets[i % nsets]["qw"], sets[i % nsets]["s"],
+                                                          sets[i % nsets]["z"], Y), 40, stream)
+        nb = gemv_bytes(N, K) + (M - 1) * (2 * K + 2 * N)
+        m1 = out["gemv_up_15360x3840"]["us"]
+        out["decode_batch_m%d_15360x3840" % M] = {"us": round(t * 1e6, 2), "GB/s": round(nb / t / 1e9, 1),
+                                                  "frac_hbm": round(nb / t / 1e9 / hbm_peak, 3),
+                                                  "vs_m_single_launches": round(t * 1e6 / (M * m1), 2)}
+    del sets
+    torch.cuda.empty_cache()
     # MoE FP4: 64 experts resident (~1 GB), 6 selected per launch
     E, N, K, topk = 64, 4096, 7168, 6
     m = synth.fp4_moe_problem(E, N, K, topk, seed=0)

@@ -115,6 +115,15 @@ int w4a16_gemm(const uint16_t *X, const uint8_t *qw, const uint16_t *s,
     w4::DeviceInfo dev;
     unsigned int *status;
     if (int r = device_state(dev, status)) return r;
+    // decode-sized batches stream the weights once on the CUDA cores; larger
+    // M goes to the tensor cores
+    if (M == 1)
+        return launched(w4::launch_gemv_int4(X, qw, s, z, Y, N, K, static_cast<cudaStream_t>(stream), status, dev),
+                        "w4a16_gemm (M = 1)");
+    if (M <= 4)
+        return launched(
+            w4::launch_gemv_int4_batched(X, qw, s, z, Y, M, N, K, static_cast<cudaStream_t>(stream), status, dev),
+            "w4a16_gemm (M <= 4)");
     return launched(w4::launch_gemm_int4(X, qw, s, z, Y, M, N, K, static_cast<cudaStream_t>(stream), status, dev),
                     "w4a16_gemm");
 }

@@ -58,7 +58,11 @@ struct GemvParams {
     int x_off;              // byte offset of the converted activation (K/32 * 72 + 256 bytes)
     int stage_bytes;        // 128-aligned
     int stage_off;          // byte offset of stage 0
-    unsigned int inject;    // test-only injection flags (0 normally), kept last
+    unsigned int inject;    // test-only injection flags (0 normally)
+    // batched decode (MV activation vectors, INT4 only), after the hot fields
+    int64_t ldy;            // output row stride (N)
+    int x_stride;           // bytes between the vectors' converted activations
+    int mv_valid;           // vectors actually given (the rest are padding)
 };
 
 struct StageMeta {
@@ -80,7 +84,7 @@ struct GemvHeader {
 
 __device__ __forceinline__ int64_t gemv_even_floor(int64_t v) { return v & ~int64_t(1); }
 
-template <bool FP4, int CW, int TT, int UPT, int RPT, bool SYM>
+template <bool FP4, int CW, int TT, int UPT, int RPT, bool SYM, int MV>
 __device__ __forceinline__ void gemv_producer(const GemvParams &a, GemvHeader<CW, RPT> &h,
                                               unsigned char *stage0, int64_t begin, int64_t end,
                                               int lane) {
@@ -91,12 +95,26 @@ __device__ __forceinline__ void gemv_producer(const GemvParams &a, GemvHeader<CW
     // the slot is reused, and its partials sit in the half of psum indexed by
     // the block's phase parity, which the slot's next block does not touch.
     auto finalize = [&](int slot, int par, const StageMeta m) {
-        for (int r = lane; r < m.rows; r += 32) {
-            const int team = r / RPT, rr = r - team * RPT;
-            float acc = 0.0f;
+        if constexpr (MV == 1) {
+            for (int r = lane; r < m.rows; r += 32) {
+                const int team = r / RPT, rr = r - team * RPT;
+                float acc = 0.0f;
 #pragma unroll
-            for (int w = 0; w < WPT; ++w) acc += h.psum[slot][par][team * WPT + w][rr];
-            a.y[m.vrow + r] = m.valid ? f32_to_bf16_bits(acc) : static_cast<uint16_t>(0);
+                for (int w = 0; w < WPT; ++w) acc += h.psum[slot][par][team * WPT + w][rr];
+                a.y[m.vrow + r] = m.valid ? f32_to_bf16_bits(acc) : static_cast<uint16_t>(0);
+            }
+        } else {
+            // batched: vector v's rows were reduced by its own teams
+            constexpr int TV = (CW * 32 / TT) / MV;  // teams per vector
+            for (int idx = lane; idx < MV * m.rows; idx += 32) {
+                const int vec = idx / m.rows, r = idx - vec * m.rows;
+                if (vec >= a.mv_valid) continue;
+                const int team = vec * TV + r / RPT, rr = r % RPT;
+                float acc = 0.0f;
+#pragma unroll
+                for (int w = 0; w < WPT; ++w) acc += h.psum[slot][par][team * WPT + w][rr];
+                a.y[vec * a.ldy + m.vrow + r] = f32_to_bf16_bits(acc);
+            }
         }
     };
     int slot = 0, phase = 0, issued = 0;
@@ -229,7 +247,8 @@ __device__ __forceinline__ int gemv_x_gp(int G) { return (G + 1) & ~1; }
 __device__ __forceinline__ int gemv_x_consts(int K) { return (K >> 5) * 64 + 256; }
 
 template <bool FP4, int CW>
-__device__ __forceinline__ void gemv_convert_x(const GemvParams &a, unsigned char *xs, int warp, int lane) {
+__device__ __forceinline__ void gemv_convert_x(const GemvParams &a, const uint16_t *x, unsigned char *xs, int warp,
+                                               int lane) {
     uint4 *xw = reinterpret_cast<uint4 *>(xs);
     const int units = a.K >> 5;
     const int gp = gemv_x_gp(a.G);
@@ -245,7 +264,7 @@ __device__ __forceinline__ void gemv_convert_x(const GemvParams &a, unsigned cha
         if (u >= units) u -= units;
         uint32_t xb[16], w[16];
         if (ok) {
-            load_x_unit(a.x + 32 * u, xb);
+            load_x_unit(x + 32 * u, xb);
         } else {
 #pragma unroll
             for (int i = 0; i < 16; ++i) xb[i] = 0u;
@@ -294,11 +313,17 @@ __device__ __forceinline__ void gemv_release_stage(GemvHeader<CW, RPT> &h, const
 // the x registers are loaded in the same rotated order, so indexing stays
 // static.  Products are exact integer dot products (DP2A); per (row, group):
 //   y += s * 2^(e-14) * (dot - z * xsum).
-template <int CW, int TT, int RPT, bool SYM>
+template <int CW, int TT, int RPT, bool SYM, int MV>
 __device__ __forceinline__ void gemv_consume_int4(const GemvParams &a, GemvHeader<CW, RPT> &h,
-                                                  const unsigned char *stage0, const unsigned char *xs,
+                                                  const unsigned char *stage0, const unsigned char *xs0,
                                                   int64_t begin, int64_t end, int warp, int lane) {
-    const int team = threadIdx.x / TT;
+    // batched (MV > 1): the teams split into MV sets, one per activation
+    // vector, each set covering every row of a stage
+    constexpr int TV = (CW * 32 / TT) / MV;  // teams per vector
+    const int team0 = threadIdx.x / TT;
+    const int vec = MV == 1 ? 0 : team0 / TV;
+    const int team = MV == 1 ? team0 : team0 % TV;
+    const unsigned char *xs = MV == 1 ? xs0 : xs0 + vec * a.x_stride;
     const int g = threadIdx.x % TT;
     const bool valid = g < a.G;
     const int gs = valid ? g : 0;
@@ -453,7 +478,7 @@ __device__ __forceinline__ void gemv_consume_fp4(const GemvParams &a, GemvHeader
     }
 }
 
-template <bool FP4, int CW, int TT, int UPT, int RPT, bool SYM>
+template <bool FP4, int CW, int TT, int UPT, int RPT, bool SYM, int MV>
 __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_stream_kernel(const GemvParams a) {
     using Header = GemvHeader<CW, RPT>;
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -490,7 +515,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_stream_kernel(const Gem
         // test-only injection: no stage is ever issued, so the consumers'
         // first waits run out and the launch ends with the timeout status
         if (!(a.inject & kInjectStallPipeline))
-            gemv_producer<FP4, CW, TT, UPT, RPT, SYM>(a, h, stage0, begin, end, lane);
+            gemv_producer<FP4, CW, TT, UPT, RPT, SYM, MV>(a, h, stage0, begin, end, lane);
         return;
     }
 
@@ -501,12 +526,20 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_stream_kernel(const Gem
     // part it owns into registers.
     if (!FP4) gemv_prefetch_groups<SYM>(a, begin, end, threadIdx.x, CW * 32);
     pdl_wait();
-    gemv_convert_x<FP4, CW>(a, smem + a.x_off, warp, lane);
+    if constexpr (MV == 1) {
+        gemv_convert_x<FP4, CW>(a, a.x, smem + a.x_off, warp, lane);
+    } else {
+        // padding vectors (past mv_valid) convert the last given one
+#pragma unroll 1
+        for (int v = 0; v < MV; ++v)
+            gemv_convert_x<FP4, CW>(a, a.x + static_cast<int64_t>(min(v, a.mv_valid - 1)) * a.K,
+                                    smem + a.x_off + v * a.x_stride, warp, lane);
+    }
     named_bar_sync(1, CW * 32);
     if constexpr (FP4)
         gemv_consume_fp4<CW, TT, UPT, RPT>(a, h, stage0, smem + a.x_off, begin, end, warp, lane);
     else
-        gemv_consume_int4<CW, TT, RPT, SYM>(a, h, stage0, smem + a.x_off, begin, end, warp, lane);
+        gemv_consume_int4<CW, TT, RPT, SYM, MV>(a, h, stage0, smem + a.x_off, begin, end, warp, lane);
 }
 
 // Host side: pick the team shape for K, size the stages, launch one CTA per SM.
@@ -542,13 +575,14 @@ inline GemvShape gemv_choose_shape(int CW, int UPR, int row_bytes, int stage_tar
 constexpr int kGemvCW = 16;             // consumer warps per CTA
 constexpr int kGemvStageTarget = 32768; // packed weight bytes per stage (upper aim)
 
-template <bool FP4, int TT, int UPT, int RPT, bool SYM>
+template <bool FP4, int TT, int UPT, int RPT, bool SYM, int MV = 1>
 cudaError_t gemv_launch(GemvParams a, cudaStream_t st, int device, int num_sms, int max_smem) {
     constexpr int CW = kGemvCW;
-    auto kern = gemv_stream_kernel<FP4, CW, TT, UPT, RPT, SYM>;
+    auto kern = gemv_stream_kernel<FP4, CW, TT, UPT, RPT, SYM, MV>;
     const int header = (static_cast<int>(sizeof(GemvHeader<CW, RPT>)) + 127) & ~127;
     a.x_off = header;
-    a.stage_off = (a.x_off + (a.K / 32) * 72 + 256 + 1023) & ~1023;  // converted x: planes, then (xsum, pw)
+    a.x_stride = (a.K / 32) * 72 + 256;  // converted x: planes, then (xsum, pw); a multiple of 16
+    a.stage_off = (a.x_off + MV * a.x_stride + 1023) & ~1023;
     int stages = (max_smem - a.stage_off) / a.stage_bytes;
     if (stages > kGemvMaxStages) stages = kGemvMaxStages;
     if (stages < 2) return cudaErrorInvalidValue;
@@ -589,9 +623,12 @@ cudaError_t gemv_launch(GemvParams a, cudaStream_t st, int device, int num_sms, 
 //        within the stage target, else 1.
 //  FP4:  TT threads x UPT units of 32 codes cover a row (gemv_choose_shape).
 // SYM: symmetric INT4 (no zero points), its own kernel instances so that the
-// asymmetric ones carry no test for it.
-template <bool FP4, bool SYM = false>
+// asymmetric ones carry no test for it.  MV > 1 (INT4): MV activation vectors
+// share one pass over the weights; each thread then takes MV rows per stage
+// (RPT = MV) and a stage holds one row per team.
+template <bool FP4, bool SYM = false, int MV = 1>
 cudaError_t gemv_dispatch(GemvParams a, cudaStream_t st, int device, int num_sms, int max_smem) {
+    static_assert(MV == 1 || !FP4, "batched vectors: INT4 only");
     const int row_bytes = a.K / 2;
     GemvShape sh = {0, 0, 0};
     if (FP4) {
@@ -603,11 +640,16 @@ cudaError_t gemv_dispatch(GemvParams a, cudaStream_t st, int device, int num_sms
             if (tt >= a.G) sh = {tt, 1, 0};
         if (sh.TT != 0) {
             const int teams = kGemvCW * 32 / sh.TT;
-            sh.RPT = (teams * 2 * row_bytes <= kGemvStageTarget && teams * 2 <= kGemvMaxRB) ? 2 : 1;
+            if (MV > 1) {
+                if (teams % MV != 0) return cudaErrorInvalidValue;
+                sh.RPT = MV;
+            } else {
+                sh.RPT = (teams * 2 * row_bytes <= kGemvStageTarget && teams * 2 <= kGemvMaxRB) ? 2 : 1;
+            }
         }
     }
     if (sh.TT == 0) return cudaErrorInvalidValue;
-    a.RB = (kGemvCW * 32 / sh.TT) * sh.RPT;
+    a.RB = (kGemvCW * 32 / sh.TT) * sh.RPT / MV;
     if (a.RB > kGemvMaxRB) return cudaErrorInvalidValue;
     a.w_bytes = a.RB * row_bytes;
     a.sz_bytes = ((a.RB * a.G * 2) + 32 + 15) & ~15;  // + slack for the 16-byte-aligned superset
@@ -623,7 +665,7 @@ cudaError_t gemv_dispatch(GemvParams a, cudaStream_t st, int device, int num_sms
         W4_GEMV_CASE(256, 2)
         W4_GEMV_CASE(32, 1)
 #undef W4_GEMV_CASE
-    } else {
+    } else if constexpr (MV == 1) {
 #define W4_GEMV_CASE(TT_)                                                                         \
     if (sh.TT == TT_)                                                                             \
         return sh.RPT == 2 ? gemv_launch<false, TT_, 1, 2, SYM>(a, st, device, num_sms, max_smem) \
@@ -632,6 +674,10 @@ cudaError_t gemv_dispatch(GemvParams a, cudaStream_t st, int device, int num_sms
         W4_GEMV_CASE(64)
         W4_GEMV_CASE(128)
 #undef W4_GEMV_CASE
+    } else {
+        if (sh.TT == 32) return gemv_launch<false, 32, 1, MV, SYM, MV>(a, st, device, num_sms, max_smem);
+        if (sh.TT == 64) return gemv_launch<false, 64, 1, MV, SYM, MV>(a, st, device, num_sms, max_smem);
+        if (sh.TT == 128) return gemv_launch<false, 128, 1, MV, SYM, MV>(a, st, device, num_sms, max_smem);
     }
     return cudaErrorInvalidValue;
 }

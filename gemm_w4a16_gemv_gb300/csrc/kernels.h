@@ -24,6 +24,12 @@ cudaError_t launch_gemv_int4(const uint16_t *x, const uint8_t *qw,
                              int64_t N, int64_t K, cudaStream_t st,
                              unsigned int *status, const DeviceInfo &dev);
 
+// M = 2..4 rows through the streaming GEMV (one pass over the weights).
+cudaError_t launch_gemv_int4_batched(const uint16_t *X, const uint8_t *qw,
+                                     const uint16_t *s, const uint16_t *z, uint16_t *Y,
+                                     int64_t M, int64_t N, int64_t K, cudaStream_t st,
+                                     unsigned int *status, const DeviceInfo &dev);
+
 cudaError_t launch_moe_fp4(const uint16_t *x, const uint8_t *qw,
                            const uint16_t *s, const int32_t *ids, int topk,
                            uint16_t *y, int64_t E, int64_t N, int64_t K,
