@@ -246,6 +246,45 @@ __device__ __forceinline__ void gemv_prefetch_groups(const GemvParams &a, int64_
 __device__ __forceinline__ int gemv_x_gp(int G) { return (G + 1) & ~1; }
 __device__ __forceinline__ int gemv_x_consts(int K) { return (K >> 5) * 64 + 256; }
 
+// One 32-element unit u of activation x into the planes at xs (the layout
+// described above): the batched conversion's body.
+template <bool FP4>
+__device__ __forceinline__ void gemv_convert_unit(const GemvParams &a, const uint16_t *x, unsigned char *xs, int u,
+                                                  bool ok, int units, int gp) {
+    uint4 *xw = reinterpret_cast<uint4 *>(xs);
+    float2 *xc = reinterpret_cast<float2 *>(xs + gemv_x_consts(a.K));
+    uint32_t xb[16], w[16];
+    if (ok) {
+        load_x_unit(x + 32 * u, xb);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) xb[i] = 0u;
+    }
+    float2 c;
+    if constexpr (FP4) {
+        c = make_float2(0.0f, fp4_x_unit(xb, w));
+    } else {
+        uint32_t m = unit_absmax_bits(xb);
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        const int e = exponent_of_absmax(m);
+        int sum = int4_x_unit(xb, e, w);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        c = make_float2(static_cast<float>(sum), pow2f(e - 14));  // |sum| < 2^23: exact
+    }
+    if (ok) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 q4 = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            if (FP4) xw[i * units + u] = q4;
+            else xw[(4 * (u & 3) + i) * gp + (u >> 2)] = q4;
+        }
+        if (FP4) xc[u] = c;
+        else if ((u & 3) == 0) xc[u >> 2] = c;
+    }
+}
+
 template <bool FP4, int CW>
 __device__ __forceinline__ void gemv_convert_x(const GemvParams &a, const uint16_t *x, unsigned char *xs, int warp,
                                                int lane) {
@@ -292,6 +331,26 @@ __device__ __forceinline__ void gemv_convert_x(const GemvParams &a, const uint16
             if (FP4) xc[u] = c;
             else if ((u & 3) == 0) xc[u >> 2] = c;
         }
+    }
+}
+
+// Batched INT4 (MV > 1): the MV vectors (x0 + v K, padding vectors repeating
+// the last given one) converted in one pass over MV * U units, vector v into
+// its region xs0 + v * x_stride; K % 128 == 0 keeps each group's four lanes
+// within one vector.
+template <int CW, int MV>
+__device__ __forceinline__ void gemv_convert_x_batched(const GemvParams &a, const uint16_t *x0, unsigned char *xs0,
+                                                       int warp, int lane) {
+    const int units = a.K >> 5;
+    const int gp = gemv_x_gp(a.G);
+    const int rot = 4 * static_cast<int>((blockIdx.x * 7u) % static_cast<unsigned>(units >> 2));
+    for (int u0 = warp * 32; u0 < MV * units; u0 += CW * 32) {  // warp-uniform
+        const bool ok = u0 + lane < MV * units;
+        const int v = ok ? (u0 + lane) / units : 0;
+        int u = u0 + lane - v * units + rot;
+        if (u >= units) u -= units;
+        gemv_convert_unit<false>(a, x0 + static_cast<int64_t>(min(v, a.mv_valid - 1)) * a.K, xs0 + v * a.x_stride,
+                                 u, ok, units, gp);
     }
 }
 
@@ -526,15 +585,10 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_stream_kernel(const Gem
     // part it owns into registers.
     if (!FP4) gemv_prefetch_groups<SYM>(a, begin, end, threadIdx.x, CW * 32);
     pdl_wait();
-    if constexpr (MV == 1) {
+    if constexpr (MV == 1)
         gemv_convert_x<FP4, CW>(a, a.x, smem + a.x_off, warp, lane);
-    } else {
-        // padding vectors (past mv_valid) convert the last given one
-#pragma unroll 1
-        for (int v = 0; v < MV; ++v)
-            gemv_convert_x<FP4, CW>(a, a.x + static_cast<int64_t>(min(v, a.mv_valid - 1)) * a.K,
-                                    smem + a.x_off + v * a.x_stride, warp, lane);
-    }
+    else
+        gemv_convert_x_batched<CW, MV>(a, a.x, smem + a.x_off, warp, lane);
     named_bar_sync(1, CW * 32);
     if constexpr (FP4)
         gemv_consume_fp4<CW, TT, UPT, RPT>(a, h, stage0, smem + a.x_off, begin, end, warp, lane);
