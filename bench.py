@@ -341,7 +341,7 @@ def per_config(torch, w4, synth, dev, stream, hbm_peak, tf_peak):
             tf = 2.0 * M * N * K / t / 1e12
             out[name] = {"us": round(t * 1e6, 2), "TFLOP/s": round(tf, 1), "frac_bf16": round(tf / tf_peak, 3)}
             del sets
-        except Exception as e:  # the tensor-core GEMM may be unavailable in this build
+        except Exception as e:  # the tensor-core GEMM may be unavailable on this device
             out[name] = {"unavailable": str(e).splitlines()[0][:120]}
         torch.cuda.empty_cache()
     # the unfused two-pass ablation: dequantise to BF16 weights in HBM, then
