@@ -282,6 +282,83 @@ def time_launches(torch, fn, n, stream):
     return e0.elapsed_time(e1) * 1e-3 / n
 
 
+# The pages' 48-layer decode step (Gemma4-12B: hidden 3840, 16 query heads and
+# 8 key/value heads of 256, MLP 15360, vocabulary 262144): 40 sliding-window
+# layers of 7 linears (q, k, v, o, gate, up, down) and 8 global layers of 6
+# (keys and values shared: no v), 328 linears, then the vocabulary GEMV.
+STEP_H, STEP_Q, STEP_KV, STEP_F, STEP_V = 3840, 4096, 2048, 15360, 262144
+STEP_SLIDING, STEP_GLOBAL = 40, 8
+
+
+def decode_step_ops(torch, synth, dev):
+    """The step's 329 INT4 linears as (x, qw, s, z, y) tuples, each with its
+    own weight copy (6.2 GB in all, so every step streams from HBM).  Scales
+    are drawn so that a linear keeps the activations' magnitude (mean scale
+    1 / (6.5 sqrt(K)), 6.5 being the spread of q - z).  Data flow through
+    activation buffers: q, k, v, gate, up read the hidden state h; o reads q
+    (the attention is not on this path) and writes h; down reads up and
+    writes h; the vocabulary GEMV reads h."""
+    protos = {}
+
+    def weights(N, K):
+        if (N, K) not in protos:
+            m = 1.0 / (6.5 * K ** 0.5)
+            p = synth.int4_problem(N, K, seed=N + K, s_range=(0.5 * m, 1.5 * m))
+            protos[(N, K)] = (torch.from_numpy(p["qw"]).to(dev),
+                              torch.from_numpy(p["s"]).view(torch.float16).to(dev),
+                              torch.from_numpy(p["z"]).view(torch.float16).to(dev))
+        return tuple(t.clone() for t in protos[(N, K)])
+
+    H, Q, KV, F = STEP_H, STEP_Q, STEP_KV, STEP_F
+    buf = {n: torch.zeros(k, dtype=torch.bfloat16, device=dev)
+           for n, k in (("h", H), ("q", Q), ("k", KV), ("v", KV), ("gate", F), ("up", F))}
+    buf["h"].copy_(torch.from_numpy(synth.normal_bf16(synth.Stream(5), (H,))).view(torch.bfloat16))
+    logits = torch.empty(STEP_V, dtype=torch.bfloat16, device=dev)
+    ops = []
+    for layer in range(STEP_SLIDING + STEP_GLOBAL):
+        proj = [("h", "q", Q, H), ("h", "k", KV, H)]
+        if layer < STEP_SLIDING:
+            proj.append(("h", "v", KV, H))
+        proj += [("q", "h", H, Q), ("h", "gate", F, H), ("h", "up", F, H), ("up", "h", H, F)]
+        for src, dst, N, K in proj:
+            ops.append((buf[src], *weights(N, K), buf[dst]))
+    ops.append((buf["h"], *weights(STEP_V, H), logits))
+    protos.clear()
+    return ops
+
+
+def decode_step(torch, w4, synth, dev, stream, hbm_peak):
+    """The decode step replayed from one CUDA graph, against the same launches
+    made one by one from the host (w4a16_linear_sequence)."""
+    ops = decode_step_ops(torch, synth, dev)
+    nbytes = sum(gemv_bytes(op[1].shape[0], 2 * op[1].shape[1]) for op in ops)
+    arr = w4.w4a16_linear_array(ops)
+    g = w4.w4a16_graph_create(ops)
+    try:
+        t_graph = time_launches(torch, lambda i: g.launch(), 20, stream)
+        t_seq = time_launches(torch, lambda i: w4.w4a16_linear_sequence(arr, count=len(ops)), 20, stream)
+        # host time of one call of each (what a decode loop pays per step)
+        torch.cuda.synchronize()
+        h0 = time.perf_counter()
+        for _ in range(5):
+            w4.w4a16_linear_sequence(arr, count=len(ops))
+        h1 = time.perf_counter()
+        for _ in range(5):
+            g.launch()
+        h2 = time.perf_counter()
+        torch.cuda.synchronize()
+        status = w4.w4a16_check_device_error()
+    finally:
+        g.destroy()
+    gbs = nbytes / t_graph / 1e9
+    return {"linears": len(ops), "weights_GB": round(nbytes / 1e9, 3), "us": round(t_graph * 1e6, 1),
+            "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm_peak, 3),
+            "host_launched_us": round(t_seq * 1e6, 1),
+            "host_us_per_step": {"sequence_call": round((h1 - h0) / 5 * 1e6, 1),
+                                 "graph_launch": round((h2 - h1) / 5 * 1e6, 1)},
+            "device_status": status}
+
+
 def per_config(torch, w4, synth, dev, stream, hbm_peak, tf_peak):
     """Kernel-only timings of every configuration (launches back to back)."""
     out = {}
@@ -371,6 +448,9 @@ def per_config(torch, w4, synth, dev, stream, hbm_peak, tf_peak):
         except Exception as e:
             out[name] = {"unavailable": str(e).splitlines()[0][:120]}
         torch.cuda.empty_cache()
+    # the whole decode step (328 linears and the vocabulary GEMV) as one graph
+    out["decode_step_328_linears_vocab"] = decode_step(torch, w4, synth, dev, stream, hbm_peak)
+    torch.cuda.empty_cache()
     return out
 
 

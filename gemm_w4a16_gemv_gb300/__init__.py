@@ -22,6 +22,8 @@ __all__ = [
     "w4a16_gemv", "w4a16_gemm", "fp4_moe_gemv", "w4a16_dequant", "w4a16_bf16_gemm",
     "w4a16_check_device_error", "w4a16_last_error_string", "w4a16_version",
     "w4a16_debug_inject", "INJECT_STALL_PIPELINE",
+    "w4a16_linear", "w4a16_linear_array", "w4a16_linear_sequence", "w4a16_graph_create", "w4a16_graph_launch",
+    "w4a16_graph_destroy", "W4A16Graph",
     "library_path", "W4A16Error", "STATUS", "FMT_INT4", "FMT_FP4",
     "OUT_F32", "OUT_BF16",
 ]
@@ -40,12 +42,26 @@ OUT_F32, OUT_BF16 = 0, 1
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
 _INT = ctypes.c_int
+
+
+class w4a16_linear(ctypes.Structure):
+    """One INT4 linear of a sequence (mirrors the C struct)."""
+    _fields_ = [("x", ctypes.c_void_p), ("qw", ctypes.c_void_p), ("s", ctypes.c_void_p),
+                ("z", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
+
+
+_OPS = ctypes.POINTER(w4a16_linear)
 SIGNATURES = {
     "w4a16_gemv": ([_P, _P, _P, _P, _P, _I64, _I64, _INT, _P], _INT),
     "w4a16_gemm": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _INT, _P], _INT),
     "w4a16_bf16_gemm": ([_P, _P, _P, _I64, _I64, _I64, _P], _INT),
     "fp4_moe_gemv": ([_P, _P, _P, _P, _INT, _P, _I64, _I64, _I64, _INT, _P], _INT),
     "w4a16_dequant": ([_INT, _P, _P, _P, _P, _INT, _I64, _I64, _INT, _P], _INT),
+    "w4a16_linear_sequence": ([_OPS, _INT, _INT, _P], _INT),
+    "w4a16_graph_create": ([_OPS, _INT, _INT, ctypes.POINTER(ctypes.c_void_p)], _INT),
+    "w4a16_graph_launch": ([_P, _P], _INT),
+    "w4a16_graph_destroy": ([_P], _INT),
     "w4a16_check_device_error": ([_P], _INT),
     "w4a16_debug_inject": ([ctypes.c_uint], _INT),
     "w4a16_last_error_string": ([], ctypes.c_char_p),
@@ -195,6 +211,81 @@ def w4a16_dequant(fmt: int, qw, s, z=None, out=None, out_dtype: int = OUT_F32,
     po = _need(out, "out", odt, rows * K, dev)
     _check(lib().w4a16_dequant(fmt, pq, ps, pz, po, out_dtype, rows, K, group, _stream(stream)))
     return out
+
+
+def w4a16_linear_array(ops, group: int = 128):
+    """ctypes array of w4a16_linear from (X, qw, s, z, Y) tuples (z may be
+    None), each checked as w4a16_gemm checks its tensors.  The array holds
+    raw addresses only: the caller keeps the tensors alive while it is used."""
+    arr = (w4a16_linear * max(1, len(ops)))()
+    for i, (X, qw, s, z, Y) in enumerate(ops):
+        N = qw.shape[0]
+        K = 2 * qw.shape[-1]
+        M = X.numel() // K
+        dev = qw.device
+        who = "op %d " % i
+        arr[i].x = _need(X, who + "x", torch.bfloat16, M * K, dev)
+        arr[i].qw = _need(qw, who + "qw", torch.uint8, N * K // 2, dev)
+        arr[i].s = _need(s, who + "s", torch.float16, N * (K // group), dev)
+        arr[i].z = _need(z, who + "z", torch.float16, N * (K // group), dev) if z is not None else None
+        arr[i].y = _need(Y, who + "y", torch.bfloat16, M * N, dev)
+        arr[i].M, arr[i].N, arr[i].K = M, N, K
+    return arr
+
+
+def w4a16_linear_sequence(ops, group: int = 128, stream=None, count=None):
+    """Launch the INT4 linears `ops` = [(X, qw, s, z, Y), ...] in order on
+    one stream (each op's X is read after the previous op has finished).
+    `ops` may also be an array from w4a16_linear_array, with `count` ops."""
+    if isinstance(ops, ctypes.Array):
+        arr, n = ops, len(ops) if count is None else int(count)
+    else:
+        arr, n = w4a16_linear_array(ops, group), len(ops)
+    _check(lib().w4a16_linear_sequence(arr, n, group, _stream(stream)))
+
+
+class W4A16Graph:
+    """Handle of a captured linear sequence (w4a16_graph_create).  Keeps the
+    tensors of its ops alive: the graph holds their addresses."""
+
+    def __init__(self, handle, tensors):
+        self._h = handle
+        self._tensors = tensors
+
+    def launch(self, stream=None):
+        w4a16_graph_launch(self, stream)
+
+    def destroy(self):
+        if self._h is not None:
+            h, self._h = self._h, None
+            _check(lib().w4a16_graph_destroy(h))
+            self._tensors = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+def w4a16_graph_create(ops, group: int = 128) -> W4A16Graph:
+    """Capture the linear sequence `ops` once into a CUDA graph on the
+    current device; replay it with w4a16_graph_launch."""
+    arr = w4a16_linear_array(ops, group)
+    h = ctypes.c_void_p()
+    _check(lib().w4a16_graph_create(arr, len(ops), group, ctypes.byref(h)))
+    return W4A16Graph(h, [t for op in ops for t in op if t is not None])
+
+
+def w4a16_graph_launch(graph: W4A16Graph, stream=None) -> None:
+    """Enqueue one replay of a captured sequence on the stream."""
+    if graph._h is None:
+        raise ValueError("graph has been destroyed")
+    _check(lib().w4a16_graph_launch(graph._h, _stream(stream)))
+
+
+def w4a16_graph_destroy(graph: W4A16Graph) -> None:
+    graph.destroy()
 
 
 def w4a16_check_device_error(stream=None) -> int:

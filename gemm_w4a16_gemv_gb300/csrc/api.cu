@@ -4,6 +4,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <new>
 
 #include "w4a16.h"
 #include "common.cuh"
@@ -71,25 +72,92 @@ int launched(cudaError_t e, const char *what) {
     return ok();
 }
 
+// Host checks of one INT4 linear, M = 1 (the GEMV's rules) or any M (the
+// GEMM's rules); `who` prefixes the message.
+int check_gemv_args(const char *who, const void *x, const void *qw, const void *s, const void *z, const void *y,
+                    int64_t N, int64_t K, int group) {
+    if (!x || !qw || !s || !y) return fail(W4A16_ERR_INVALID_ARG, "%s: null pointer", who);
+    if (N < 1 || K < 1)
+        return fail(W4A16_ERR_INVALID_ARG, "%s: N=%lld K=%lld must be >= 1", who, (long long)N, (long long)K);
+    if (group != 128) return fail(W4A16_ERR_UNSUPPORTED, "%s: group %d (only 128)", who, group);
+    if (K % 128 != 0) return fail(W4A16_ERR_INVALID_ARG, "%s: K=%lld not a multiple of the group", who, (long long)K);
+    if (K > 16384) return fail(W4A16_ERR_UNSUPPORTED, "%s: K=%lld > 16384", who, (long long)K);
+    if (N > (int64_t(1) << 31)) return fail(W4A16_ERR_UNSUPPORTED, "%s: N=%lld too large", who, (long long)N);
+    if (!aligned16(x) || !aligned16(qw) || !aligned16(s) || (z && !aligned16(z)) || !aligned16(y))
+        return fail(W4A16_ERR_MISALIGNED, "%s: pointers must be 16-byte aligned", who);
+    return W4A16_OK;
+}
+
+int check_gemm_args(const char *who, const void *X, const void *qw, const void *s, const void *z, const void *Y,
+                    int64_t M, int64_t N, int64_t K, int group) {
+    if (!X || !qw || !s || !Y) return fail(W4A16_ERR_INVALID_ARG, "%s: null pointer", who);
+    if (M < 1 || N < 1 || K < 1)
+        return fail(W4A16_ERR_INVALID_ARG, "%s: M=%lld N=%lld K=%lld must be >= 1", who, (long long)M,
+                    (long long)N, (long long)K);
+    if (group != 128) return fail(W4A16_ERR_UNSUPPORTED, "%s: group %d (only 128)", who, group);
+    if (K % 128 != 0) return fail(W4A16_ERR_INVALID_ARG, "%s: K=%lld not a multiple of the group", who, (long long)K);
+    if (N % 16 != 0) return fail(W4A16_ERR_UNSUPPORTED, "%s: N=%lld not a multiple of 16", who, (long long)N);
+    if (K > 16384) return fail(W4A16_ERR_UNSUPPORTED, "%s: K=%lld > 16384", who, (long long)K);
+    if (M > (int64_t(1) << 30) || N > (int64_t(1) << 30) || M * N > (int64_t(1) << 40))
+        return fail(W4A16_ERR_UNSUPPORTED, "%s: sizes too large", who);
+    if (!aligned16(X) || !aligned16(qw) || !aligned16(s) || (z && !aligned16(z)) || !aligned16(Y))
+        return fail(W4A16_ERR_MISALIGNED, "%s: pointers must be 16-byte aligned", who);
+    return W4A16_OK;
+}
+
+// Decode-sized batches stream the weights once on the CUDA cores (M = 1: the
+// GEMV; M <= 4: the M rows share one pass); larger M goes to the tensor cores.
+cudaError_t launch_int4_linear(const uint16_t *X, const uint8_t *qw, const uint16_t *s, const uint16_t *z,
+                               uint16_t *Y, int64_t M, int64_t N, int64_t K, cudaStream_t st, unsigned int *status,
+                               const w4::DeviceInfo &dev) {
+    if (M == 1) return w4::launch_gemv_int4(X, qw, s, z, Y, N, K, st, status, dev);
+    if (M <= 4) return w4::launch_gemv_int4_batched(X, qw, s, z, Y, M, N, K, st, status, dev);
+    return w4::launch_gemm_int4(X, qw, s, z, Y, M, N, K, st, status, dev);
+}
+
+// The checks of op i of a sequence (M = 1: the GEMV's rules).
+int check_linear(const w4a16_linear &op, int i, int group, const char *fn) {
+    char who[96];
+    snprintf(who, sizeof who, "%s: op %d", fn, i);
+    if (op.M == 1) return check_gemv_args(who, op.x, op.qw, op.s, op.z, op.y, op.N, op.K, group);
+    return check_gemm_args(who, op.x, op.qw, op.s, op.z, op.y, op.M, op.N, op.K, group);
+}
+
+int check_sequence(const w4a16_linear *ops, int count, int group, const char *fn) {
+    if (count < 0) return fail(W4A16_ERR_INVALID_ARG, "%s: count %d < 0", fn, count);
+    if (count > 0 && !ops) return fail(W4A16_ERR_INVALID_ARG, "%s: null ops", fn);
+    for (int i = 0; i < count; ++i)
+        if (int r = check_linear(ops[i], i, group, fn)) return r;
+    return W4A16_OK;
+}
+
+// Launches every op in order; on a launch error returns it and the index.
+cudaError_t launch_sequence(const w4a16_linear *ops, int count, cudaStream_t st, unsigned int *status,
+                            const w4::DeviceInfo &dev, int &failed_at) {
+    for (int i = 0; i < count; ++i) {
+        const w4a16_linear &o = ops[i];
+        cudaError_t e = launch_int4_linear(o.x, o.qw, o.s, o.z, o.y, o.M, o.N, o.K, st, status, dev);
+        if (e != cudaSuccess) {
+            failed_at = i;
+            return e;
+        }
+    }
+    failed_at = -1;
+    return cudaSuccess;
+}
+
 }  // namespace
 
 extern "C" {
 
-int w4a16_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+int w4a16_version(void) { return 1 * 10000 + 1 * 100 + 0; }
 
 const char *w4a16_last_error_string(void) { return g_err; }
 
 int w4a16_gemv(const uint16_t *x, const uint8_t *qw, const uint16_t *s,
                const uint16_t *z, uint16_t *y, int64_t N, int64_t K,
                int group, void *stream) {
-    if (!x || !qw || !s || !y) return fail(W4A16_ERR_INVALID_ARG, "w4a16_gemv: null pointer");
-    if (N < 1 || K < 1) return fail(W4A16_ERR_INVALID_ARG, "w4a16_gemv: N=%lld K=%lld must be >= 1", (long long)N, (long long)K);
-    if (group != 128) return fail(W4A16_ERR_UNSUPPORTED, "w4a16_gemv: group %d (only 128)", group);
-    if (K % 128 != 0) return fail(W4A16_ERR_INVALID_ARG, "w4a16_gemv: K=%lld not a multiple of the group", (long long)K);
-    if (K > 16384) return fail(W4A16_ERR_UNSUPPORTED, "w4a16_gemv: K=%lld > 16384", (long long)K);
-    if (N > (int64_t(1) << 31)) return fail(W4A16_ERR_UNSUPPORTED, "w4a16_gemv: N=%lld too large", (long long)N);
-    if (!aligned16(x) || !aligned16(qw) || !aligned16(s) || (z && !aligned16(z)) || !aligned16(y))
-        return fail(W4A16_ERR_MISALIGNED, "w4a16_gemv: pointers must be 16-byte aligned");
+    if (int r = check_gemv_args("w4a16_gemv", x, qw, s, z, y, N, K, group)) return r;
     w4::DeviceInfo dev;
     unsigned int *status;
     if (int r = device_state(dev, status)) return r;
@@ -100,31 +168,11 @@ int w4a16_gemv(const uint16_t *x, const uint8_t *qw, const uint16_t *s,
 int w4a16_gemm(const uint16_t *X, const uint8_t *qw, const uint16_t *s,
                const uint16_t *z, uint16_t *Y, int64_t M, int64_t N,
                int64_t K, int group, void *stream) {
-    if (!X || !qw || !s || !Y) return fail(W4A16_ERR_INVALID_ARG, "w4a16_gemm: null pointer");
-    if (M < 1 || N < 1 || K < 1)
-        return fail(W4A16_ERR_INVALID_ARG, "w4a16_gemm: M=%lld N=%lld K=%lld must be >= 1", (long long)M,
-                    (long long)N, (long long)K);
-    if (group != 128) return fail(W4A16_ERR_UNSUPPORTED, "w4a16_gemm: group %d (only 128)", group);
-    if (K % 128 != 0) return fail(W4A16_ERR_INVALID_ARG, "w4a16_gemm: K=%lld not a multiple of the group", (long long)K);
-    if (N % 16 != 0) return fail(W4A16_ERR_UNSUPPORTED, "w4a16_gemm: N=%lld not a multiple of 16", (long long)N);
-    if (K > 16384) return fail(W4A16_ERR_UNSUPPORTED, "w4a16_gemm: K=%lld > 16384", (long long)K);
-    if (M > (int64_t(1) << 30) || N > (int64_t(1) << 30) || M * N > (int64_t(1) << 40))
-        return fail(W4A16_ERR_UNSUPPORTED, "w4a16_gemm: sizes too large");
-    if (!aligned16(X) || !aligned16(qw) || !aligned16(s) || (z && !aligned16(z)) || !aligned16(Y))
-        return fail(W4A16_ERR_MISALIGNED, "w4a16_gemm: pointers must be 16-byte aligned");
+    if (int r = check_gemm_args("w4a16_gemm", X, qw, s, z, Y, M, N, K, group)) return r;
     w4::DeviceInfo dev;
     unsigned int *status;
     if (int r = device_state(dev, status)) return r;
-    // decode-sized batches stream the weights once on the CUDA cores; larger
-    // M goes to the tensor cores
-    if (M == 1)
-        return launched(w4::launch_gemv_int4(X, qw, s, z, Y, N, K, static_cast<cudaStream_t>(stream), status, dev),
-                        "w4a16_gemm (M = 1)");
-    if (M <= 4)
-        return launched(
-            w4::launch_gemv_int4_batched(X, qw, s, z, Y, M, N, K, static_cast<cudaStream_t>(stream), status, dev),
-            "w4a16_gemm (M <= 4)");
-    return launched(w4::launch_gemm_int4(X, qw, s, z, Y, M, N, K, static_cast<cudaStream_t>(stream), status, dev),
+    return launched(launch_int4_linear(X, qw, s, z, Y, M, N, K, static_cast<cudaStream_t>(stream), status, dev),
                     "w4a16_gemm");
 }
 
@@ -192,6 +240,92 @@ int w4a16_dequant(int fmt, const uint8_t *qw, const uint16_t *s,
     return launched(w4::launch_dequant(fmt, qw, s, z, out, out_dtype, rows, K, group,
                                        static_cast<cudaStream_t>(stream), dev),
                     "w4a16_dequant");
+}
+
+int w4a16_linear_sequence(const w4a16_linear *ops, int count, int group, void *stream) {
+    if (int r = check_sequence(ops, count, group, "w4a16_linear_sequence")) return r;
+    if (count == 0) return ok();
+    w4::DeviceInfo dev;
+    unsigned int *status;
+    if (int r = device_state(dev, status)) return r;
+    int at = -1;
+    cudaError_t e = launch_sequence(ops, count, static_cast<cudaStream_t>(stream), status, dev, at);
+    if (e != cudaSuccess)
+        return fail(W4A16_ERR_CUDA, "w4a16_linear_sequence: op %d launch: %s (ops before it queued)", at,
+                    cudaGetErrorString(e));
+    return ok();
+}
+
+}  // extern "C"
+
+struct w4a16_graph_s {
+    cudaGraphExec_t exec;
+    int device;
+};
+
+extern "C" {
+
+int w4a16_graph_create(const w4a16_linear *ops, int count, int group, w4a16_graph_t *out) {
+    if (!out) return fail(W4A16_ERR_INVALID_ARG, "w4a16_graph_create: null handle pointer");
+    *out = nullptr;
+    if (count < 1) return fail(W4A16_ERR_INVALID_ARG, "w4a16_graph_create: count %d < 1", count);
+    if (int r = check_sequence(ops, count, group, "w4a16_graph_create")) return r;
+    w4::DeviceInfo dev;
+    unsigned int *status;
+    if (int r = device_state(dev, status)) return r;
+    cudaStream_t cs = nullptr;
+    cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return fail(W4A16_ERR_CUDA, "w4a16_graph_create: stream: %s", cudaGetErrorString(e));
+    // relaxed capture: a launcher's first call per kernel sets the kernel's
+    // shared-memory attribute, which is not a stream operation
+    e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed);
+    if (e != cudaSuccess) {
+        cudaStreamDestroy(cs);
+        return fail(W4A16_ERR_CUDA, "w4a16_graph_create: begin capture: %s", cudaGetErrorString(e));
+    }
+    int at = -1;
+    const cudaError_t le = launch_sequence(ops, count, cs, status, dev, at);
+    cudaGraph_t g = nullptr;
+    e = cudaStreamEndCapture(cs, &g);
+    cudaStreamDestroy(cs);
+    if (le != cudaSuccess || e != cudaSuccess) {
+        if (g) cudaGraphDestroy(g);
+        cudaGetLastError();  // the launch error is reported here, not left pending
+        if (le != cudaSuccess)
+            return fail(W4A16_ERR_CUDA, "w4a16_graph_create: op %d launch: %s", at, cudaGetErrorString(le));
+        return fail(W4A16_ERR_CUDA, "w4a16_graph_create: end capture: %s", cudaGetErrorString(e));
+    }
+    cudaGraphExec_t exec = nullptr;
+    e = cudaGraphInstantiate(&exec, g, 0);
+    cudaGraphDestroy(g);
+    if (e != cudaSuccess) return fail(W4A16_ERR_CUDA, "w4a16_graph_create: instantiate: %s", cudaGetErrorString(e));
+    w4a16_graph_s *h = new (std::nothrow) w4a16_graph_s;
+    if (!h) {
+        cudaGraphExecDestroy(exec);
+        return fail(W4A16_ERR_CUDA, "w4a16_graph_create: out of host memory");
+    }
+    h->exec = exec;
+    h->device = dev.device;
+    *out = h;
+    return ok();
+}
+
+int w4a16_graph_launch(w4a16_graph_t graph, void *stream) {
+    if (!graph) return fail(W4A16_ERR_INVALID_ARG, "w4a16_graph_launch: null graph");
+    const cudaError_t e = cudaGraphLaunch(graph->exec, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return fail(W4A16_ERR_CUDA, "w4a16_graph_launch (graph of device %d): %s", graph->device,
+                    cudaGetErrorString(e));
+    return ok();
+}
+
+int w4a16_graph_destroy(w4a16_graph_t graph) {
+    if (!graph) return ok();
+    // an executable graph still running is released when it completes
+    const cudaError_t e = cudaGraphExecDestroy(graph->exec);
+    delete graph;
+    if (e != cudaSuccess) return fail(W4A16_ERR_CUDA, "w4a16_graph_destroy: %s", cudaGetErrorString(e));
+    return ok();
 }
 
 int w4a16_check_device_error(void *stream) {

@@ -139,6 +139,65 @@ int w4a16_dequant(int fmt, const uint8_t *qw, const uint16_t *s,
                   int64_t K, int group, void *stream);
 
 /*
+ * One INT4 linear of a decode sequence: Y = X W^T exactly as w4a16_gemm
+ * computes it (M = 1 as w4a16_gemv), with the same layouts.
+ *   x  : bfloat16 [M, K];  qw : uint8 [N, K/2];  s : binary16 [N, K/group];
+ *   z  : binary16 [N, K/group] or NULL (symmetric INT4);  y : bfloat16 [M, N].
+ * Requirements: those of w4a16_gemv when M == 1, of w4a16_gemm when M > 1.
+ */
+typedef struct {
+    const uint16_t *x;
+    const uint8_t *qw;
+    const uint16_t *s;
+    const uint16_t *z;
+    uint16_t *y;
+    int64_t M, N, K;
+} w4a16_linear;
+
+/*
+ * A decode step as one call ("Lab 5", sections "CUDA Graph" and
+ * "Performance analysis": a decode step is 328 quantised linears plus the
+ * vocabulary GEMV, and the launch overhead of the short GEMVs is what the
+ * CUDA graph removes).  Launches ops[0 .. count-1] in order on `stream`.
+ * Each op reads its x and writes its y only after the previous op has
+ * finished (only its weight prefetch into L2 may overlap the previous op),
+ * so an op may read the output of any earlier op and may overwrite a buffer
+ * that an earlier op read.  The `ops` array is read during the call only.
+ * Every op is checked before anything is launched: a failed check launches
+ * nothing and the message names the op.  count == 0 launches nothing and
+ * returns W4A16_OK.  A CUDA launch error at op i returns W4A16_ERR_CUDA
+ * with ops 0 .. i-1 already queued.
+ */
+int w4a16_linear_sequence(const w4a16_linear *ops, int count, int group,
+                          void *stream);
+
+/*
+ * The same sequence captured once into a CUDA graph and replayed by
+ * w4a16_graph_launch: one host call per decode step, with the launches
+ * chained on the device.
+ *   w4a16_graph_create  checks every op as w4a16_linear_sequence does (a
+ *       failed check captures nothing), captures the launches on a private
+ *       stream of the current device, instantiates the graph and returns an
+ *       opaque handle in *out (NULL on any failure; count must be >= 1).
+ *       The graph keeps the ops' pointers, not their contents: every buffer
+ *       must stay allocated at the same address until the handle is
+ *       destroyed, and each replay reads the buffers as they are when it
+ *       runs (write the next step's x in place between replays).  The
+ *       injection flags in force at creation are kept by the graph.
+ *   w4a16_graph_launch  enqueues one replay on `stream` (a stream of the
+ *       device the graph was created on); asynchronous like every call.
+ *   w4a16_graph_destroy releases the handle (NULL is accepted); a replay
+ *       still in flight completes first.
+ * The handle is owned by the caller and may be used from one host thread at
+ * a time.
+ */
+typedef struct w4a16_graph_s *w4a16_graph_t;
+int w4a16_graph_create(const w4a16_linear *ops, int count, int group,
+                       w4a16_graph_t *out);
+int w4a16_graph_launch(w4a16_graph_t graph, void *stream);
+int w4a16_graph_destroy(w4a16_graph_t graph);
+
+/*
  * Synchronises `stream`, then reads and clears this device's sticky status.
  * Returns W4A16_OK, W4A16_ERR_TIMEOUT, W4A16_ERR_DEVICE or W4A16_ERR_CUDA.
  */

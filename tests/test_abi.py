@@ -30,7 +30,8 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("w4a16_gemv", "w4a16_gemm", "fp4_moe_gemv", "w4a16_dequant", "w4a16_bf16_gemm",
               "w4a16_check_device_error", "w4a16_last_error_string", "w4a16_version",
-              "w4a16_debug_inject"):
+              "w4a16_debug_inject", "w4a16_linear_sequence", "w4a16_graph_create",
+              "w4a16_graph_launch", "w4a16_graph_destroy"):
         assert n in names
 
 
@@ -78,3 +79,45 @@ def test_host_validation_codes(libw4):
     assert _call(libw4, "w4a16_dequant", 0, A, A, A, A, 0, 4, 128, 64, None) == 2
     msg = _call(libw4, "w4a16_last_error_string").decode()
     assert "group" in msg
+
+
+def test_linear_struct_layout_matches_the_header():
+    # five pointers then three int64: 64 bytes, no padding
+    import gemm_w4a16_gemv_gb300 as w4
+    assert ctypes.sizeof(w4.w4a16_linear) == 64
+    assert w4.w4a16_linear.M.offset == 40 and w4.w4a16_linear.K.offset == 56
+
+
+def test_sequence_and_graph_host_validation(libw4):
+    # every case fails (or succeeds with nothing to do) before any CUDA call
+    import gemm_w4a16_gemv_gb300 as w4
+    A = 1 << 20
+    ops = (w4.w4a16_linear * 3)()
+    for i, (M, N, K) in enumerate([(1, 24, 256), (3, 32, 256), (1, 16, 384)]):
+        ops[i].x = ops[i].qw = ops[i].s = ops[i].z = ops[i].y = A
+        ops[i].M, ops[i].N, ops[i].K = M, N, K
+    ops[2].K = 320                      # not a multiple of the group
+    assert _call(libw4, "w4a16_linear_sequence", ops, 3, 128, None) == 1
+    assert "op 2" in _call(libw4, "w4a16_last_error_string").decode()
+    ops[2].K = 384
+    ops[0].N = 24                       # M = 1: the GEMV's rules, any N
+    ops[1].N = 24                       # M > 1: the GEMM's rules, N % 16
+    assert _call(libw4, "w4a16_linear_sequence", ops, 3, 128, None) == 2
+    assert "op 1" in _call(libw4, "w4a16_last_error_string").decode()
+    ops[1].N = 32
+    ops[1].y = A + 8
+    assert _call(libw4, "w4a16_linear_sequence", ops, 3, 128, None) == 3
+    ops[1].y = A
+    assert _call(libw4, "w4a16_linear_sequence", ops, 3, 64, None) == 2
+    assert _call(libw4, "w4a16_linear_sequence", ops, -1, 128, None) == 1
+    assert _call(libw4, "w4a16_linear_sequence", None, 2, 128, None) == 1
+    assert _call(libw4, "w4a16_linear_sequence", None, 0, 128, None) == 0   # empty: nothing to launch
+    h = ctypes.c_void_p(123)
+    assert _call(libw4, "w4a16_graph_create", ops, 0, 128, ctypes.byref(h)) == 1
+    assert h.value is None              # the handle is cleared on failure
+    ops[0].qw = 0
+    assert _call(libw4, "w4a16_graph_create", ops, 3, 128, ctypes.byref(h)) == 1
+    assert "op 0" in _call(libw4, "w4a16_last_error_string").decode()
+    assert _call(libw4, "w4a16_graph_create", ops, 3, 128, None) == 1
+    assert _call(libw4, "w4a16_graph_launch", None, None) == 1
+    assert _call(libw4, "w4a16_graph_destroy", None) == 0
