@@ -379,7 +379,7 @@ def per_config(torch, w4, synth, dev, stream, hbm_peak, tf_peak):
     N, K = UP
     nsets = L2_SETS
     sets, _ = make_gemv_sets(torch, synth, dev, N, K, seed=0, nsets=nsets)
-    for M in (2, 4):
+    for M in (2, 4, 8):
         X = torch.randn(M, K, device=dev).to(torch.bfloat16)
         Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
         t = time_launches(torch, lambda i: w4.w4a16_gemm(X, sets[i % nsets]["qw"], sets[i % nsets]["s"],

@@ -105,13 +105,23 @@ int check_gemm_args(const char *who, const void *X, const void *qw, const void *
     return W4A16_OK;
 }
 
-// Decode-sized batches stream the weights once on the CUDA cores (M = 1: the
-// GEMV; M <= 4: the M rows share one pass); larger M goes to the tensor cores.
+// Decode-sized batches stream the weights on the CUDA cores: M = 1 the GEMV,
+// M <= 4 rows sharing one pass, 5 <= M <= 8 two passes (four rows, then the
+// rest).  Larger M goes to the tensor cores, whose GEMM has a fixed pipeline
+// latency that dominates at small M (measured at N = 15360, K = 3840, GEMM
+// against two passes: M = 5 28.7 / 22.3 us, M = 6 31.5 / 24.6 us, M = 8
+// 30.8 / 29.6 us, M = 12 30.7 / 44.3 us).
 cudaError_t launch_int4_linear(const uint16_t *X, const uint8_t *qw, const uint16_t *s, const uint16_t *z,
                                uint16_t *Y, int64_t M, int64_t N, int64_t K, cudaStream_t st, unsigned int *status,
                                const w4::DeviceInfo &dev) {
     if (M == 1) return w4::launch_gemv_int4(X, qw, s, z, Y, N, K, st, status, dev);
     if (M <= 4) return w4::launch_gemv_int4_batched(X, qw, s, z, Y, M, N, K, st, status, dev);
+    if (M <= 8) {
+        const cudaError_t e = w4::launch_gemv_int4_batched(X, qw, s, z, Y, 4, N, K, st, status, dev);
+        if (e != cudaSuccess) return e;
+        // rows 4 .. M-1: X + 4K and Y + 4N stay 16-byte aligned (K % 128 == 0, N % 16 == 0)
+        return launch_int4_linear(X + 4 * K, qw, s, z, Y + 4 * N, M - 4, N, K, st, status, dev);
+    }
     return w4::launch_gemm_int4(X, qw, s, z, Y, M, N, K, st, status, dev);
 }
 

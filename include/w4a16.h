@@ -82,8 +82,9 @@ int w4a16_gemv(const uint16_t *x, const uint8_t *qw, const uint16_t *s,
  *       symmetric INT4);  Y : bfloat16 [M, N].
  * Requires group == 128, K % 128 == 0, 128 <= K <= 16384, N % 16 == 0.  Any
  * M >= 1 is accepted (rows past M in the last tile are masked).  Decode-sized
- * batches (M <= 4) run as the streaming GEMV instead, the M rows sharing one
- * pass over the weights; larger M runs on the tensor cores.
+ * batches run as the streaming GEMV instead: M <= 4 rows share one pass over
+ * the weights, 5 <= M <= 8 take two passes (four rows, then the rest);
+ * larger M runs on the tensor cores.
  */
 int w4a16_gemm(const uint16_t *X, const uint8_t *qw, const uint16_t *s,
                const uint16_t *z, uint16_t *Y, int64_t M, int64_t N,

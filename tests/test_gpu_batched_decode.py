@@ -1,6 +1,7 @@
-"""Decode-sized batches (M = 1..4) through w4a16_gemm: the rows share one
-streaming pass over the weights (the M = 1 GEMV pipeline with one team set
-per activation row), checked against the binary64 oracle."""
+"""Decode-sized batches (M = 1..8) through w4a16_gemm: up to four rows share
+one streaming pass over the weights (the M = 1 GEMV pipeline with one team set
+per activation row), M = 5..8 take two passes; checked against the binary64
+oracle."""
 import pytest
 
 import oracle
@@ -17,7 +18,7 @@ def _gemm(w4, torch, p, M, N, K, sym=False):
     return host_bits16(Y).reshape(M, N)
 
 
-@pytest.mark.parametrize("M", [1, 2, 3, 4])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("N,K", [(16, 128), (112, 384), (1008, 3840), (336, 15360), (64, 16384)])
 def test_small_batch_decode(M, N, K):
     torch, w4 = cuda_or_skip()
@@ -26,7 +27,7 @@ def test_small_batch_decode(M, N, K):
     assert_close(_gemm(w4, torch, p, M, N, K), ref, "batched decode M=%d %dx%d" % (M, N, K))
 
 
-@pytest.mark.parametrize("M", [2, 4])
+@pytest.mark.parametrize("M", [2, 4, 6, 8])
 def test_small_batch_decode_full_width(M):
     torch, w4 = cuda_or_skip()
     N, K = 15360, 3840
@@ -35,7 +36,7 @@ def test_small_batch_decode_full_width(M):
     assert_close(_gemm(w4, torch, p, M, N, K), ref, "batched decode M=%d full width" % M)
 
 
-@pytest.mark.parametrize("M", [2, 3])
+@pytest.mark.parametrize("M", [2, 3, 5, 7])
 def test_small_batch_decode_symmetric(M):
     torch, w4 = cuda_or_skip()
     N, K = 496, 1920
