@@ -309,22 +309,27 @@ def decode_step_ops(torch, synth, dev):
                               torch.from_numpy(p["z"]).view(torch.float16).to(dev))
         return tuple(t.clone() for t in protos[(N, K)])
 
-    H, Q, KV, F = STEP_H, STEP_Q, STEP_KV, STEP_F
-    buf = {n: torch.zeros(k, dtype=torch.bfloat16, device=dev)
-           for n, k in (("h", H), ("q", Q), ("k", KV), ("v", KV), ("gate", F), ("up", F))}
-    buf["h"].copy_(torch.from_numpy(synth.normal_bf16(synth.Stream(5), (H,))).view(torch.bfloat16))
-    logits = torch.empty(STEP_V, dtype=torch.bfloat16, device=dev)
-    ops = []
-    for layer in range(STEP_SLIDING + STEP_GLOBAL):
-        proj = [("h", "q", Q, H), ("h", "k", KV, H)]
-        if layer < STEP_SLIDING:
-            proj.append(("h", "v", KV, H))
-        proj += [("q", "h", H, Q), ("h", "gate", F, H), ("h", "up", F, H), ("up", "h", H, F)]
-        for src, dst, N, K in proj:
-            ops.append((buf[src], *weights(N, K), buf[dst]))
-    ops.append((buf["h"], *weights(STEP_V, H), logits))
+    size = {"h": STEP_H, "q": STEP_Q, "k": STEP_KV, "v": STEP_KV, "gate": STEP_F, "up": STEP_F,
+            "logits": STEP_V}
+    buf = {n: torch.zeros(k, dtype=torch.bfloat16, device=dev) for n, k in size.items()}
+    buf["h"].copy_(torch.from_numpy(synth.normal_bf16(synth.Stream(5), (STEP_H,))).view(torch.bfloat16))
+    ops = [(buf[src], *weights(N, K), buf[dst]) for src, dst, N, K in decode_step_linears()]
     protos.clear()
     return ops
+
+
+def decode_step_linears():
+    """(source buffer, destination buffer, N, K) of the step's linears in
+    launch order."""
+    H, Q, KV, F = STEP_H, STEP_Q, STEP_KV, STEP_F
+    out = []
+    for layer in range(STEP_SLIDING + STEP_GLOBAL):
+        out += [("h", "q", Q, H), ("h", "k", KV, H)]
+        if layer < STEP_SLIDING:
+            out.append(("h", "v", KV, H))
+        out += [("q", "h", H, Q), ("h", "gate", F, H), ("h", "up", F, H), ("up", "h", H, F)]
+    out.append(("h", "logits", STEP_V, H))
+    return out
 
 
 def decode_step(torch, w4, synth, dev, stream, hbm_peak):
