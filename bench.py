@@ -290,10 +290,10 @@ STEP_H, STEP_Q, STEP_KV, STEP_F, STEP_V = 3840, 4096, 2048, 15360, 262144
 STEP_SLIDING, STEP_GLOBAL = 40, 8
 
 
-def decode_step_ops(torch, synth, dev):
-    """The step's 329 INT4 linears as (x, qw, s, z, y) tuples, each with its
-    own weight copy (6.2 GB in all, so every step streams from HBM).  Scales
-    are drawn so that a linear keeps the activations' magnitude (mean scale
+def decode_step_ops(torch, synth, dev, fused=False):
+    """The step's INT4 linears as (x, qw, s, z, y) tuples, each with its own
+    weight copy (6.2 GB in all, so every step streams from HBM).  Scales are
+    drawn so that a linear keeps the activations' magnitude (mean scale
     1 / (6.5 sqrt(K)), 6.5 being the spread of q - z).  Data flow through
     activation buffers: q, k, v, gate, up read the hidden state h; o reads q
     (the attention is not on this path) and writes h; down reads up and
@@ -309,33 +309,63 @@ def decode_step_ops(torch, synth, dev):
                               torch.from_numpy(p["z"]).view(torch.float16).to(dev))
         return tuple(t.clone() for t in protos[(N, K)])
 
-    size = {"h": STEP_H, "q": STEP_Q, "k": STEP_KV, "v": STEP_KV, "gate": STEP_F, "up": STEP_F,
-            "logits": STEP_V}
-    buf = {n: torch.zeros(k, dtype=torch.bfloat16, device=dev) for n, k in size.items()}
-    buf["h"].copy_(torch.from_numpy(synth.normal_bf16(synth.Stream(5), (STEP_H,))).view(torch.bfloat16))
-    ops = [(buf[src], *weights(N, K), buf[dst]) for src, dst, N, K in decode_step_linears()]
+    views = decode_step_views(fused)
+    store = {}
+    for base, off, n in views.values():
+        store[base] = max(store.get(base, 0), off + n)
+    store = {k: torch.zeros(n, dtype=torch.bfloat16, device=dev) for k, n in store.items()}
+    h = torch.from_numpy(synth.normal_bf16(synth.Stream(5), (STEP_H,))).view(torch.bfloat16)
+    store["h"].copy_(h)
+
+    def view(name, n):
+        base, off, _ = views[name]
+        return store[base][off:off + n]
+
+    ops = [(view(src, K), *weights(N, K), view(dst, N)) for src, dst, N, K in decode_step_linears(fused)]
     protos.clear()
     return ops
 
 
-def decode_step_linears():
-    """(source buffer, destination buffer, N, K) of the step's linears in
-    launch order."""
+def decode_step_linears(fused=False):
+    """(source, destination, N, K) of the step's linears in launch order.
+    fused: the linears that read the same input stored as one weight tensor
+    (q|k|v and gate|up, a layout choice of the model: the same weights and
+    bytes), so that one launch covers each group: 48 x 4 + 1 launches."""
     H, Q, KV, F = STEP_H, STEP_Q, STEP_KV, STEP_F
     out = []
     for layer in range(STEP_SLIDING + STEP_GLOBAL):
+        sliding = layer < STEP_SLIDING
+        if fused:
+            out += [("h", "qkv", Q + (2 if sliding else 1) * KV, H), ("q", "h", H, Q),
+                    ("h", "gateup", 2 * F, H), ("up", "h", H, F)]
+            continue
         out += [("h", "q", Q, H), ("h", "k", KV, H)]
-        if layer < STEP_SLIDING:
+        if sliding:
             out.append(("h", "v", KV, H))
         out += [("q", "h", H, Q), ("h", "gate", F, H), ("h", "up", F, H), ("up", "h", H, F)]
     out.append(("h", "logits", STEP_V, H))
     return out
 
 
-def decode_step(torch, w4, synth, dev, stream, hbm_peak):
+def decode_step_views(fused=False):
+    """Activation buffer name -> (storage, offset, length).  In the fused
+    layout q and up are the leading part of the q|k|v output and the
+    trailing part of the gate|up output."""
+    H, Q, KV, F = STEP_H, STEP_Q, STEP_KV, STEP_F
+    v = {"h": ("h", 0, H), "logits": ("logits", 0, STEP_V)}
+    if fused:
+        v.update({"qkv": ("qkv", 0, Q + 2 * KV), "q": ("qkv", 0, Q),
+                  "gateup": ("gateup", 0, 2 * F), "up": ("gateup", F, F)})
+    else:
+        v.update({"q": ("q", 0, Q), "k": ("k", 0, KV), "v": ("v", 0, KV), "gate": ("gate", 0, F),
+                  "up": ("up", 0, F)})
+    return v
+
+
+def decode_step(torch, w4, synth, dev, stream, hbm_peak, fused=False):
     """The decode step replayed from one CUDA graph, against the same launches
     made one by one from the host (w4a16_linear_sequence)."""
-    ops = decode_step_ops(torch, synth, dev)
+    ops = decode_step_ops(torch, synth, dev, fused)
     nbytes = sum(gemv_bytes(op[1].shape[0], 2 * op[1].shape[1]) for op in ops)
     arr = w4.w4a16_linear_array(ops)
     g = w4.w4a16_graph_create(ops)
@@ -453,9 +483,14 @@ def per_config(torch, w4, synth, dev, stream, hbm_peak, tf_peak):
         except Exception as e:
             out[name] = {"unavailable": str(e).splitlines()[0][:120]}
         torch.cuda.empty_cache()
-    # the whole decode step (328 linears and the vocabulary GEMV) as one graph
-    out["decode_step_328_linears_vocab"] = decode_step(torch, w4, synth, dev, stream, hbm_peak)
-    torch.cuda.empty_cache()
+    # the whole decode step (328 linears and the vocabulary GEMV) as one graph;
+    # then the same weights with q|k|v and gate|up each stored as one tensor
+    for name, fused in (("decode_step_328_linears_vocab", False), ("decode_step_fused_qkv_gateup", True)):
+        try:
+            out[name] = decode_step(torch, w4, synth, dev, stream, hbm_peak, fused)
+        except Exception as e:
+            out[name] = {"unavailable": str(e).splitlines()[0][:120]}
+        torch.cuda.empty_cache()
     return out
 
 

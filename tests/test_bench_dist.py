@@ -64,21 +64,29 @@ def test_single_process_helpers_are_identity():
     bench.dist_barrier()
 
 
-def test_decode_step_structure():
+@pytest.mark.parametrize("fused", [False, True])
+def test_decode_step_structure(fused):
     # the pages' step: 48 layers (40 sliding, 8 global), 328 quantised
-    # linears, then the 262144-row vocabulary GEMV; every activation buffer
-    # is written before it is read, and each linear's K is its source's size
+    # linears, then the 262144-row vocabulary GEMV (the fused layout stores
+    # q|k|v and gate|up as one tensor each: the same weights in 193 launches);
+    # every activation buffer is written before it is read, within its
+    # storage, and each linear's K is its source's length
     import bench
-    ops = bench.decode_step_linears()
-    assert len(ops) == 329
-    assert sum(1 for op in ops[:-1] if op[1] == "v") == 40
+    ops = bench.decode_step_linears(fused)
+    views = bench.decode_step_views(fused)
+    assert len(ops) == (193 if fused else 329)
     assert ops[-1] == ("h", "logits", 262144, 3840)
-    size = {"h": 3840}
+    written = {"h": 3840}
     for src, dst, N, K in ops:
-        assert src in size and size[src] == K, (src, dst)
-        size[dst] = N
+        base, off, n = views[src]
+        assert n == K and written.get(base, 0) >= off + K, (src, dst)
+        base, off, n = views[dst]
+        assert off == 0 and N <= n
+        written[base] = max(written.get(base, 0), N)
     # INT4 codes + binary16 scales and zeros of the 328 linears (reading of
     # the pages' 5,705,441,280 bytes, whose breakdown is lost): within 0.5 %
     w = sum(N * K // 2 + 2 * 2 * N * (K // 128) for _, _, N, K in ops[:-1])
     assert w == 5681971200
     assert abs(w - 5705441280) / 5705441280 < 5e-3
+    if not fused:
+        assert sum(1 for op in ops[:-1] if op[1] == "v") == 40
