@@ -238,7 +238,11 @@ def w4a16_linear_sequence(ops, group: int = 128, stream=None, count=None):
     one stream (each op's X is read after the previous op has finished).
     `ops` may also be an array from w4a16_linear_array, with `count` ops."""
     if isinstance(ops, ctypes.Array):
+        if ops._type_ is not w4a16_linear:
+            raise TypeError("ops must be an array of w4a16_linear")
         arr, n = ops, len(ops) if count is None else int(count)
+        if not 0 <= n <= len(ops):
+            raise ValueError("count %d outside 0..%d (the array's length)" % (n, len(ops)))
     else:
         arr, n = w4a16_linear_array(ops, group), len(ops)
     _check(lib().w4a16_linear_sequence(arr, n, group, _stream(stream)))

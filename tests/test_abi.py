@@ -121,3 +121,15 @@ def test_sequence_and_graph_host_validation(libw4):
     assert _call(libw4, "w4a16_graph_create", ops, 3, 128, None) == 1
     assert _call(libw4, "w4a16_graph_launch", None, None) == 1
     assert _call(libw4, "w4a16_graph_destroy", None) == 0
+
+
+def test_binding_checks_prebuilt_op_arrays():
+    # a prebuilt array is never read past its length (checked before the call)
+    import gemm_w4a16_gemv_gb300 as w4
+    arr = (w4.w4a16_linear * 2)()
+    with pytest.raises(ValueError, match="outside"):
+        w4.w4a16_linear_sequence(arr, count=3)
+    with pytest.raises(ValueError, match="outside"):
+        w4.w4a16_linear_sequence(arr, count=-1)
+    with pytest.raises(TypeError):
+        w4.w4a16_linear_sequence((ctypes.c_int64 * 8)(), count=1)
