@@ -24,6 +24,9 @@
  *  - all data pointers are DEVICE pointers owned by the caller; the library
  *    keeps no reference after the call returns and allocates no memory;
  *  - every data pointer must be 16-byte aligned (else W4A16_ERR_MISALIGNED);
+ *  - an output must not overlap any input of the same call (CTAs write
+ *    their outputs while others may still read the inputs); this is not
+ *    checked;
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream); calls are
  *    asynchronous on it and never synchronise the host, so they may be
  *    captured into a CUDA graph;
@@ -163,7 +166,8 @@ typedef struct {
  * Each op reads its x and writes its y only after the previous op has
  * finished (only its weight prefetch into L2 may overlap the previous op),
  * so an op may read the output of any earlier op and may overwrite a buffer
- * that an earlier op read.  The `ops` array is read during the call only.
+ * that an earlier op read (but, as for every call, not its own input).  The
+ * `ops` array is read during the call only.
  * Every op is checked before anything is launched: a failed check launches
  * nothing and the message names the op.  count == 0 launches nothing and
  * returns W4A16_OK.  A CUDA launch error at op i returns W4A16_ERR_CUDA
