@@ -90,3 +90,14 @@ def test_decode_step_structure(fused):
     assert abs(w - 5705441280) / 5705441280 < 5e-3
     if not fused:
         assert sum(1 for op in ops[:-1] if op[1] == "v") == 40
+
+
+def test_algorithmic_bytes_of_the_roofline():
+    # per launch: packed codes (N K / 2) + binary16 scales and zeros
+    # (2 x 2 N K / 128) + the activation (2 K) + the output (2 N)
+    import bench
+    up, down = bench.gemv_bytes(15360, 3840), bench.gemv_bytes(3840, 15360)
+    assert up == 15360 * (1920 + 120) + 7680 + 30720 == 31372800
+    assert down == up                     # the same matrix transposed: same total
+    assert bench.STEP_BYTES == 2 * 31372800
+    assert bench.gemv_bytes(262144, 3840) == 535305728   # the vocabulary GEMV
