@@ -181,13 +181,41 @@ def oracle_rows_per_second(oracle, synth, N, K, rows):
     return rows / (time.perf_counter() - t0)
 
 
-def oracle_step_sample(oracle, synth, seconds):
+def host_cpu():
+    """(usable cores, CPU model name) of this host."""
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        cores = os.cpu_count() or 1
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except OSError:
+            pass
+    return cores, model or "unknown"
+
+
+def oracle_step_sample(oracle, synth, seconds, threads=1):
     """A bounded sample of one step for the CPU oracle: the same fraction of
-    the up and the down projection rows, sized to take about `seconds`.
-    Returns (callable running the sample, algorithmic bytes of the sample)."""
+    the up and the down projection rows, sized to take about `seconds` with
+    `threads` threads.  Returns (callable running the sample, algorithmic
+    bytes of the sample, description)."""
+    oracle.set_threads(threads)
     oracle_rows_per_second(oracle, synth, UP[0], UP[1], 2)  # load the library first
-    up_rps = oracle_rows_per_second(oracle, synth, UP[0], UP[1], 64)
-    dn_rps = oracle_rows_per_second(oracle, synth, DOWN[0], DOWN[1], 16)
+    up_rps = oracle_rows_per_second(oracle, synth, UP[0], UP[1], 64 * threads)
+    dn_rps = oracle_rows_per_second(oracle, synth, DOWN[0], DOWN[1], 16 * threads)
     # fraction f of both projections: f*UP[0]/up_rps + f*DOWN[0]/dn_rps = seconds
     f = seconds / (UP[0] / up_rps + DOWN[0] / dn_rps)
     f = max(min(f, 1.0), 1e-4)
@@ -202,24 +230,37 @@ def oracle_step_sample(oracle, synth, seconds):
 
     sample_bytes = (n_up * (UP[1] // 2 + 4 * (UP[1] // 128)) + 2 * UP[1] + 2 * n_up
                     + n_dn * (DOWN[1] // 2 + 4 * (DOWN[1] // 128)) + 2 * DOWN[1] + 2 * n_dn)
-    desc = "%d of %d up rows + %d of %d down rows per step, single thread" % (n_up, UP[0], n_dn, DOWN[0])
+    desc = "%d of %d up rows + %d of %d down rows per step, %d thread%s" % (
+        n_up, UP[0], n_dn, DOWN[0], threads, "" if threads == 1 else "s (OpenMP over output rows)")
     return run, sample_bytes, desc
 
 
-def cpu_baseline(seconds=8.0):
+def cpu_baseline(seconds=10.0):
+    """The oracle timed on this host: on all its cores (the reported value)
+    and on one core; each leg a bounded sample of the step."""
     import oracle
     import synth
-    run, nbytes, desc = oracle_step_sample(oracle, synth, seconds / 2)
-    t0 = time.perf_counter()
-    n = 0
-    while True:
-        run()
-        n += 1
-        if time.perf_counter() - t0 >= seconds / 2 and n >= 1:
-            break
-    dt = time.perf_counter() - t0
-    return {"value": round(nbytes * n / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": desc + ", %d repetitions in %.1f s" % (n, dt)}
+    cores, model = host_cpu()
+
+    def leg(threads, secs):
+        run, nbytes, desc = oracle_step_sample(oracle, synth, secs / 2, threads)
+        t0 = time.perf_counter()
+        n = 0
+        while True:
+            run()
+            n += 1
+            if time.perf_counter() - t0 >= secs / 2:
+                break
+        dt = time.perf_counter() - t0
+        return nbytes * n / dt / 1e9, desc + ", %d repetitions in %.1f s" % (n, dt)
+
+    try:
+        v_all, d_all = leg(cores, seconds)
+        v_one, d_one = leg(1, seconds / 2)
+    finally:
+        oracle.set_threads(1)
+    return {"value": round(v_all, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": d_all,
+            "cpu_model": model, "single_thread": {"value": round(v_one, 4), "unit": "GB/s", "sample": d_one}}
 
 
 def run_reference(args):
@@ -230,22 +271,24 @@ def run_reference(args):
         return 0
     import oracle
     import synth
+    cores, model = host_cpu()
     per_step = max(0.05, 100.0 / max(1, args.steps + args.warmup))
-    run, nbytes, desc = oracle_step_sample(oracle, synth, per_step)
+    run, nbytes, desc = oracle_step_sample(oracle, synth, per_step, cores)
     for _ in range(args.warmup):
         run()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         run()
     dt = time.perf_counter() - t0
+    oracle.set_threads(1)
     value = nbytes * args.steps / dt / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD, "sample": desc},
-            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": desc},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": desc, "cpu_model": model},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -264,6 +307,37 @@ def make_gemv_sets(torch, synth, dev, N, K, seed, nsets):
     sets = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(nsets - 1)]
     x_host = torch.from_numpy(p["x"].reshape(-1)).view(torch.bfloat16)
     return sets, x_host
+
+
+def time_each(torch, fn, n, stream):
+    """Device time of each of n launches, bracketed one by one by CUDA events
+    (an event between launches also ends any overlap of consecutive
+    kernels): (p10, median, p90) in seconds."""
+    for i in range(3):
+        fn(i)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    torch.cuda._sleep(int(5e7))
+    ev[0].record(stream)
+    for i in range(n):
+        fn(i)
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    d = sorted(ev[i].elapsed_time(ev[i + 1]) * 1e-3 for i in range(n))
+    pick = lambda q: d[min(n - 1, max(0, int(round(q * (n - 1)))))]
+    return pick(0.1), pick(0.5), pick(0.9)
+
+
+def spread(torch, fn, n, stream, scale=1e6):
+    """p10 / median / p90 of individually bracketed launches, in us."""
+    p10, p50, p90 = time_each(torch, fn, n, stream)
+    return {"p10_us": round(p10 * scale, 2), "median_us": round(p50 * scale, 2), "p90_us": round(p90 * scale, 2)}
+
+
+def l2_sets(nbytes, l2_bytes=129e6, cap=24):
+    """Weight copies to rotate through so that their total is at least twice
+    the L2 (each launch then streams its weights from HBM)."""
+    return max(1, min(cap, int(2 * l2_bytes // nbytes) + 1))
 
 
 def time_launches(torch, fn, n, stream):
@@ -399,20 +473,21 @@ def per_config(torch, w4, synth, dev, stream, hbm_peak, tf_peak):
     out = {}
     for name, (N, K) in {"gemv_3840x3840": (3840, 3840), "gemv_up_15360x3840": UP,
                          "gemv_down_3840x15360": DOWN, "gemv_vocab_262144x3840": (262144, 3840)}.items():
-        nsets = max(1, min(L2_SETS, int(4e8 // gemv_bytes(N, K)) + 1))
+        nsets = l2_sets(gemv_bytes(N, K))
         sets, xh = make_gemv_sets(torch, synth, dev, N, K, seed=0, nsets=nsets)
         x = xh.to(dev)
         y = torch.empty(N, dtype=torch.bfloat16, device=dev)
-        t = time_launches(torch, lambda i: w4.w4a16_gemv(x, sets[i % nsets]["qw"], sets[i % nsets]["s"],
-                                                          sets[i % nsets]["z"], y), 40, stream)
+        fn = lambda i: w4.w4a16_gemv(x, sets[i % nsets]["qw"], sets[i % nsets]["s"], sets[i % nsets]["z"], y)
+        t = time_launches(torch, fn, 40, stream)
         gbs = gemv_bytes(N, K) / t / 1e9
-        out[name] = {"us": round(t * 1e6, 2), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm_peak, 3)}
+        out[name] = {"us": round(t * 1e6, 2), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm_peak, 3),
+                     "weight_sets": nsets, "each": spread(torch, fn, 100, stream)}
         del sets
         torch.cuda.empty_cache()
     # decode-sized batches through w4a16_gemm: the M rows share one pass over
     # the weights (bytes: weights + scales/zeros once, M activations/outputs)
     N, K = UP
-    nsets = L2_SETS
+    nsets = l2_sets(gemv_bytes(N, K))
     sets, _ = make_gemv_sets(torch, synth, dev, N, K, seed=0, nsets=nsets)
     for M in (2, 4, 8):
         X = torch.randn(M, K, device=dev).to(torch.bfloat16)
@@ -434,10 +509,12 @@ def per_config(torch, w4, synth, dev, stream, hbm_peak, tf_peak):
     x = torch.from_numpy(m["x"]).view(torch.bfloat16).to(dev)
     ids = [torch.from_numpy(synth.sample_experts(synth.Stream(100 + i), E, topk)).to(dev) for i in range(16)]
     y = torch.empty(topk, N, dtype=torch.bfloat16, device=dev)
-    t = time_launches(torch, lambda i: w4.fp4_moe_gemv(x, qw, s, ids[i % 16], y), 40, stream)
+    fn = lambda i: w4.fp4_moe_gemv(x, qw, s, ids[i % 16], y)
+    t = time_launches(torch, fn, 40, stream)
     mb = topk * (N * K // 2 + 2 * N * (K // 32)) + 2 * K + 2 * topk * N + 4 * topk
     out["moe_fp4_64x4096x7168_top6"] = {"us": round(t * 1e6, 2), "GB/s": round(mb / t / 1e9, 1),
-                                        "frac_hbm": round(mb / t / 1e9 / hbm_peak, 3)}
+                                        "frac_hbm": round(mb / t / 1e9 / hbm_peak, 3),
+                                        "each": spread(torch, fn, 100, stream)}
     del qw, s
     torch.cuda.empty_cache()
     # prefill GEMM through the tensor cores
@@ -445,13 +522,15 @@ def per_config(torch, w4, synth, dev, stream, hbm_peak, tf_peak):
         name = "gemm_m%d_15360x3840" % M
         try:
             N, K = 15360, 3840
-            sets, _ = make_gemv_sets(torch, synth, dev, N, K, seed=0, nsets=4)
+            ns = l2_sets(gemv_bytes(N, K))
+            sets, _ = make_gemv_sets(torch, synth, dev, N, K, seed=0, nsets=ns)
             X = torch.randn(M, K, device=dev).to(torch.bfloat16)
             Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
-            t = time_launches(torch, lambda i: w4.w4a16_gemm(X, sets[i % 4]["qw"], sets[i % 4]["s"],
-                                                              sets[i % 4]["z"], Y), 20, stream)
+            fn = lambda i: w4.w4a16_gemm(X, sets[i % ns]["qw"], sets[i % ns]["s"], sets[i % ns]["z"], Y)
+            t = time_launches(torch, fn, 20, stream)
             tf = 2.0 * M * N * K / t / 1e12
-            out[name] = {"us": round(t * 1e6, 2), "TFLOP/s": round(tf, 1), "frac_bf16": round(tf / tf_peak, 3)}
+            out[name] = {"us": round(t * 1e6, 2), "TFLOP/s": round(tf, 1), "frac_bf16": round(tf / tf_peak, 3),
+                         "weight_sets": ns, "each": spread(torch, fn, 50, stream)}
             del sets
         except Exception as e:  # the tensor-core GEMM may be unavailable on this device
             out[name] = {"unavailable": str(e).splitlines()[0][:120]}
@@ -462,18 +541,20 @@ def per_config(torch, w4, synth, dev, stream, hbm_peak, tf_peak):
         name = "two_pass_m%d_15360x3840" % M
         try:
             N, K = 15360, 3840
-            sets, _ = make_gemv_sets(torch, synth, dev, N, K, seed=0, nsets=4)
-            Wb = [torch.empty(N, K, dtype=torch.bfloat16, device=dev) for _ in range(4)]
+            ns = l2_sets(gemv_bytes(N, K))
+            sets, _ = make_gemv_sets(torch, synth, dev, N, K, seed=0, nsets=ns)
+            nw = l2_sets(2 * N * K)  # BF16 weight matrices, 118 MB each
+            Wb = [torch.empty(N, K, dtype=torch.bfloat16, device=dev) for _ in range(nw)]
             X = torch.randn(M, K, device=dev).to(torch.bfloat16)
             Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
 
             def deq(i):
-                w4.w4a16_dequant(w4.FMT_INT4, sets[i % 4]["qw"], sets[i % 4]["s"], sets[i % 4]["z"],
-                                 out=Wb[i % 4], out_dtype=w4.OUT_BF16)
+                w4.w4a16_dequant(w4.FMT_INT4, sets[i % ns]["qw"], sets[i % ns]["s"], sets[i % ns]["z"],
+                                 out=Wb[i % nw], out_dtype=w4.OUT_BF16)
 
             t_deq = time_launches(torch, deq, 20, stream)
-            t_mm = time_launches(torch, lambda i: w4.w4a16_bf16_gemm(X, Wb[i % 4], Y), 20, stream)
-            t_two = time_launches(torch, lambda i: (deq(i), w4.w4a16_bf16_gemm(X, Wb[i % 4], Y)), 20, stream)
+            t_mm = time_launches(torch, lambda i: w4.w4a16_bf16_gemm(X, Wb[i % nw], Y), 20, stream)
+            t_two = time_launches(torch, lambda i: (deq(i), w4.w4a16_bf16_gemm(X, Wb[i % nw], Y)), 20, stream)
             fused = out.get("gemm_m%d_15360x3840" % M, {}).get("us")
             out[name] = {"us": round(t_two * 1e6, 2), "dequant_us": round(t_deq * 1e6, 2),
                          "bf16_gemm_us": round(t_mm * 1e6, 2),
@@ -525,9 +606,9 @@ def run_ours(args):
         raise SystemExit("device status set during warm-up")
 
     # CUDA graphs: one holding a step for each of the L2_SETS weight sets back
-    # to back (so consecutive launches chain inside the graph), and one per
-    # single step for the remainder; the timed loop runs exactly args.steps
-    # steps.
+    # to back (so consecutive launches chain inside the graph), and one
+    # holding the remaining steps % L2_SETS steps, likewise chained; the timed
+    # loop runs exactly args.steps steps.
     graphs = None
     if not args.no_graph:
         try:
@@ -535,17 +616,17 @@ def run_ours(args):
             with torch.cuda.graph(whole):
                 for i in range(L2_SETS):
                     step(i)
-            singles = []
-            for i in range(L2_SETS):
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g):
-                    step(i)
-                singles.append(g)
+            rest = None
+            if args.steps % L2_SETS:
+                rest = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(rest):
+                    for i in range(args.steps % L2_SETS):
+                        step(i)
             whole.replay()
-            for g in singles:
-                g.replay()
+            if rest is not None:
+                rest.replay()
             torch.cuda.synchronize()
-            graphs = (whole, singles)
+            graphs = (whole, rest)
         except Exception:
             graphs = None
             torch.cuda.synchronize()
@@ -559,11 +640,11 @@ def run_ours(args):
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     if graphs is not None:
-        whole, singles = graphs
+        whole, rest = graphs
         for _ in range(args.steps // L2_SETS):
             whole.replay()
-        for i in range(args.steps % L2_SETS):
-            singles[i].replay()
+        if rest is not None:
+            rest.replay()
     else:
         for i in range(args.steps):
             step(i)

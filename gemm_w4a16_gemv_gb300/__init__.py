@@ -21,7 +21,7 @@ import torch
 __all__ = [
     "w4a16_gemv", "w4a16_gemm", "fp4_moe_gemv", "w4a16_dequant", "w4a16_bf16_gemm",
     "w4a16_check_device_error", "w4a16_last_error_string", "w4a16_version",
-    "w4a16_debug_inject", "INJECT_STALL_PIPELINE",
+    "w4a16_debug_inject", "INJECT_STALL_PIPELINE", "INJECT_STALL_CONSUMERS",
     "w4a16_linear", "w4a16_linear_array", "w4a16_linear_sequence", "w4a16_graph_create", "w4a16_graph_launch",
     "w4a16_graph_destroy", "W4A16Graph",
     "library_path", "W4A16Error", "STATUS", "FMT_INT4", "FMT_FP4",
@@ -104,9 +104,11 @@ def _check(status: int):
         raise W4A16Error(status, msg)
 
 
-def _stream(stream):
+def _stream(stream, device=None):
+    """The stream handle to pass: the given stream, else the current stream
+    of `device` (of the current device when None)."""
     if stream is None:
-        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
     if isinstance(stream, torch.cuda.Stream):
         return ctypes.c_void_p(stream.cuda_stream)
     return ctypes.c_void_p(int(stream))
@@ -141,7 +143,8 @@ def w4a16_gemv(x, qw, s, z, y=None, group: int = 128, stream=None):
     if y is None:
         y = torch.empty(N, dtype=torch.bfloat16, device=dev)
     py = _need(y, "y", torch.bfloat16, N, dev)
-    _check(lib().w4a16_gemv(px, pq, ps, pz, py, N, K, group, _stream(stream)))
+    with torch.cuda.device(dev):  # the library launches on the current device
+        _check(lib().w4a16_gemv(px, pq, ps, pz, py, N, K, group, _stream(stream, dev)))
     return y
 
 
@@ -159,7 +162,8 @@ def w4a16_gemm(X, qw, s, z, Y=None, group: int = 128, stream=None):
     if Y is None:
         Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
     pY = _need(Y, "Y", torch.bfloat16, M * N, dev)
-    _check(lib().w4a16_gemm(pX, pq, ps, pz, pY, M, N, K, group, _stream(stream)))
+    with torch.cuda.device(dev):  # the library launches on the current device
+        _check(lib().w4a16_gemm(pX, pq, ps, pz, pY, M, N, K, group, _stream(stream, dev)))
     return Y
 
 
@@ -173,7 +177,8 @@ def w4a16_bf16_gemm(X, W, Y=None, stream=None):
     if Y is None:
         Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
     pY = _need(Y, "Y", torch.bfloat16, M * N, dev)
-    _check(lib().w4a16_bf16_gemm(pX, pW, pY, M, N, K, _stream(stream)))
+    with torch.cuda.device(dev):  # the library launches on the current device
+        _check(lib().w4a16_bf16_gemm(pX, pW, pY, M, N, K, _stream(stream, dev)))
     return Y
 
 
@@ -190,7 +195,8 @@ def fp4_moe_gemv(x, qw, s, expert_ids, y=None, group: int = 32, stream=None):
     if y is None:
         y = torch.empty(topk, N, dtype=torch.bfloat16, device=dev)
     py = _need(y, "y", torch.bfloat16, topk * N, dev)
-    _check(lib().fp4_moe_gemv(px, pq, ps, pi, topk, py, E, N, K, group, _stream(stream)))
+    with torch.cuda.device(dev):  # the library launches on the current device
+        _check(lib().fp4_moe_gemv(px, pq, ps, pi, topk, py, E, N, K, group, _stream(stream, dev)))
     return y
 
 
@@ -209,7 +215,8 @@ def w4a16_dequant(fmt: int, qw, s, z=None, out=None, out_dtype: int = OUT_F32,
     if out is None:
         out = torch.empty(rows, K, dtype=odt, device=dev)
     po = _need(out, "out", odt, rows * K, dev)
-    _check(lib().w4a16_dequant(fmt, pq, ps, pz, po, out_dtype, rows, K, group, _stream(stream)))
+    with torch.cuda.device(dev):  # the library launches on the current device
+        _check(lib().w4a16_dequant(fmt, pq, ps, pz, po, out_dtype, rows, K, group, _stream(stream, dev)))
     return out
 
 
@@ -243,18 +250,22 @@ def w4a16_linear_sequence(ops, group: int = 128, stream=None, count=None):
         arr, n = ops, len(ops) if count is None else int(count)
         if not 0 <= n <= len(ops):
             raise ValueError("count %d outside 0..%d (the array's length)" % (n, len(ops)))
+        dev = torch.cuda.current_device()  # raw addresses: the caller's current device
     else:
         arr, n = w4a16_linear_array(ops, group), len(ops)
-    _check(lib().w4a16_linear_sequence(arr, n, group, _stream(stream)))
+        dev = ops[0][1].device if ops else torch.cuda.current_device()
+    with torch.cuda.device(dev):  # the library launches on the current device
+        _check(lib().w4a16_linear_sequence(arr, n, group, _stream(stream, dev)))
 
 
 class W4A16Graph:
     """Handle of a captured linear sequence (w4a16_graph_create).  Keeps the
     tensors of its ops alive: the graph holds their addresses."""
 
-    def __init__(self, handle, tensors):
+    def __init__(self, handle, tensors, device):
         self._h = handle
         self._tensors = tensors
+        self.device = device
 
     def launch(self, stream=None):
         w4a16_graph_launch(self, stream)
@@ -277,15 +288,18 @@ def w4a16_graph_create(ops, group: int = 128) -> W4A16Graph:
     current device; replay it with w4a16_graph_launch."""
     arr = w4a16_linear_array(ops, group)
     h = ctypes.c_void_p()
-    _check(lib().w4a16_graph_create(arr, len(ops), group, ctypes.byref(h)))
-    return W4A16Graph(h, [t for op in ops for t in op if t is not None])
+    dev = ops[0][1].device if ops else torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(dev):  # the graph is captured on the current device
+        _check(lib().w4a16_graph_create(arr, len(ops), group, ctypes.byref(h)))
+    return W4A16Graph(h, [t for op in ops for t in op if t is not None], dev)
 
 
 def w4a16_graph_launch(graph: W4A16Graph, stream=None) -> None:
     """Enqueue one replay of a captured sequence on the stream."""
     if graph._h is None:
         raise ValueError("graph has been destroyed")
-    _check(lib().w4a16_graph_launch(graph._h, _stream(stream)))
+    with torch.cuda.device(graph.device):
+        _check(lib().w4a16_graph_launch(graph._h, _stream(stream, graph.device)))
 
 
 def w4a16_graph_destroy(graph: W4A16Graph) -> None:
@@ -298,13 +312,15 @@ def w4a16_check_device_error(stream=None) -> int:
 
 
 INJECT_STALL_PIPELINE = 1
+INJECT_STALL_CONSUMERS = 2
 
 
 def w4a16_debug_inject(flags: int = 0) -> None:
-    """Test-only: make every later GEMV/MoE/GEMM launch on this device issue
-    no stage of its pipeline (flags=1), so that its bounded waits run out
-    (after about 2 s) and the device status reports a timeout; flags=0
-    restores normal operation."""
+    """Test-only: make every later GEMV/MoE/GEMM launch on the current device
+    issue no stage of its pipeline (flags=1), or take no stage that its
+    producers issue (flags=2), so that its bounded waits run out (after about
+    2 s) and the device status reports a timeout; flags=0 restores normal
+    operation."""
     _check(lib().w4a16_debug_inject(int(flags)))
 
 

@@ -1,9 +1,12 @@
 // C ABI (include/w4a16.h): argument checks on the host, then one launch.
 // Nothing here allocates device memory or synchronises except
 // w4a16_check_device_error, which synchronises the given stream by design.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <initializer_list>
+#include <mutex>
 #include <new>
 
 #include "w4a16.h"
@@ -34,12 +37,16 @@ int ok() {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Per-device state, filled once per device under a mutex (host threads may
+// make their first calls concurrently); after that it is read without a lock.
 struct DevCache {
-    bool ready;
-    w4::DeviceInfo info;  // info.inject: this device's injection flags
-    unsigned int *status;
+    std::atomic<bool> ready{false};
+    w4::DeviceInfo info{};                 // constant once ready (inject is kept apart)
+    unsigned int *status = nullptr;
+    std::atomic<unsigned int> inject{0};  // this device's injection flags
 };
 DevCache g_dev[64];
+std::mutex g_dev_mu;
 
 // Current device's info and status-word address (looked up once per device).
 int device_state(w4::DeviceInfo &info, unsigned int *&status, DevCache **cache = nullptr) {
@@ -48,22 +55,51 @@ int device_state(w4::DeviceInfo &info, unsigned int *&status, DevCache **cache =
     if (e != cudaSuccess) return fail(W4A16_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
     if (d < 0 || d >= 64) return fail(W4A16_ERR_UNSUPPORTED, "device ordinal %d >= 64", d);
     DevCache &c = g_dev[d];
-    if (!c.ready) {
-        w4::DeviceInfo inf{};
-        inf.device = d;
-        e = cudaDeviceGetAttribute(&inf.num_sms, cudaDevAttrMultiProcessorCount, d);
-        if (e == cudaSuccess)
-            e = cudaDeviceGetAttribute(&inf.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d);
-        void *p = nullptr;
-        if (e == cudaSuccess) e = cudaGetSymbolAddress(&p, g_status);
-        if (e != cudaSuccess) return fail(W4A16_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
-        c.info = inf;
-        c.status = static_cast<unsigned int *>(p);
-        c.ready = true;
+    if (!c.ready.load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lk(g_dev_mu);
+        if (!c.ready.load(std::memory_order_relaxed)) {
+            w4::DeviceInfo inf{};
+            inf.device = d;
+            e = cudaDeviceGetAttribute(&inf.num_sms, cudaDevAttrMultiProcessorCount, d);
+            if (e == cudaSuccess)
+                e = cudaDeviceGetAttribute(&inf.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d);
+            void *p = nullptr;
+            if (e == cudaSuccess) e = cudaGetSymbolAddress(&p, g_status);
+            if (e != cudaSuccess) return fail(W4A16_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
+            c.info = inf;
+            c.status = static_cast<unsigned int *>(p);
+            c.ready.store(true, std::memory_order_release);
+        }
     }
     info = c.info;
+    info.inject = c.inject.load(std::memory_order_relaxed);
     status = c.status;
     if (cache) *cache = &c;
+    return W4A16_OK;
+}
+
+// Every data pointer must be memory of the current device (the launches go
+// to the current device): device memory of that device, or managed memory.
+// Null entries (an absent optional tensor) are skipped.
+int check_device_ptrs(const char *who, int device, std::initializer_list<const void *> ptrs) {
+    int i = 0;
+    for (const void *p : ptrs) {
+        ++i;
+        if (!p) continue;
+        cudaPointerAttributes at;
+        const cudaError_t e = cudaPointerGetAttributes(&at, p);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(W4A16_ERR_INVALID_ARG, "%s: pointer %d is not CUDA memory (%s)", who, i,
+                        cudaGetErrorString(e));
+        }
+        if (at.type == cudaMemoryTypeManaged) continue;
+        if (at.type != cudaMemoryTypeDevice)
+            return fail(W4A16_ERR_INVALID_ARG, "%s: pointer %d is not device memory", who, i);
+        if (at.device != device)
+            return fail(W4A16_ERR_INVALID_ARG, "%s: pointer %d is memory of device %d, the current device is %d", who,
+                        i, at.device, device);
+    }
     return W4A16_OK;
 }
 
@@ -141,6 +177,16 @@ int check_sequence(const w4a16_linear *ops, int count, int group, const char *fn
     return W4A16_OK;
 }
 
+int check_sequence_ptrs(const w4a16_linear *ops, int count, int device, const char *fn) {
+    char who[96];
+    for (int i = 0; i < count; ++i) {
+        snprintf(who, sizeof who, "%s: op %d", fn, i);
+        const w4a16_linear &o = ops[i];
+        if (int r = check_device_ptrs(who, device, {o.x, o.qw, o.s, o.z, o.y})) return r;
+    }
+    return W4A16_OK;
+}
+
 // Launches every op in order; on a launch error returns it and the index.
 cudaError_t launch_sequence(const w4a16_linear *ops, int count, cudaStream_t st, unsigned int *status,
                             const w4::DeviceInfo &dev, int &failed_at) {
@@ -171,6 +217,7 @@ int w4a16_gemv(const uint16_t *x, const uint8_t *qw, const uint16_t *s,
     w4::DeviceInfo dev;
     unsigned int *status;
     if (int r = device_state(dev, status)) return r;
+    if (int r = check_device_ptrs("w4a16_gemv", dev.device, {x, qw, s, z, y})) return r;
     return launched(w4::launch_gemv_int4(x, qw, s, z, y, N, K, static_cast<cudaStream_t>(stream), status, dev),
                     "w4a16_gemv");
 }
@@ -182,6 +229,7 @@ int w4a16_gemm(const uint16_t *X, const uint8_t *qw, const uint16_t *s,
     w4::DeviceInfo dev;
     unsigned int *status;
     if (int r = device_state(dev, status)) return r;
+    if (int r = check_device_ptrs("w4a16_gemm", dev.device, {X, qw, s, z, Y})) return r;
     return launched(launch_int4_linear(X, qw, s, z, Y, M, N, K, static_cast<cudaStream_t>(stream), status, dev),
                     "w4a16_gemm");
 }
@@ -200,6 +248,7 @@ int w4a16_bf16_gemm(const uint16_t *X, const uint16_t *W, uint16_t *Y, int64_t M
     w4::DeviceInfo dev;
     unsigned int *status;
     if (int r = device_state(dev, status)) return r;
+    if (int r = check_device_ptrs("w4a16_bf16_gemm", dev.device, {X, W, Y})) return r;
     return launched(w4::launch_bf16_gemm(X, W, Y, M, N, K, static_cast<cudaStream_t>(stream), status, dev),
                     "w4a16_bf16_gemm");
 }
@@ -223,6 +272,7 @@ int fp4_moe_gemv(const uint16_t *x, const uint8_t *qw, const uint16_t *s,
     w4::DeviceInfo dev;
     unsigned int *status;
     if (int r = device_state(dev, status)) return r;
+    if (int r = check_device_ptrs("fp4_moe_gemv", dev.device, {x, qw, s, expert_ids, y})) return r;
     return launched(w4::launch_moe_fp4(x, qw, s, expert_ids, topk, y, E, N, K, static_cast<cudaStream_t>(stream),
                                        status, dev),
                     "fp4_moe_gemv");
@@ -246,6 +296,7 @@ int w4a16_dequant(int fmt, const uint8_t *qw, const uint16_t *s,
     w4::DeviceInfo dev;
     unsigned int *status;
     if (int r = device_state(dev, status)) return r;
+    if (int r = check_device_ptrs("w4a16_dequant", dev.device, {qw, s, z, out})) return r;
     (void)status;
     return launched(w4::launch_dequant(fmt, qw, s, z, out, out_dtype, rows, K, group,
                                        static_cast<cudaStream_t>(stream), dev),
@@ -258,6 +309,7 @@ int w4a16_linear_sequence(const w4a16_linear *ops, int count, int group, void *s
     w4::DeviceInfo dev;
     unsigned int *status;
     if (int r = device_state(dev, status)) return r;
+    if (int r = check_sequence_ptrs(ops, count, dev.device, "w4a16_linear_sequence")) return r;
     int at = -1;
     cudaError_t e = launch_sequence(ops, count, static_cast<cudaStream_t>(stream), status, dev, at);
     if (e != cudaSuccess)
@@ -283,6 +335,7 @@ int w4a16_graph_create(const w4a16_linear *ops, int count, int group, w4a16_grap
     w4::DeviceInfo dev;
     unsigned int *status;
     if (int r = device_state(dev, status)) return r;
+    if (int r = check_sequence_ptrs(ops, count, dev.device, "w4a16_graph_create")) return r;
     cudaStream_t cs = nullptr;
     cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
     if (e != cudaSuccess) return fail(W4A16_ERR_CUDA, "w4a16_graph_create: stream: %s", cudaGetErrorString(e));
@@ -362,11 +415,11 @@ int w4a16_debug_inject(unsigned int flags) {
     unsigned int *status;
     DevCache *c = nullptr;
     if (int r = device_state(dev, status, &c)) return r;
-    if (flags & ~static_cast<unsigned int>(w4::kInjectStallPipeline))
+    if (flags & ~static_cast<unsigned int>(w4::kInjectStallPipeline | w4::kInjectStallConsumers))
         return fail(W4A16_ERR_INVALID_ARG, "unknown injection flags 0x%x", flags);
     // the flags travel as a kernel argument of later launches: the normal
     // path reads no memory for them
-    c->info.inject = flags;
+    c->inject.store(flags, std::memory_order_relaxed);
     return ok();
 }
 

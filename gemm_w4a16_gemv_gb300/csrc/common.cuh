@@ -16,9 +16,12 @@ enum : unsigned int {
 };
 // Test-only injection flags, passed to the kernels as an argument: with
 // kInjectStallPipeline the producers issue nothing, so that the waits on
-// them run out -- the bounded-wait path, exercised without a fault.
+// them run out; with kInjectStallConsumers the consumers take nothing, so
+// that the producers' waits run out while their copies are issued -- the
+// bounded-wait paths, exercised without a fault.
 enum : unsigned int {
     kInjectStallPipeline = 1u,
+    kInjectStallConsumers = 2u,
 };
 
 // Wait limit for every mbarrier spin, in nanoseconds of %globaltimer.

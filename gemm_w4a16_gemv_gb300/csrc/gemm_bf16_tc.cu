@@ -167,13 +167,8 @@ cudaError_t launch_bf16_gemm(const uint16_t *X, const uint16_t *W, uint16_t *Y, 
     a.K = static_cast<int>(K);
     const int smem = 1024 + STAGES * STAGE_BYTES + static_cast<int>(sizeof(DenseBarriers));
     if (smem > dev.max_smem_optin) return cudaErrorNotSupported;
-    static int configured[64] = {0};
-    const int d = dev.device & 63;
-    if (configured[d] < smem) {
-        cudaError_t e = cudaFuncSetAttribute(bf16_gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        configured[d] = smem;
-    }
+    static SmemLimit limit;
+    if (cudaError_t e = limit.ensure(reinterpret_cast<const void *>(bf16_gemm_tc_kernel), dev.device, smem)) return e;
     const dim3 grid(static_cast<unsigned>((N + TN - 1) / TN), static_cast<unsigned>((M + TM - 1) / TM), 1);
     bf16_gemm_tc_kernel<<<grid, THREADS, smem, st>>>(tmW, tmX, a);
     return cudaGetLastError();

@@ -30,13 +30,10 @@
 // costs about 200 SM cycles of latency on this part even when the phase has
 // already completed, so each role waits once per group, not per MMA step.
 //
-// One CTA computes a tile of 112 output columns n x 128 rows m:
-//  * CTAs that share an X tile (neighbours along N) form a cluster of C = 4
-//    (or 2, 1); each loads 128 / C of its rows and multicasts them, so the
-//    L2 serves every X tile C times fewer; the grid is padded to a multiple
-//    of C with CTAs that carry no weight rows (they only share the loads);
+// One CTA computes a tile of 112 output columns n x 128 rows m; each CTA
+// loads its own X tiles (from L2 after the first CTA that needs them):
 //  * warp 0 (one lane): one bulk copy each of the tile's scale and zero rows;
-//    per group its X rows (two TMA boxes, 128-byte swizzle, multicast);
+//    per group its X rows (two TMA boxes, 128-byte swizzle);
 //  * warp 2 (one lane): every two groups the packed codes of the tile's rows,
 //    128 bytes each (TMA), on a ring of its own;
 //  * warps 8-11 (even groups) and 16-19 (odd groups), TMEM lane quarters
@@ -49,8 +46,8 @@
 //    the tensor pipe sees a steady stream: per group wait for the operand
 //    stage (one of four), the X tile and a free accumulator (one of two),
 //    issue 8 x tcgen05.mma (M=128, N=128, K=16, A from TMEM) and commit
-//    three times: to the X stage's barrier in every CTA of the cluster, to
-//    the operand stage's (local) and to the accumulator's;
+//    three times: to the X stage's barrier, to the operand stage's and to
+//    the accumulator's;
 //  * warps 4-7 and 12-15: per group load the accumulator (warp w: TMEM lanes
 //    32 (w mod 4) .. +31, one half of the 128 columns) into registers,
 //    release it at once and fold y += s A_g (- s z_r S_g) into registers;
@@ -108,7 +105,6 @@ struct GemmArgs {
     int M, N, K, G;
     int sz_bytes;  // bytes of one staged scale (or zero) tile, 16-aligned
     int xp;        // X ring depth in groups
-    int csize;     // CTAs per cluster along N (X multicast)
     int off_w, off_sz;
     unsigned int inject;  // test-only injection flags (0 normally); kept last:
                           // inserting it earlier shifted the hot fields and
@@ -116,8 +112,8 @@ struct GemmArgs {
 };
 
 struct Barriers {
-    uint64_t xfull[MAX_XP];   // a group's X tile landed (TMA tx bytes from every cluster CTA)
-    uint64_t xempty[MAX_XP];  // MMAs of every cluster CTA done with the group
+    uint64_t xfull[MAX_XP];   // a group's X tile landed (TMA tx bytes)
+    uint64_t xempty[MAX_XP];  // MMAs done with the group
     uint64_t wfull[WS];       // packed codes landed (TMA tx bytes)
     uint64_t wempty[WS];      // packed codes read (operand builders)
     uint64_t aready[AP];      // TMEM operand stage written (operand builders)
@@ -154,7 +150,7 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     if (threadIdx.x == 0) {
         for (int i = 0; i < XP; ++i) {
             mbar_init(&bar.xfull[i], 1);
-            mbar_init(&bar.xempty[i], a.csize);
+            mbar_init(&bar.xempty[i], 1);
         }
         for (int i = 0; i < WS; ++i) {
             mbar_init(&bar.wfull[i], 1);
@@ -180,11 +176,7 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    cluster_sync();  // every CTA's barriers exist before any multicast reaches them
     const uint32_t tmem = bar.tmem_holder;
-    const uint32_t crank = cluster_ctarank();
-    const uint16_t cmask = static_cast<uint16_t>((1u << a.csize) - 1u);
-    const int xrows = BM / a.csize;  // X rows this CTA loads for the cluster
 
     // Registers per warpgroup, set at the top of each role: the producers and
     // MMA issuers (warps 0-3) need few; each epilogue thread (warps 4-7,
@@ -218,19 +210,14 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         // test-only injection: no X stage is ever issued, so the waits on it
         // run out and the launch ends with the timeout status
         const int xgroups = (a.inject & kInjectStallPipeline) ? 0 : ngroups;
-        for (int g = 0; g < xgroups; ++g) {
+        int issued = 0;
+        for (int g = 0; g < xgroups; ++g, ++issued) {
             if (g >= XP && !mbar_wait<kHintProd>(&bar.xempty[xs], xph ^ 1, a.status)) break;
             if (lane == 0) {
-                mbar_arrive_expect_tx(&bar.xfull[xs], 2 * X_BYTES);  // both boxes, from all slices
-                unsigned char *dst = smem + OFF_X + xs * 2 * X_BYTES + static_cast<int>(crank) * xrows * 128;
-                const int row = m0 + static_cast<int>(crank) * xrows;
-                for (int h = 0; h < 2; ++h) {
-                    if (a.csize > 1)
-                        tma_load_2d_multicast_hint(dst + h * X_BYTES, &tmX, g * GK + h * BK, row, &bar.xfull[xs],
-                                                   cmask, pol_x);
-                    else
-                        tma_load_2d_hint(dst + h * X_BYTES, &tmX, g * GK + h * BK, row, &bar.xfull[xs], pol_x);
-                }
+                mbar_arrive_expect_tx(&bar.xfull[xs], 2 * X_BYTES);  // both boxes
+                unsigned char *dst = smem + OFF_X + xs * 2 * X_BYTES;
+                for (int h = 0; h < 2; ++h)
+                    tma_load_2d_hint(dst + h * X_BYTES, &tmX, g * GK + h * BK, m0, &bar.xfull[xs], pol_x);
             }
             __syncwarp();
             if (++xs == XP) {
@@ -238,6 +225,12 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                 xph ^= 1;
             }
         }
+        // No copy of this CTA may still be landing when it exits: wait
+        // (bounded, whatever the status word says) for the tiles issued and
+        // not known to be consumed, and for the scale/zero copies.
+        for (int it = issued > XP ? issued - XP : 0; it < issued; ++it)
+            mbar_wait(&bar.xfull[it % XP], (it / XP) & 1, nullptr);
+        mbar_wait(&bar.szfull, 0, nullptr);
     } else if (warp == 2) {
         reg_release<kRegLight>();
         // ---------------------------------------- packed-code TMA producer
@@ -247,13 +240,17 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_first();
             const int nwb = (ngroups + 1) / 2;
-            for (int wb = 0; wb < nwb; ++wb) {
+            int issued = 0;
+            for (int wb = 0; wb < nwb; ++wb, ++issued) {
                 const int ws = wb % WS;
                 if (wb >= WS && !mbar_wait<kHintProd>(&bar.wempty[ws], ((wb / WS) - 1) & 1, a.status)) break;
                 mbar_arrive_expect_tx(&bar.wfull[ws], W_BYTES);
                 // rows past N (last and padding tiles) read as zeros
                 tma_load_2d_hint(smem + a.off_w + ws * W_BYTES, &tmW, wb * 128, n0, &bar.wfull[ws], pol_w);
             }
+            // as for the X tiles: no copy in flight when the CTA exits
+            for (int it = issued > WS ? issued - WS : 0; it < issued; ++it)
+                mbar_wait(&bar.wfull[it % WS], (it / WS) & 1, nullptr);
         }
     } else if (warp == 1 || warp == 3) {
         reg_release<kRegLight>();
@@ -273,10 +270,12 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         // after the accumulator, in a second round.
         constexpr uint32_t idesc = idesc_kind_f16(128, BM, 1u);  // BF16, M = 128 lanes, N = 128 rows of X
         const bool x_second = (XP & 1) && XP < DB + 2;
+        // test-only injection: the issuers take nothing, so the producers'
+        // waits for free stages run out with their copies issued
         const int g0 = warp == 1 ? 0 : 1;
-        bool ok = true;
+        bool ok = !(a.inject & kInjectStallConsumers);
         int xs = g0, xph = 0, db = g0, dph = 0, ap = g0, aph = 0;
-        for (int g = g0; g < ngroups; g += 2) {
+        for (int g = g0; ok && g < ngroups; g += 2) {
             uint64_t *wbar = nullptr;
             uint32_t par = 0;
             if (lane == 0) {
@@ -303,10 +302,7 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                 for (int k = 0; k < GK / 16; ++k)
                     umma_f16_tmem_a(t_acc, a_t + 8 * k,
                                     smem_desc_sw128_kmajor(b_addr + (k >> 2) * X_BYTES + 32 * (k & 3)), idesc, k != 0);
-                if (a.csize > 1)
-                    umma_commit_multicast(&bar.xempty[xs], cmask);
-                else
-                    umma_commit(&bar.xempty[xs]);
+                umma_commit(&bar.xempty[xs]);
                 umma_commit(&bar.aempty[ap]);
                 umma_commit(&bar.accfull[db]);
             }
@@ -511,8 +507,6 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar.done);
     }
-    // no CTA leaves while cluster peers may still signal or fill its memory
-    cluster_sync();
 }
 
 
@@ -524,19 +518,13 @@ cudaError_t launch_gemm_int4(const uint16_t *X, const uint8_t *qw, const uint16_
     if (K > MAX_K) return cudaErrorNotSupported;
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
-    const unsigned gx0 = static_cast<unsigned>((N + BNW - 1) / BNW), gy = static_cast<unsigned>((M + BM - 1) / BM);
-    // X multicast across clusters of 4 for a single M tile; with several M
-    // tiles the cluster-wide stage release and cluster scheduling cost more
-    // than the L2-resident X reads it saves (measured at M = 2048: 398 us with
-    // clusters of 4, 372 us without)
-    const int csize = gy > 1 ? 1 : gx0 >= 4 ? 4 : gx0 >= 2 ? 2 : 1;
-    const unsigned gx = (gx0 + csize - 1) / csize * csize;  // padding CTAs share the X loads only
+    const unsigned gx = static_cast<unsigned>((N + BNW - 1) / BNW), gy = static_cast<unsigned>((M + BM - 1) / BM);
     CUtensorMap tmX, tmW;
     {
-        // X as BF16 [M, K]; box of 64 (one K block) x 128/csize rows, 128-byte swizzle
+        // X as BF16 [M, K]; box of 64 (one K block) x 128 rows, 128-byte swizzle
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-        const cuuint32_t box[2] = {BK, static_cast<cuuint32_t>(BM / csize)};
+        const cuuint32_t box[2] = {BK, static_cast<cuuint32_t>(BM)};
         const cuuint32_t estr[2] = {1, 1};
         if (enc(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(X), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -555,7 +543,6 @@ cudaError_t launch_gemm_int4(const uint16_t *X, const uint8_t *qw, const uint16_
             return cudaErrorInvalidValue;
     }
     GemmArgs a;
-    a.csize = csize;
     a.s = s;
     a.z = z;
     a.Y = Y;
@@ -580,9 +567,8 @@ cudaError_t launch_gemm_int4(const uint16_t *X, const uint8_t *qw, const uint16_
     // one instance per zero-point mode, each configured once per device
     const int sym = z ? 0 : 1;
     auto kern = sym ? gemm_int4_tc_kernel<true> : gemm_int4_tc_kernel<false>;
-    static int configured[2][64] = {{0}};
-    const int d = dev.device & 63;
-    if (configured[sym][d] == 0) {
+    static SmemLimit limit[2];
+    auto check_regs = [kern]() -> cudaError_t {
         // the per-role register split (setmaxnreg) must fit in what the block
         // is launched with, or the growing warpgroups would wait for ever
         cudaFuncAttributes fa;
@@ -592,24 +578,15 @@ cudaError_t launch_gemm_int4(const uint16_t *X, const uint8_t *qw, const uint16_
         if (launch_regs * THREADS < kRegSplit || launch_regs < static_cast<int>(kRegBuild) ||
             launch_regs < static_cast<int>(kRegLight) || launch_regs > static_cast<int>(kRegEpi))
             return cudaErrorNotSupported;
-    }
-    if (configured[sym][d] < smem) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        configured[sym][d] = smem;
-    }
+        return cudaSuccess;
+    };
+    if (cudaError_t e = limit[sym].ensure(reinterpret_cast<const void *>(kern), dev.device, smem, check_regs))
+        return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(gx, gy, 1);
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(csize);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, tmX, tmW, a);
 }
 

@@ -28,6 +28,7 @@
 
 #include "common.cuh"
 #include "gemv_common.cuh"
+#include "kernels.h"
 
 namespace w4 {
 
@@ -118,6 +119,15 @@ __device__ __forceinline__ void gemv_producer(const GemvParams &a, GemvHeader<CW
         }
     };
     int slot = 0, phase = 0, issued = 0;
+    // After a wait ran out: wait (bounded, whatever the status word says)
+    // until the copies of every stage issued and not yet retired have landed,
+    // so that no copy into this CTA's shared memory is in flight when it
+    // exits.  A stage's full barrier completes on its own copies alone.
+    auto drain_copies = [&]() {
+        const int first = issued > a.stages ? issued - a.stages : 0;
+        for (int it = first; it < issued; ++it)
+            mbar_wait(&h.full[it % a.stages], (it / a.stages) & 1, nullptr);
+    };
     // Expert slot (FP4; INT4 has one slot of N rows) holding row `begin`.
     int64_t i_slot = FP4 ? begin / a.rows_per_slot : 0;
     int64_t slot_end = FP4 ? (i_slot + 1) * a.rows_per_slot : end;
@@ -126,7 +136,10 @@ __device__ __forceinline__ void gemv_producer(const GemvParams &a, GemvHeader<CW
         const bool recycle = issued >= a.stages;
         StageMeta old{};
         if (recycle) {
-            if (!mbar_wait(&h.empty[slot], phase ^ 1, a.status)) return;
+            if (!mbar_wait(&h.empty[slot], phase ^ 1, a.status)) {
+                drain_copies();
+                return;
+            }
             old = h.meta[slot];
             __syncwarp();
         }
@@ -191,7 +204,10 @@ __device__ __forceinline__ void gemv_producer(const GemvParams &a, GemvHeader<CW
     const int first = issued > a.stages ? issued - a.stages : 0;
     for (int it = first; it < issued; ++it) {
         const int sl = it % a.stages;
-        if (!mbar_wait(&h.empty[sl], (it / a.stages) & 1, a.status)) return;
+        if (!mbar_wait(&h.empty[sl], (it / a.stages) & 1, a.status)) {
+            drain_copies();
+            return;
+        }
         finalize(sl, (it / a.stages) & 1, h.meta[sl]);
     }
 }
@@ -585,6 +601,9 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_stream_kernel(const Gem
     // part it owns into registers.
     if (!FP4) gemv_prefetch_groups<SYM>(a, begin, end, threadIdx.x, CW * 32);
     pdl_wait();
+    // test-only injection: the consumers take no stage, so the producer's
+    // waits for free stages run out with its copies issued
+    if (a.inject & kInjectStallConsumers) return;
     if constexpr (MV == 1)
         gemv_convert_x<FP4, CW>(a, a.x, smem + a.x_off, warp, lane);
     else
@@ -642,13 +661,8 @@ cudaError_t gemv_launch(GemvParams a, cudaStream_t st, int device, int num_sms, 
     if (stages < 2) return cudaErrorInvalidValue;
     a.stages = stages;
     const int smem = a.stage_off + stages * a.stage_bytes;
-    static int configured[64] = {0};
-    const int d = device & 63;
-    if (configured[d] < smem) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        configured[d] = smem;
-    }
+    static SmemLimit limit;
+    if (cudaError_t e = limit.ensure(reinterpret_cast<const void *>(kern), device, smem)) return e;
     int64_t ctas = num_sms;
     const int64_t max_ctas = (a.V + 1) / 2;  // at least two rows each
     if (ctas > max_ctas) ctas = max_ctas;

@@ -3,9 +3,35 @@
 #pragma once
 
 #include <cstdint>
+#include <mutex>
 #include <cuda_runtime.h>
 
 namespace w4 {
+
+// A kernel's dynamic shared-memory limit, raised once per device to the
+// largest size launched so far.  Host threads may launch concurrently, so the
+// record is kept under a mutex.  `check` (optional) runs once per device
+// before the first raise and may refuse the kernel.
+struct SmemLimit {
+    std::mutex mu;
+    int bytes[64] = {};
+    template <typename Check>
+    cudaError_t ensure(const void *kern, int device, int need, Check check) {
+        std::lock_guard<std::mutex> lk(mu);
+        const int d = device & 63;
+        if (bytes[d] >= need) return cudaSuccess;
+        if (bytes[d] == 0) {
+            const cudaError_t e = check();
+            if (e != cudaSuccess) return e;
+        }
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, need);
+        if (e == cudaSuccess) bytes[d] = need;
+        return e;
+    }
+    cudaError_t ensure(const void *kern, int device, int need) {
+        return ensure(kern, device, need, [] { return cudaSuccess; });
+    }
+};
 
 struct DeviceInfo {
     int device;

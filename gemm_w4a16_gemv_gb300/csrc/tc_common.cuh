@@ -142,48 +142,6 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *tmap) {
 
 namespace w4 {
 
-// ----------------------------------------------------------- clusters
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-// Whole-cluster barrier (every thread of every CTA of the cluster).
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// 2-D tiled load multicast to the CTAs of `mask` (same shared-memory offset
-// in each; each destination's barrier at the same offset receives the bytes).
-__device__ __forceinline__ void tma_load_2d_multicast(void *dst, const CUtensorMap *tmap, int c0, int c1,
-                                                      uint64_t *bar, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
-        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(mask)
-        : "memory");
-}
-
-// The same with an L2 cache policy for the loaded lines.
-__device__ __forceinline__ void tma_load_2d_multicast_hint(void *dst, const CUtensorMap *tmap, int c0, int c1,
-                                                           uint64_t *bar, uint16_t mask, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(mask), "l"(policy)
-        : "memory");
-}
-
-// Commit whose arrival is delivered to the barrier at the same offset in
-// every CTA of `mask`.
-__device__ __forceinline__ void umma_commit_multicast(uint64_t *bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(mask)
-        : "memory");
-}
-
 // a - b for two BF16 pairs in one fused multiply-add (a * 1 + (-b), a single
 // rounding: exact whenever the difference is a BF16 number).
 __device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {

@@ -23,6 +23,10 @@
  * Conventions shared by every entry point:
  *  - all data pointers are DEVICE pointers owned by the caller; the library
  *    keeps no reference after the call returns and allocates no memory;
+ *  - kernels run on the CURRENT device (cudaSetDevice) and every data
+ *    pointer must be memory of that device (device memory of it, or managed
+ *    memory): a pointer to another device's memory or to host memory is
+ *    refused with W4A16_ERR_INVALID_ARG before anything is launched;
  *  - every data pointer must be 16-byte aligned (else W4A16_ERR_MISALIGNED);
  *  - an output must not overlap any input of the same call (CTAs write
  *    their outputs while others may still read the inputs); this is not
@@ -35,7 +39,12 @@
  *    message available from w4a16_last_error_string();
  *  - kernels never trap: a device-side problem (an expert id out of range, a
  *    pipeline wait that timed out) sets a sticky per-device status word that
- *    w4a16_check_device_error() reports and clears.
+ *    w4a16_check_device_error() reports and clears.  There is one status
+ *    word per device, shared by the launches of every stream and host thread
+ *    on that device.
+ *  - host threads may call concurrently (the per-device set-up made on first
+ *    use is guarded); the usual rule holds that concurrent calls on one
+ *    stream are ordered as the host makes them.
  */
 #ifndef W4A16_H
 #define W4A16_H
@@ -203,8 +212,13 @@ int w4a16_graph_launch(w4a16_graph_t graph, void *stream);
 int w4a16_graph_destroy(w4a16_graph_t graph);
 
 /*
- * Synchronises `stream`, then reads and clears this device's sticky status.
- * Returns W4A16_OK, W4A16_ERR_TIMEOUT, W4A16_ERR_DEVICE or W4A16_ERR_CUDA.
+ * Synchronises `stream`, then reads and clears the current device's sticky
+ * status.  Returns W4A16_OK, W4A16_ERR_TIMEOUT, W4A16_ERR_DEVICE or
+ * W4A16_ERR_CUDA.  The status word is per device, not per stream: only
+ * `stream` is synchronised, so a bit set by a launch on another stream that
+ * is still running may be missed, and a bit set by another stream's launch
+ * is reported (and cleared) here.  Synchronise the device first (or use one
+ * stream) to attribute the status to particular launches.
  */
 int w4a16_check_device_error(void *stream);
 
@@ -217,7 +231,11 @@ int w4a16_check_device_error(void *stream);
  *      stages of the GEMM), so its waits run out after their limit (about
  *      2 s); the launch then returns with an unspecified output and
  *      w4a16_check_device_error reports W4A16_ERR_TIMEOUT (the context stays
- *      usable).
+ *      usable);
+ *   2  the same launches issue their pipeline stages but never consume
+ *      them, so the producers' waits for free stages run out while their
+ *      copies are issued: each producer then waits for its own copies to
+ *      land before the launch ends (W4A16_ERR_TIMEOUT as for flag 1).
  * The flags are a host-side setting passed to each later launch (a CUDA
  * graph keeps the flags it was captured with).  Not for production use.
  * Returns W4A16_OK, or W4A16_ERR_INVALID_ARG for an unknown flag.

@@ -46,7 +46,10 @@ def build(force: bool = False) -> str:
     tmp = _LIB + ".tmp.%d" % os.getpid()
     cmd = ["gcc", "-O2", "-ffp-contract=off", "-std=c11", "-Wall", "-shared",
            "-fPIC", _SRC, "-o", tmp, "-lm"]
-    subprocess.run(cmd, check=True)
+    # OpenMP only spreads independent output elements over threads (for the
+    # timed all-cores baseline); without it the same code runs serially.
+    if subprocess.run(cmd[:1] + ["-fopenmp"] + cmd[1:], capture_output=True).returncode != 0:
+        subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB)
     return _LIB
 
@@ -82,6 +85,8 @@ def _load():
         lib.oracle_moe_fp4.restype = None
         lib.oracle_gemm_bf16.argtypes = [P, P, I64, I64, I64, P]
         lib.oracle_gemm_bf16.restype = None
+        lib.oracle_set_threads.argtypes = [ctypes.c_int]
+        lib.oracle_set_threads.restype = None
         _lib = lib
         return lib
 
@@ -100,6 +105,13 @@ def _ptr(a: np.ndarray):
 def _zptr(z):
     """Zero points or NULL (symmetric INT4)."""
     return ctypes.c_void_p(None) if z is None else _ptr(z)
+
+
+def set_threads(n: int) -> None:
+    """Threads used by the products (default 1).  Every output element is
+    still computed by one thread in the serial order, so results are the
+    same for any count; only the timed CPU baseline raises it."""
+    _load().oracle_set_threads(int(n))
 
 
 # ----------------------------------------------------------------- formats

@@ -38,6 +38,17 @@
 #include <string.h>
 #include <math.h>
 
+/* Threads for the products below (1 unless oracle_set_threads raises it).
+ * Each output element is computed by one thread exactly as in the serial
+ * loop (same operations, k ascending), so the results do not depend on the
+ * thread count; only the timed CPU baseline uses more than one. */
+static int g_threads = 1;
+
+void oracle_set_threads(int n)
+{
+    g_threads = n < 1 ? 1 : n;
+}
+
 /* ---------------------------------------------------------------- formats */
 
 /* IEEE 754 binary16 bit pattern -> value (format definition). */
@@ -175,6 +186,7 @@ void oracle_gemm_int4(const uint16_t *X, const uint8_t *qw, const uint16_t *s,
                       int64_t g, double *Y)
 {
     int64_t G = K / g;
+#pragma omp parallel for collapse(2) schedule(static) num_threads(g_threads) if (g_threads > 1)
     for (int64_t m = 0; m < M; ++m) {
         for (int64_t n = 0; n < N; ++n) {
             double acc = 0.0;
@@ -211,6 +223,7 @@ void oracle_moe_fp4(const uint16_t *x, const uint8_t *qw, const uint16_t *s,
                 *bad += 1;
             continue;
         }
+#pragma omp parallel for schedule(static) num_threads(g_threads) if (g_threads > 1)
         for (int64_t n = 0; n < N; ++n) {
             int64_t r = e * N + n;   /* row of the [E*N, K] stack */
             double acc = 0.0;
@@ -235,6 +248,7 @@ void oracle_moe_fp4(const uint16_t *x, const uint8_t *qw, const uint16_t *s,
 void oracle_gemm_bf16(const uint16_t *X, const uint16_t *W, int64_t M,
                       int64_t N, int64_t K, double *Y)
 {
+#pragma omp parallel for collapse(2) schedule(static) num_threads(g_threads) if (g_threads > 1)
     for (int64_t m = 0; m < M; ++m) {
         for (int64_t n = 0; n < N; ++n) {
             double acc = 0.0;

@@ -68,12 +68,13 @@ def test_moe_writes_only_its_output():
     assert_close(host_bits16(y).reshape(topk, N), ref, "guarded moe")
 
 
-def _inject(w4, on):
-    w4.w4a16_debug_inject(w4.INJECT_STALL_PIPELINE if on else 0)
-
-
+@pytest.mark.parametrize("flag", ["producers", "consumers"])
 @pytest.mark.parametrize("kind", ["gemv", "moe", "gemm"])
-def test_bounded_wait_reports_timeout_and_recovers(kind):
+def test_bounded_wait_reports_timeout_and_recovers(kind, flag):
+    """flag "producers": no stage is ever issued, the consumers' waits run
+    out.  flag "consumers": stages are issued but never taken, so the
+    producers' waits for free stages run out with their copies issued; each
+    producer then waits for its own copies before the launch ends."""
     torch, w4 = cuda_or_skip()
     assert w4.w4a16_check_device_error() == 0
     if kind == "gemv":
@@ -96,14 +97,14 @@ def test_bounded_wait_reports_timeout_and_recovers(kind):
                 dev_tensor(p["s"], torch.float16), dev_tensor(p["z"], torch.float16))
         run = lambda: w4.w4a16_gemm(*args)
         ref = oracle.gemm_int4(p["x"], p["qw"], p["s"], p["z"], K=K)
-    _inject(w4, True)
+    w4.w4a16_debug_inject(w4.INJECT_STALL_PIPELINE if flag == "producers" else w4.INJECT_STALL_CONSUMERS)
     try:
         t0 = time.monotonic()
         run()
         status = w4.w4a16_check_device_error()  # synchronises; reads and clears
         waited = time.monotonic() - t0
     finally:
-        _inject(w4, False)
+        w4.w4a16_debug_inject(0)
     assert status == 5  # W4A16_ERR_TIMEOUT
     # the waits ran out at their limit (about 2 s), not at once and not never
     assert 1.5 < waited < 30.0, waited
@@ -112,3 +113,28 @@ def test_bounded_wait_reports_timeout_and_recovers(kind):
     torch.cuda.synchronize()
     assert w4.w4a16_check_device_error() == 0
     assert_close(host_bits16(y).reshape(ref.shape), ref, kind + " after recovery")
+
+
+def test_pointers_must_be_memory_of_the_current_device():
+    """A host pointer (here a 16-byte-aligned numpy buffer) passed as an
+    activation is refused on the host with INVALID_ARG, and nothing runs."""
+    import ctypes
+    torch, w4 = cuda_or_skip()
+    N, K = 64, 256
+    p = synth.int4_problem(N, K, seed=2)
+    qw, s, z = dev_tensor(p["qw"], torch.uint8), dev_tensor(p["s"], torch.float16), dev_tensor(p["z"], torch.float16)
+    y = torch.zeros(N, dtype=torch.bfloat16, device="cuda")
+    host = np.zeros(K + 8, dtype=np.uint16)
+    off = (-host.ctypes.data % 16) // 2
+    hx = host[off:off + K]
+    assert hx.ctypes.data % 16 == 0
+    lib = w4.lib()
+    st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    r = lib.w4a16_gemv(ctypes.c_void_p(hx.ctypes.data), ctypes.c_void_p(qw.data_ptr()),
+                       ctypes.c_void_p(s.data_ptr()), ctypes.c_void_p(z.data_ptr()),
+                       ctypes.c_void_p(y.data_ptr()), N, K, 128, st)
+    assert r == 1, r  # W4A16_ERR_INVALID_ARG
+    assert "not device memory" in w4.w4a16_last_error_string() or "not CUDA memory" in w4.w4a16_last_error_string()
+    torch.cuda.synchronize()
+    assert int(torch.count_nonzero(y.view(torch.int16))) == 0  # nothing was launched
+    assert w4.w4a16_check_device_error() == 0

@@ -46,6 +46,8 @@ def test_pins_reject_mutated_oracle(name, tmp_path):
                                                   "__pycache__"))
     shutil.copytree(os.path.join(ROOT, "tests"), tmp_path / "tests",
                     ignore=shutil.ignore_patterns("__pycache__"))
+    shutil.copytree(os.path.join(ROOT, "synth"), tmp_path / "synth",
+                    ignore=shutil.ignore_patterns("__pycache__"))
     shutil.copy(os.path.join(ROOT, "pytest.ini"), tmp_path / "pytest.ini")
     (tmp_path / "oracle" / "w4a16_oracle.c").write_text(src.replace(before, after))
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p",

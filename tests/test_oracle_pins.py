@@ -15,6 +15,7 @@ import pytest
 import torch
 
 import oracle
+import synth
 from tests.conftest import read_golden
 
 ONE_BF16 = 0x3F80
@@ -389,3 +390,20 @@ def test_two_pass_within_bf16_weight_rounding_of_fused():
     bound = 2.0 ** -9 * (np.abs(bf16_vals(X).reshape(2, K)) @ np.abs(Wf.astype(np.float64)).T)
     assert np.all(np.abs(two - fused) <= bound + 1e-12)
     assert np.any(two != fused)  # the rounding is real
+
+
+def test_thread_count_does_not_change_results():
+    """The oracle's optional threads only spread independent output elements:
+    results are bitwise those of the serial loop."""
+    p = synth.int4_problem(37, 512, M=3, seed=5)
+    m = synth.fp4_moe_problem(6, 40, 256, 4, seed=5)
+    ref_g = oracle.gemm_int4(p["x"], p["qw"], p["s"], p["z"], K=512)
+    ref_m, _ = oracle.moe_fp4(m["x"], m["qw"], m["s"], m["ids"], E=6, N=40, K=256)
+    try:
+        oracle.set_threads(4)
+        g4 = oracle.gemm_int4(p["x"], p["qw"], p["s"], p["z"], K=512)
+        m4, _ = oracle.moe_fp4(m["x"], m["qw"], m["s"], m["ids"], E=6, N=40, K=256)
+    finally:
+        oracle.set_threads(1)
+    assert np.array_equal(g4.view(np.uint64), ref_g.view(np.uint64))
+    assert np.array_equal(m4.view(np.uint64), ref_m.view(np.uint64))
