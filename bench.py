@@ -4,8 +4,10 @@
 Workload (one "step"): the decode MLP GEMV pair at M = 1 -- the up projection
 N=15360, K=3840 followed by the down projection N=3840, K=15360, INT4
 asymmetric weights with FP16 scale/zero per 128 codes, BF16 activations and
-outputs (Gemma4-12B-shaped linears; synthetic seeded data).  Eight rotating
-weight sets (about 500 MB) keep every step's weights out of the 129 MB L2.
+outputs (Gemma4-12B-shaped linears; synthetic seeded data), run as one chain
+launch (w4a16_linear_chain: both linears in one persistent kernel).  Eight
+rotating weight sets (about 500 MB) keep every step's weights out of the
+129 MB L2.
 
 Metric: whole-job HBM throughput in GB/s over the algorithmic bytes (packed
 weights + scales + zeros + activations + outputs).  Also reported: the
@@ -53,7 +55,7 @@ STEP_BYTES = gemv_bytes(*UP) + gemv_bytes(*DOWN)
 def kernel_sources_digest():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gemm_w4a16_gemv_gb300", "csrc")
-    for name in ("gemv_kernel.cuh", "gemv_common.cuh", "common.cuh", "gemv_int4.cu"):
+    for name in ("gemv_kernel.cuh", "gemv_common.cuh", "common.cuh", "gemv_chain.cu"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -72,7 +74,7 @@ def read_peaks():
 def read_traffic(digest):
     """DRAM bytes per launch of the GEMV kernel from the committed ncu summary,
     or None when the summary was taken on different kernel sources."""
-    path = os.path.join(ROOT, "profiles", "gemv_int4_decode_mlp_pair.md")
+    path = os.path.join(ROOT, "profiles", "gemv_chain_decode_mlp_pair.md")
     try:
         text = open(path).read()
     except OSError:
@@ -85,7 +87,7 @@ def read_traffic(digest):
     if vals.get("kernel_sources_sha256_16") != digest:
         return None
     try:
-        return float(vals["dram_bytes_per_launch_pair_avg"])
+        return float(vals["dram_bytes_per_launch"])
     except (KeyError, ValueError):
         return None
 
@@ -468,6 +470,28 @@ def decode_step(torch, w4, synth, dev, stream, hbm_peak, fused=False):
             "device_status": status}
 
 
+def decode_step_chain(torch, w4, synth, dev, stream, hbm_peak, fused=False):
+    """The decode step as chains of linears (w4a16_linear_chain: at most 192
+    linears per persistent launch, two launches for the 329), timed per step,
+    against the same step's per-linear launches from one graph."""
+    ops = decode_step_ops(torch, synth, dev, fused)
+    nbytes = sum(gemv_bytes(op[1].shape[0], 2 * op[1].shape[1]) for op in ops)
+    arr = w4.w4a16_linear_array(ops)
+    scratch = w4.chain_scratch(len(ops), dev)
+    t = time_launches(torch, lambda i: w4.w4a16_linear_chain(arr, scratch, count=len(ops)), 20, stream)
+    torch.cuda.synchronize()
+    h0 = time.perf_counter()
+    for _ in range(5):
+        w4.w4a16_linear_chain(arr, scratch, count=len(ops))
+    h1 = time.perf_counter()
+    torch.cuda.synchronize()
+    status = w4.w4a16_check_device_error()
+    gbs = nbytes / t / 1e9
+    return {"linears": len(ops), "launches": (len(ops) + 191) // 192, "weights_GB": round(nbytes / 1e9, 3),
+            "us": round(t * 1e6, 1), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm_peak, 3),
+            "host_us_per_call": round((h1 - h0) / 5 * 1e6, 1), "device_status": status}
+
+
 def per_config(torch, w4, synth, dev, stream, hbm_peak, tf_peak):
     """Kernel-only timings of every configuration (launches back to back)."""
     out = {}
@@ -572,6 +596,11 @@ def per_config(torch, w4, synth, dev, stream, hbm_peak, tf_peak):
         except Exception as e:
             out[name] = {"unavailable": str(e).splitlines()[0][:120]}
         torch.cuda.empty_cache()
+        try:
+            out[name + "_chain"] = decode_step_chain(torch, w4, synth, dev, stream, hbm_peak, fused)
+        except Exception as e:
+            out[name + "_chain"] = {"unavailable": str(e).splitlines()[0][:120]}
+        torch.cuda.empty_cache()
     return out
 
 
@@ -594,10 +623,23 @@ def run_ours(args):
     yu = torch.empty(UP[0], dtype=torch.bfloat16, device=dev)
     yd = torch.empty(DOWN[0], dtype=torch.bfloat16, device=dev)
 
-    def step(i, x_up=xu, x_dn=xd, y_up=yu, y_dn=yd):
+    # one op array per weight set: the pair as a chain (the two linears are
+    # independent, so the chain streams them back to back in one launch)
+    scratch = w4.chain_scratch(2, dev)
+
+    def pair_ops(i, x_up, x_dn, y_up, y_dn):
         a, b = up_sets[i % L2_SETS], dn_sets[i % L2_SETS]
-        w4.w4a16_gemv(x_up, a["qw"], a["s"], a["z"], y_up)
-        w4.w4a16_gemv(x_dn, b["qw"], b["s"], b["z"], y_dn)
+        return w4.w4a16_linear_array([(x_up, a["qw"], a["s"], a["z"], y_up), (x_dn, b["qw"], b["s"], b["z"], y_dn)])
+
+    arrays = [pair_ops(i, xu, xd, yu, yd) for i in range(L2_SETS)]
+
+    def step(i):
+        w4.w4a16_linear_chain(arrays[i % L2_SETS], scratch, count=2)
+
+    def step_two_launches(i):
+        a, b = up_sets[i % L2_SETS], dn_sets[i % L2_SETS]
+        w4.w4a16_gemv(xu, a["qw"], a["s"], a["z"], yu)
+        w4.w4a16_gemv(xd, b["qw"], b["s"], b["z"], yd)
 
     for i in range(args.warmup):
         step(i)
@@ -658,16 +700,16 @@ def run_ours(args):
                            torch.distributed.get_backend() == "nccl" else None)
     value = STEP_BYTES * args.steps * world / elapsed_max / 1e9
 
-    # roofline of the GEMV kernel: the step is two launches of it
-    launch_s = elapsed / (2 * args.steps)
-    achieved = (STEP_BYTES / 2) / launch_s / 1e9
+    # roofline of the chain kernel: one launch per step
+    launch_s = elapsed / args.steps
+    achieved = STEP_BYTES / launch_s / 1e9
     digest = kernel_sources_digest()
     traffic = read_traffic(digest)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
                 "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs: copy bandwidth)" if peak_src == "measured"
-                else "fallback 6.8 TB/s", "kernel": "gemv_stream_kernel<INT4>",
-                "bytes_per_launch": STEP_BYTES // 2, "launch_us": round(launch_s * 1e6, 3)}
+                else "fallback 6.8 TB/s", "kernel": "gemv_chain_kernel (up and down linears in one launch)",
+                "bytes_per_launch": STEP_BYTES, "launch_us": round(launch_s * 1e6, 3)}
 
     # end to end through the C ABI with host buffers: H2D x, two GEMVs, D2H y
     xu_pin = xu_h.clone().pin_memory()
@@ -677,11 +719,12 @@ def run_ours(args):
     xu_d = torch.empty_like(xu)
     xd_d = torch.empty_like(xd)
     e2e_steps = min(args.steps, 300)
+    e2e_arrays = [pair_ops(i, xu_d, xd_d, yu, yd) for i in range(L2_SETS)]
 
     def e2e_step(i):
         xu_d.copy_(xu_pin, non_blocking=True)
         xd_d.copy_(xd_pin, non_blocking=True)
-        step(i, xu_d, xd_d, yu, yd)
+        w4.w4a16_linear_chain(e2e_arrays[i % L2_SETS], scratch, count=2)
         yu_pin.copy_(yu, non_blocking=True)
         yd_pin.copy_(yd, non_blocking=True)
         torch.cuda.current_stream().synchronize()
@@ -702,7 +745,10 @@ def run_ours(args):
 
     extra = {}
     if rank == 0 and not args.no_configs:
-        extra = per_config(torch, w4, synth, dev, stream, hbm_peak, tf_peak)
+        t2 = time_launches(torch, step_two_launches, 400, stream)
+        extra["gemv_pair_two_launches"] = {"us": round(t2 * 1e6, 2), "GB/s": round(STEP_BYTES / t2 / 1e9, 1),
+                                           "frac_hbm": round(STEP_BYTES / t2 / 1e9 / hbm_peak, 3)}
+        extra.update(per_config(torch, w4, synth, dev, stream, hbm_peak, tf_peak))
     base = None
     if rank == 0 and not args.no_cpu:
         try:
@@ -714,16 +760,21 @@ def run_ours(args):
     line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(elapsed_max / args.steps * 1e3, 5), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "scaling": "weak", "vs_baseline": None, "dtype": "s32+f32",
             "data": "synthetic",
             "config": {"workload": WORKLOAD, "bytes_per_step": STEP_BYTES,
+                       "arithmetic": ("u4 codes times s16 fixed-point activations (one power-of-two scale per "
+                                      "128-element group; the largest values of each 64-element half group above "
+                                      "its third-largest binade enter exactly in f32) in exact s32 dot products; "
+                                      "f32 scale, zero point and accumulation; bf16 output"),
                        "l2": "%d rotating weight sets of %.1f MB each (inputs larger than the 129 MB L2)"
                              % (L2_SETS, STEP_BYTES / 1e6),
-                       "launch": ("CUDA graph of %d steps (programmatic dependent launch between kernels)" % L2_SETS)
-                       if graphs is not None else "eager (programmatic dependent launch between kernels)",
+                       "launch": ("CUDA graph of %d steps, one chain launch each (programmatic dependent launch "
+                                  "between kernels)" % L2_SETS)
+                       if graphs is not None else "eager chain launches (programmatic dependent launch between kernels)",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": roofline, "cpu_baseline": base, "e2e": e2e,
-            "gpu_launches": 2 * args.steps, "clocks": clk, "device_status": status,
+            "gpu_launches": args.steps, "clocks": clk, "device_status": status,
             "per_config": extra}
     print(json.dumps(line), flush=True)
     return 0

@@ -23,6 +23,7 @@ __all__ = [
     "w4a16_check_device_error", "w4a16_last_error_string", "w4a16_version",
     "w4a16_debug_inject", "INJECT_STALL_PIPELINE", "INJECT_STALL_CONSUMERS",
     "w4a16_linear", "w4a16_linear_array", "w4a16_linear_sequence", "w4a16_graph_create", "w4a16_graph_launch",
+    "w4a16_linear_chain", "w4a16_linear_chain_scratch_bytes", "chain_scratch",
     "w4a16_graph_destroy", "W4A16Graph",
     "library_path", "W4A16Error", "STATUS", "FMT_INT4", "FMT_FP4",
     "OUT_F32", "OUT_BF16",
@@ -59,6 +60,8 @@ SIGNATURES = {
     "fp4_moe_gemv": ([_P, _P, _P, _P, _INT, _P, _I64, _I64, _I64, _INT, _P], _INT),
     "w4a16_dequant": ([_INT, _P, _P, _P, _P, _INT, _I64, _I64, _INT, _P], _INT),
     "w4a16_linear_sequence": ([_OPS, _INT, _INT, _P], _INT),
+    "w4a16_linear_chain": ([_OPS, _INT, _INT, _P, _I64, _P], _INT),
+    "w4a16_linear_chain_scratch_bytes": ([_INT], _I64),
     "w4a16_graph_create": ([_OPS, _INT, _INT, ctypes.POINTER(ctypes.c_void_p)], _INT),
     "w4a16_graph_launch": ([_P, _P], _INT),
     "w4a16_graph_destroy": ([_P], _INT),
@@ -256,6 +259,43 @@ def w4a16_linear_sequence(ops, group: int = 128, stream=None, count=None):
         dev = ops[0][1].device if ops else torch.cuda.current_device()
     with torch.cuda.device(dev):  # the library launches on the current device
         _check(lib().w4a16_linear_sequence(arr, n, group, _stream(stream, dev)))
+
+
+def w4a16_linear_chain_scratch_bytes(count: int) -> int:
+    """Bytes of scratch memory w4a16_linear_chain needs for `count` ops."""
+    return int(lib().w4a16_linear_chain_scratch_bytes(int(count)))
+
+
+def chain_scratch(count: int, device=None) -> torch.Tensor:
+    """A zeroed scratch buffer (int32) for chains of up to `count` ops."""
+    n = (w4a16_linear_chain_scratch_bytes(count) + 3) // 4
+    return torch.zeros(max(n, 1), dtype=torch.int32, device=device if device is not None else "cuda")
+
+
+def w4a16_linear_chain(ops, scratch, group: int = 128, stream=None, count=None):
+    """The M = 1 INT4 linears `ops` = [(x, qw, s, z, y), ...] (or an array
+    from w4a16_linear_array with `count` ops) in one persistent launch,
+    computing what w4a16_linear_sequence computes.  `scratch`: a zeroed
+    device tensor of at least w4a16_linear_chain_scratch_bytes(count)
+    bytes (see chain_scratch), left zeroed by every call."""
+    if isinstance(ops, ctypes.Array):
+        if ops._type_ is not w4a16_linear:
+            raise TypeError("ops must be an array of w4a16_linear")
+        arr, n = ops, len(ops) if count is None else int(count)
+        if not 0 <= n <= len(ops):
+            raise ValueError("count %d outside 0..%d (the array's length)" % (n, len(ops)))
+        dev = scratch.device
+    else:
+        arr, n = w4a16_linear_array(ops, group), len(ops)
+        dev = ops[0][1].device if ops else scratch.device
+    if not isinstance(scratch, torch.Tensor) or not scratch.is_cuda or scratch.device != dev:
+        raise ValueError("scratch must be a CUDA tensor on %s" % dev)
+    if not scratch.is_contiguous():
+        raise ValueError("scratch must be contiguous")
+    nbytes = scratch.numel() * scratch.element_size()
+    with torch.cuda.device(dev):  # the library launches on the current device
+        _check(lib().w4a16_linear_chain(arr, n, group, ctypes.c_void_p(scratch.data_ptr()), nbytes,
+                                        _stream(stream, dev)))
 
 
 class W4A16Graph:

@@ -142,23 +142,27 @@ int check_gemm_args(const char *who, const void *X, const void *qw, const void *
 }
 
 // Decode-sized batches stream the weights on the CUDA cores: M = 1 the GEMV,
-// M <= 4 rows sharing one pass, 5 <= M <= 8 two passes (four rows, then the
-// rest).  Larger M goes to the tensor cores, whose GEMM has a fixed pipeline
-// latency that dominates at small M (measured at N = 15360, K = 3840, GEMM
-// against two passes: M = 5 28.7 / 22.3 us, M = 6 31.5 / 24.6 us, M = 8
-// 30.8 / 29.6 us, M = 12 30.7 / 44.3 us).
+// up to four rows sharing one pass (fewer where K leaves fewer teams per
+// CTA), M <= 8 in passes of that many rows.  Larger M goes to the tensor
+// cores, whose GEMM has a fixed pipeline latency that dominates at small M
+// (measured at N = 15360, K = 3840, GEMM against two passes: M = 5 28.7 /
+// 22.3 us, M = 6 31.5 / 24.6 us, M = 8 30.8 / 29.6 us, M = 12 30.7 / 44.3 us).
 cudaError_t launch_int4_linear(const uint16_t *X, const uint8_t *qw, const uint16_t *s, const uint16_t *z,
                                uint16_t *Y, int64_t M, int64_t N, int64_t K, cudaStream_t st, unsigned int *status,
                                const w4::DeviceInfo &dev) {
-    if (M == 1) return w4::launch_gemv_int4(X, qw, s, z, Y, N, K, st, status, dev);
-    if (M <= 4) return w4::launch_gemv_int4_batched(X, qw, s, z, Y, M, N, K, st, status, dev);
-    if (M <= 8) {
-        const cudaError_t e = w4::launch_gemv_int4_batched(X, qw, s, z, Y, 4, N, K, st, status, dev);
+    if (M > 8) return w4::launch_gemm_int4(X, qw, s, z, Y, M, N, K, st, status, dev);
+    const int64_t mv_max = w4::gemv_int4_max_mv(K) >= 4 ? 4 : 2;
+    while (M > 0) {
+        const int64_t mv = M >= mv_max ? mv_max : M >= 2 ? 2 : 1;
+        const cudaError_t e = mv == 1 ? w4::launch_gemv_int4(X, qw, s, z, Y, N, K, st, status, dev)
+                                      : w4::launch_gemv_int4_batched(X, qw, s, z, Y, mv, N, K, st, status, dev);
         if (e != cudaSuccess) return e;
-        // rows 4 .. M-1: X + 4K and Y + 4N stay 16-byte aligned (K % 128 == 0, N % 16 == 0)
-        return launch_int4_linear(X + 4 * K, qw, s, z, Y + 4 * N, M - 4, N, K, st, status, dev);
+        // the next rows: X + mv K and Y + mv N stay 16-byte aligned (K % 128 == 0, N % 16 == 0)
+        X += mv * K;
+        Y += mv * N;
+        M -= mv;
     }
-    return w4::launch_gemm_int4(X, qw, s, z, Y, M, N, K, st, status, dev);
+    return cudaSuccess;
 }
 
 // The checks of op i of a sequence (M = 1: the GEMV's rules).
@@ -199,6 +203,87 @@ cudaError_t launch_sequence(const w4a16_linear *ops, int count, cudaStream_t st,
         }
     }
     failed_at = -1;
+    return cudaSuccess;
+}
+
+struct Range {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+Range range_of(const void *p, int64_t bytes) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    return {a, p ? a + static_cast<uintptr_t>(bytes) : a};
+}
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+
+// Checks a chain of M = 1 linears and fills the kernel's op table: for each
+// op the last earlier op it conflicts with (it reads what that op writes,
+// or writes what that op reads or writes), -1 for none.  Refused: an op
+// whose output overlaps its own input, outputs that overlap any op's
+// weights (weights are streamed ahead of the ops' order) or the scratch.
+int plan_chain(const w4a16_linear *ops, int count, Range scratch, w4::ChainOp *plan) {
+    for (int i = 0; i < count; ++i) {
+        const w4a16_linear &o = ops[i];
+        if (o.M != 1)
+            return fail(W4A16_ERR_UNSUPPORTED, "w4a16_linear_chain: op %d has M=%lld (a chain takes M = 1 ops)", i,
+                        (long long)o.M);
+        if (o.N > 0x7FFFFFFF)
+            return fail(W4A16_ERR_UNSUPPORTED, "w4a16_linear_chain: op %d N=%lld too large", i, (long long)o.N);
+        const Range xi = range_of(o.x, 2 * o.K), yi = range_of(o.y, 2 * o.N);
+        if (overlap(xi, yi)) return fail(W4A16_ERR_INVALID_ARG, "w4a16_linear_chain: op %d writes its own input", i);
+        if (overlap(yi, scratch)) return fail(W4A16_ERR_INVALID_ARG, "w4a16_linear_chain: op %d writes the scratch", i);
+        for (int j = 0; j < count; ++j) {
+            const w4a16_linear &w = ops[j];
+            const int64_t Gj = w.K / 128;
+            if (overlap(yi, range_of(w.qw, w.N * w.K / 2)) || overlap(yi, range_of(w.s, 2 * w.N * Gj)) ||
+                (w.z && overlap(yi, range_of(w.z, 2 * w.N * Gj))))
+                return fail(W4A16_ERR_INVALID_ARG, "w4a16_linear_chain: op %d writes the weights of op %d", i, j);
+        }
+        w4::ChainOp &c = plan[i];
+        c.x = o.x;
+        c.qw = o.qw;
+        c.s = o.s;
+        c.z = o.z;
+        c.y = o.y;
+        c.N = static_cast<int>(o.N);
+        c.K = static_cast<int>(o.K);
+        w4::gemv_chain_shape(o.K, c.tt_log2, c.rpt);
+        c.dep = -1;
+        for (int j = i - 1; j >= 0; --j) {
+            const Range xj = range_of(ops[j].x, 2 * ops[j].K), yj = range_of(ops[j].y, 2 * ops[j].N);
+            if (overlap(yj, xi) || overlap(xj, yi) || overlap(yj, yi)) {
+                c.dep = j;
+                break;
+            }
+        }
+    }
+    return W4A16_OK;
+}
+
+int64_t chain_scratch_bytes(int count) {
+    if (count < 1) return 0;
+    const int64_t launches = (count + w4::kChainMaxOps - 1) / w4::kChainMaxOps;
+    return 4 * (static_cast<int64_t>(count) + launches);
+}
+
+// Launches a planned chain in pieces of at most kChainMaxOps ops, each with
+// its own counters in the scratch; a dependency on an op of an earlier piece
+// is met by the stream order.
+cudaError_t launch_chain(w4::ChainOp *plan, int count, unsigned int *scratch, cudaStream_t st, unsigned int *status,
+                         const w4::DeviceInfo &dev) {
+    unsigned int *done = scratch;
+    for (int c0 = 0; c0 < count; c0 += w4::kChainMaxOps) {
+        const int n = count - c0 < w4::kChainMaxOps ? count - c0 : w4::kChainMaxOps;
+        w4::ChainOp *piece = plan + c0;
+        for (int i = 0; i < n; ++i) {
+            piece[i].dep = piece[i].dep >= c0 ? piece[i].dep - c0 : -1;
+            piece[i].report = 0;
+        }
+        for (int i = 0; i < n; ++i)
+            if (piece[i].dep >= 0) piece[piece[i].dep].report = 1;
+        const cudaError_t e = w4::launch_gemv_chain(piece, n, done, st, status, dev);
+        if (e != cudaSuccess) return e;
+        done += n + 1;
+    }
     return cudaSuccess;
 }
 
@@ -301,6 +386,36 @@ int w4a16_dequant(int fmt, const uint8_t *qw, const uint16_t *s,
     return launched(w4::launch_dequant(fmt, qw, s, z, out, out_dtype, rows, K, group,
                                        static_cast<cudaStream_t>(stream), dev),
                     "w4a16_dequant");
+}
+
+int64_t w4a16_linear_chain_scratch_bytes(int count) { return chain_scratch_bytes(count); }
+
+int w4a16_linear_chain(const w4a16_linear *ops, int count, int group, void *scratch, int64_t scratch_bytes,
+                       void *stream) {
+    if (int r = check_sequence(ops, count, group, "w4a16_linear_chain")) return r;
+    if (count == 0) return ok();
+    if (!scratch) return fail(W4A16_ERR_INVALID_ARG, "w4a16_linear_chain: null scratch");
+    if ((reinterpret_cast<uintptr_t>(scratch) & 3u) != 0)
+        return fail(W4A16_ERR_MISALIGNED, "w4a16_linear_chain: scratch must be 4-byte aligned");
+    const int64_t need = chain_scratch_bytes(count);
+    if (scratch_bytes < need)
+        return fail(W4A16_ERR_INVALID_ARG, "w4a16_linear_chain: scratch of %lld bytes, %lld needed",
+                    (long long)scratch_bytes, (long long)need);
+    w4::ChainOp *plan = new (std::nothrow) w4::ChainOp[count];
+    if (!plan) return fail(W4A16_ERR_CUDA, "w4a16_linear_chain: out of host memory");
+    int r = plan_chain(ops, count, range_of(scratch, need), plan);
+    w4::DeviceInfo dev;
+    unsigned int *status = nullptr;
+    if (!r) r = device_state(dev, status);
+    if (!r) r = check_sequence_ptrs(ops, count, dev.device, "w4a16_linear_chain");
+    if (!r) r = check_device_ptrs("w4a16_linear_chain: scratch", dev.device, {scratch});
+    if (!r) {
+        const cudaError_t e = launch_chain(plan, count, static_cast<unsigned int *>(scratch),
+                                           static_cast<cudaStream_t>(stream), status, dev);
+        r = launched(e, "w4a16_linear_chain");
+    }
+    delete[] plan;
+    return r;
 }
 
 int w4a16_linear_sequence(const w4a16_linear *ops, int count, int group, void *stream) {

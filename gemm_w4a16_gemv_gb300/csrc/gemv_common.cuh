@@ -3,17 +3,31 @@
 // multi-row warp reduction.
 //
 // Arithmetic budget.  A GEMV streaming at HBM speed on 152 SMs must retire
-// about 40 weight codes per SM clock.  Measured on sm_103a (codes per SM
-// clock, instruction stream alone): the binary16 route -- two codes per
-// logic op via the exponent-bias OR, then the mixed-precision
-// fma.rn.f32.f16 -- sustains about 43; the integer route -- even codes as
-// bytes c, odd codes as bytes 16c (one logic op each for four codes), then
-// dp2a against 16-bit activations -- about 87.  INT4 therefore takes the
-// integer route: activations become signed 16-bit integers with one
-// power-of-two scale per 128-element group (exact for the group's top eight
-// binades, rounded by at most 2^-15 of the group maximum below that), every
-// product and sum of a group is exact in 32-bit integers, and the scale, zero
-// point and activation scale are applied once per (row, group) in binary32.
+// about 50 weight codes per SM clock.  Measured on sm_103a: the integer dot
+// product instructions (dp2a / dp4a) issue at roughly 32 per SM clock, so
+// the integer route -- even codes as bytes c, odd codes as bytes 16c (one
+// logic op each for four codes), then dp2a against 16-bit activations, four
+// dp2a per eight codes -- keeps up with HBM (64 codes per clock), while every
+// further dot-product instruction per eight codes costs about an eighth of
+// the rate (a second, 8-bit activation part measured 14% slower on the
+// 262144 x 3840 GEMV).  The binary16 route (exponent-bias OR, then the mixed
+// fma.rn.f32.f16) sustains about 43 codes per clock.
+//
+// INT4 therefore takes the integer route with one 16-bit integer per
+// activation against a power-of-two scale per 128-element group, chosen so
+// that a wide range inside a group costs no precision where it matters.  With
+// e1 and e3 the exponents of the group's largest and third-largest |x|: if
+// e3 >= e1 - 1, e = e1; else e = e3 and the values at or above 2^(e3+1) (the
+// largest one or two) are set aside:
+//   x = hi * 2^(e-14),  hi = rint(x * 2^(14-e)) in int16     (every other value)
+// Values in [2^(e-7), 2^(e+1)) are exact -- so every value at most six binades
+// below the third largest's binade -- smaller ones are rounded to a multiple
+// of 2^(e-14); the set-aside values ("outliers") enter exactly, as
+// binary32 products s * (q - z) * x added per (row, group).  So a group whose
+// largest value is 2^14 times the rest keeps the rest at the precision of a
+// group without it.  Every product and sum of the integer part is exact in
+// 32-bit integers; scale, zero point and activation scale are applied once
+// per (row, group) in binary32.
 // FP4 codes are not integers (E2M1); they decode exactly to binary16 pairs
 // (cvt.rn.f16x2.e2m1x2) and meet binary16 activations, scaled exactly by a
 // power of two per 32-element unit, in the mixed-precision FMA.
@@ -75,13 +89,14 @@ __device__ __forceinline__ int unit_exponent(const uint32_t (&xb)[16]) {
 __device__ __forceinline__ float pow2f(int e) { return __uint_as_float(static_cast<uint32_t>(e + 127) << 23); }
 
 // Load 32 BF16 activations (64 bytes, 16-byte aligned, global memory) as 16
-// words of packed pairs: xb[i] = {x[2i], x[2i+1]}.  A plain (coherent) load:
-// the activation may have been written by the previous kernel of the stream.
+// words of packed pairs: xb[i] = {x[2i], x[2i+1]}.  Cached in L2 only: the
+// activation may have been written by the previous kernel of the stream or,
+// in a chain of linears, by another CTA of the same launch.
 __device__ __forceinline__ void load_x_unit(const uint16_t *x, uint32_t (&xb)[16]) {
     const uint4 *p = reinterpret_cast<const uint4 *>(x);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        const uint4 v = p[q];
+        const uint4 v = __ldcg(p + q);
         xb[4 * q + 0] = v.x;
         xb[4 * q + 1] = v.y;
         xb[4 * q + 2] = v.z;
@@ -119,31 +134,91 @@ __device__ __forceinline__ uint32_t pack_i16x2(int lo, int hi) {
     return (static_cast<uint32_t>(lo) & 0xFFFFu) | (static_cast<uint32_t>(hi) << 16);
 }
 
-// INT4 activation unit: 32 BF16 values (as 16 words of pairs) -> 16 words of
-// signed 16-bit pairs, x_int = rint(x * 2^(14-e)), in the order the integer
-// dot products meet them: for word m of a packed unit (codes 8m..8m+7; its
-// bytes hold codes (8m+2i, 8m+2i+1)), the even codes come as bytes
-// (c0, c2, c4, c6) and the odd ones as (16 c1, 16 c3, 16 c5, 16 c7), so the
-// pairs are (x0, x2), (x4, x6), (x1, x3), (x5, x7).  e is the exponent of the
-// largest |x| of the whole 128-element group, whose top binade therefore maps
-// exactly into [2^14, 2^15) (|x_int| <= 32640); only values below 2^(e-7)
-// are rounded, by at most 2^-15 of the group's maximum.  Returns sum x_int.
-__device__ __forceinline__ int int4_x_unit(const uint32_t (&xb)[16], int e, uint32_t (&xr)[16]) {
+// The three largest |x| (BF16 magnitude bit patterns) of a set, with the
+// position and the signed bits of the first two; ties keep the earlier.
+struct Top3 {
+    uint32_t a1, a2, a3;  // magnitudes, a1 >= a2 >= a3
+    uint32_t p1, p2;      // positions of a1, a2
+    uint32_t v1, v2;      // their signed BF16 bits
+};
+
+__device__ __forceinline__ void top3_insert(Top3 &t, uint32_t bits, uint32_t pos) {
+    const uint32_t m = bits & 0x7FFFu;
+    const bool c1 = m > t.a1, c2 = m > t.a2, c3 = m > t.a3;
+    t.a3 = c2 ? t.a2 : (c3 ? m : t.a3);
+    t.a2 = c1 ? t.a1 : (c2 ? m : t.a2);
+    t.p2 = c1 ? t.p1 : (c2 ? pos : t.p2);
+    t.v2 = c1 ? t.v1 : (c2 ? bits : t.v2);
+    t.a1 = c1 ? m : t.a1;
+    t.p1 = c1 ? pos : t.p1;
+    t.v1 = c1 ? bits : t.v1;
+}
+
+// Top3 of the union of two sets, A listed before B (ties keep A's).
+__device__ __forceinline__ Top3 top3_merge(const Top3 &A, const Top3 &B) {
+    Top3 t = A;
+    top3_insert(t, B.v1, B.p1);
+    top3_insert(t, B.v2, B.p2);
+    t.a3 = max(t.a3, min(B.a3, t.a2));  // B's third value can only end up third
+    return t;
+}
+
+// Top3 over the 128 values of a group held by L = 16 / W neighbouring lanes
+// (8 W each, positions 8 W (lane mod L) + i); every lane of the L gets the
+// same result.  All 32 lanes of the warp call it together.
+template <int W>
+__device__ __forceinline__ Top3 group_top3(const uint32_t (&xb)[4 * W], int lane) {
+    constexpr int L = 16 / W;
+    Top3 t = {0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    const uint32_t base = 8u * W * static_cast<uint32_t>(lane & (L - 1));
+#pragma unroll
+    for (int k = 0; k < 8 * W; ++k) top3_insert(t, (k & 1) ? xb[k >> 1] >> 16 : xb[k >> 1] & 0xFFFFu, base + k);
+#pragma unroll
+    for (int d = 1; d < L; d <<= 1) {
+        Top3 o;
+        o.a1 = __shfl_xor_sync(0xffffffffu, t.a1, d);
+        o.a2 = __shfl_xor_sync(0xffffffffu, t.a2, d);
+        o.a3 = __shfl_xor_sync(0xffffffffu, t.a3, d);
+        o.p1 = __shfl_xor_sync(0xffffffffu, t.p1, d);
+        o.p2 = __shfl_xor_sync(0xffffffffu, t.p2, d);
+        o.v1 = __shfl_xor_sync(0xffffffffu, t.v1, d);
+        o.v2 = __shfl_xor_sync(0xffffffffu, t.v2, d);
+        t = (lane & d) ? top3_merge(o, t) : top3_merge(t, o);  // the lower positions first on both lanes
+    }
+    return t;
+}
+
+// Number of the 2N values (N words of pairs) whose magnitude bit pattern is
+// >= thr.
+template <int N>
+__device__ __forceinline__ int count_at_least(const uint32_t (&xb)[N], uint32_t thr) {
+    int c = 0;
+#pragma unroll
+    for (int i = 0; i < N; ++i) c += ((xb[i] & 0x7FFFu) >= thr) + (((xb[i] >> 16) & 0x7FFFu) >= thr);
+    return c;
+}
+
+// INT4 activation word: 8 BF16 values (4 words of pairs, codes k..k+7 of a
+// packed word, whose bytes hold codes (k+2i, k+2i+1)), group exponent e and a
+// mask of set-aside values -> 4 words of signed 16-bit pairs hi = rint(x *
+// 2^(14-e)) (0 where masked) in the order the integer dot products meet
+// them: the even codes come as bytes (c0, c2, c4, c6) and the odd ones as
+// (16 c1, 16 c3, 16 c5, 16 c7), so the pairs are (x0, x2), (x4, x6), (x1, x3),
+// (x5, x7).  |hi| <= 32640.  Returns the sum of the 8 hi.
+__device__ __forceinline__ int int4_x_word(const uint32_t *xb, int e, uint32_t skip, uint32_t (&xr)[4]) {
     const float inv = pow2f(14 - e);
+    int v[8];
     int sum = 0;
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        int v[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            v[q] = rint_scaled(bf16_elem(xb, 8 * m + q), inv);  // x * inv is exact
-            sum += v[q];
-        }
-        xr[4 * m + 0] = pack_i16x2(v[0], v[2]);
-        xr[4 * m + 1] = pack_i16x2(v[4], v[6]);
-        xr[4 * m + 2] = pack_i16x2(v[1], v[3]);
-        xr[4 * m + 3] = pack_i16x2(v[5], v[7]);
+    for (int q = 0; q < 8; ++q) {
+        const float x = bf16_bits_to_f32((q & 1) ? xb[q >> 1] >> 16 : xb[q >> 1] & 0xFFFFu);
+        v[q] = (skip >> q) & 1u ? 0 : rint_scaled(x, inv);  // x * inv is exact
+        sum += v[q];
     }
+    xr[0] = pack_i16x2(v[0], v[2]);
+    xr[1] = pack_i16x2(v[4], v[6]);
+    xr[2] = pack_i16x2(v[1], v[3]);
+    xr[3] = pack_i16x2(v[5], v[7]);
     return sum;
 }
 

@@ -32,6 +32,8 @@ cudaError_t launch_gemv_int4(const uint16_t *x, const uint8_t *qw, const uint16_
              : gemv_dispatch<false, true>(a, st, dev.device, dev.num_sms, dev.max_smem_optin);
 }
 
+int gemv_int4_max_mv(int64_t K) { return gemv_int4_teams(K); }
+
 // Batched decode: M = 2..4 activation rows X [M, K] against one pass over the
 // weights (the rows share every weight stage), Y [M, N].
 cudaError_t launch_gemv_int4_batched(const uint16_t *X, const uint8_t *qw, const uint16_t *s, const uint16_t *z,

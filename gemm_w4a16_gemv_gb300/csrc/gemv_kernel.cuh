@@ -19,10 +19,11 @@
 // are bitwise reproducible) and writes the BF16 outputs.
 //
 // Warps 0..CW-1 consume.  They convert the activation once per CTA into
-// shared memory (INT4: signed 16-bit integers with a power-of-two scale per
-// 128-element group, for exact DP2A integer dot products; FP4: binary16
-// pairs with a scale per 32-element unit, for the mixed-precision FMA), then
-// keep the part each thread owns in registers and work through the stages.
+// shared memory (INT4: a 16-bit and an 8-bit integer part per value against a
+// power-of-two scale per 128-element group, for exact dp2a / dp4a integer dot
+// products; FP4: binary16 pairs with a scale per 32-element unit, for the
+// mixed-precision FMA), then keep the part each thread owns in registers and
+// work through the stages.
 // All waits are bounded.
 #pragma once
 
@@ -250,25 +251,28 @@ __device__ __forceinline__ void gemv_prefetch_groups(const GemvParams &a, int64_
     if (!SYM) gemv_prefetch_range(a.z, g0, g1, tid, nthreads);
 }
 
-// Activation conversion, once per CTA, one 32-element unit per consumer
-// thread (U = K/32 units; INT4 has U % 4 == 0).  Shared-memory layout at xs, as uint4 "planes" laid
-// out so that the threads' later register loads are free of bank conflicts:
-//  INT4: plane p = 4s + i (s: unit within the 128-element group, i: quarter
-//        of the unit's 16 words) holds Gp = G rounded up to even entries, one
-//        per group; per group a float2 (xsum, pw) follows at xs + 64U + 256.
-//        Four neighbouring lanes (the group's units; K % 128 == 0 keeps every
-//        group whole) agree on the group exponent through shuffles.
-//  FP4:  plane i holds U entries, one per unit; per unit a float2 (0, pw).
-__device__ __forceinline__ int gemv_x_gp(int G) { return (G + 1) & ~1; }
+// Activation conversion, once per CTA, into shared memory at xs, laid out as
+// uint4 "planes" so that the threads' later register loads are free of bank
+// conflicts.
+//  INT4: one 8-value word per thread (K/8 words; the 16 words of a group are
+//        16 neighbouring lanes, K % 128 == 0 keeps every group whole).
+//        Plane p = 4s + i (s: 32-value unit within the group, i: word within
+//        the unit) holds Gp = G rounded up to even entries, one per group;
+//        plane 16 holds per group (sum of hi, set-aside list, x of the first
+//        and of the second set-aside value), the list packing their
+//        positions in the group (bits 0-6, 8-14), their count (bits 16-17)
+//        and e + 128 (bits 24-31).
+//  FP4:  one 32-value unit per thread; plane i holds U = K/32 entries, one
+//        per unit; per unit a float2 (0, pw) at xs + 64U + 256.
 __device__ __forceinline__ int gemv_x_consts(int K) { return (K >> 5) * 64 + 256; }
+__device__ __host__ __forceinline__ int gemv_x_gp(int K) { return ((K >> 7) + 1) & ~1; }
+__device__ __host__ __forceinline__ int gemv_int4_x_bytes(int K) { return 17 * 16 * gemv_x_gp(K); }
 
-// One 32-element unit u of activation x into the planes at xs (the layout
-// described above): the batched conversion's body.
-template <bool FP4>
-__device__ __forceinline__ void gemv_convert_unit(const GemvParams &a, const uint16_t *x, unsigned char *xs, int u,
-                                                  bool ok, int units, int gp) {
+// FP4: one 32-value unit u of activation x into the planes at xs; `ok`
+// false: a padding lane, which stores nothing.
+__device__ __forceinline__ void gemv_convert_fp4_unit(const uint16_t *x, unsigned char *xs, int u, bool ok,
+                                                      int units) {
     uint4 *xw = reinterpret_cast<uint4 *>(xs);
-    float2 *xc = reinterpret_cast<float2 *>(xs + gemv_x_consts(a.K));
     uint32_t xb[16], w[16];
     if (ok) {
         load_x_unit(x + 32 * u, xb);
@@ -276,97 +280,232 @@ __device__ __forceinline__ void gemv_convert_unit(const GemvParams &a, const uin
 #pragma unroll
         for (int i = 0; i < 16; ++i) xb[i] = 0u;
     }
-    float2 c;
-    if constexpr (FP4) {
-        c = make_float2(0.0f, fp4_x_unit(xb, w));
-    } else {
-        uint32_t m = unit_absmax_bits(xb);
-        m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-        const int e = exponent_of_absmax(m);
-        int sum = int4_x_unit(xb, e, w);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-        c = make_float2(static_cast<float>(sum), pow2f(e - 14));  // |sum| < 2^23: exact
-    }
+    const float2 c = make_float2(0.0f, fp4_x_unit(xb, w));
     if (ok) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint4 q4 = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-            if (FP4) xw[i * units + u] = q4;
-            else xw[(4 * (u & 3) + i) * gp + (u >> 2)] = q4;
-        }
-        if (FP4) xc[u] = c;
-        else if ((u & 3) == 0) xc[u >> 2] = c;
+        for (int i = 0; i < 4; ++i) xw[i * units + u] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        reinterpret_cast<float2 *>(xs + gemv_x_consts(units * 32))[u] = c;
     }
 }
 
-template <bool FP4, int CW>
-__device__ __forceinline__ void gemv_convert_x(const GemvParams &a, const uint16_t *x, unsigned char *xs, int warp,
-                                               int lane) {
+// INT4: W consecutive 8-value words (their BF16 bits v, zero on padding
+// lanes), starting at word w of an activation of K values, into the planes
+// at xs (the layout above).  The 16 / W lanes of a group are neighbours; all
+// 32 lanes of the warp call it together (the group shuffles); `ok` false: a
+// padding lane (of a whole padding group), which stores nothing.
+template <int W>
+__device__ __forceinline__ void gemv_convert_int4_words(const uint32_t (&xb)[4 * W], unsigned char *xs, int w, bool ok,
+                                                        int K) {
+    constexpr int L = 16 / W;  // lanes of a group
     uint4 *xw = reinterpret_cast<uint4 *>(xs);
-    const int units = a.K >> 5;
-    const int gp = gemv_x_gp(a.G);
-    float2 *xc = reinterpret_cast<float2 *>(xs + gemv_x_consts(a.K));
-    // Every CTA reads the same few KB at the same moment; starting each CTA at
-    // a different group (a rotation by whole groups, so that the four lanes
-    // of a group stay together) spreads the requests over the L2 slices.
-    const int rot = FP4 ? static_cast<int>((blockIdx.x * 7u) % static_cast<unsigned>(units))
-                        : 4 * static_cast<int>((blockIdx.x * 7u) % static_cast<unsigned>(units >> 2));
-    for (int u0 = warp * 32; u0 < units; u0 += CW * 32) {  // warp-uniform
-        const bool ok = u0 + lane < units;
-        int u = u0 + lane + rot;
-        if (u >= units) u -= units;
-        uint32_t xb[16], w[16];
-        if (ok) {
-            load_x_unit(x + 32 * u, xb);
-        } else {
+    const int lane = threadIdx.x & 31;
+    // the group's largest |x| (exponent e1) and how many values have an
+    // exponent of at least e1 - 1
+    uint32_t m2 = 0;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) xb[i] = 0u;
-        }
-        float2 c;
-        if constexpr (FP4) {
-            c = make_float2(0.0f, fp4_x_unit(xb, w));
-        } else {
-            uint32_t m = unit_absmax_bits(xb);
-            m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-            m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-            const int e = exponent_of_absmax(m);
-            int sum = int4_x_unit(xb, e, w);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-            c = make_float2(static_cast<float>(sum), pow2f(e - 14));  // |sum| < 2^23: exact
-        }
-        if (ok) {
+    for (int i = 0; i < 4 * W; ++i) m2 = __vmaxu2(m2, xb[i] & 0x7FFF7FFFu);
+    uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint4 q4 = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-                if (FP4) xw[i * units + u] = q4;
-                else xw[(4 * (u & 3) + i) * gp + (u >> 2)] = q4;
-            }
-            if (FP4) xc[u] = c;
-            else if ((u & 3) == 0) xc[u >> 2] = c;
+    for (int d = 1; d < L; d <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, d));
+    int e = exponent_of_absmax(m);
+    int c = (m & 0x7F80u) > 0x0080u ? count_at_least<4 * W>(xb, (m & 0x7F80u) - 0x0080u) : 3;
+#pragma unroll
+    for (int d = 1; d < L; d <<= 1) c += __shfl_xor_sync(0xffffffffu, c, d);
+    Top3 t = {0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    bool o1 = false, o2 = false;
+    // the third largest more than one binade below the largest: the largest
+    // one or two may lie above the third largest's binade (warp-uniform
+    // branch: the group search shuffles)
+    if (__any_sync(0xffffffffu, c < 3)) {
+        t = group_top3<W>(xb, lane);
+        if (c < 3) {
+            const bool few = t.a3 == 0u;  // at most two nonzero values: set them aside
+            e = few ? 0 : exponent_of_absmax(t.a3);
+            const uint32_t thr = static_cast<uint32_t>(e + 128) << 7;  // magnitude bits of 2^(e+1)
+            o1 = t.a1 != 0u && (few || t.a1 >= thr);
+            o2 = t.a2 != 0u && (few || t.a2 >= thr);  // implies o1
         }
+    }
+    const int gp = gemv_x_gp(K), grp = w >> 4;
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
+        const uint32_t j = static_cast<uint32_t>((w + i) & 15);  // word within the group
+        uint32_t skip = 0u;
+        if (o1 && (t.p1 >> 3) == j) skip |= 1u << (t.p1 & 7u);
+        if (o2 && (t.p2 >> 3) == j) skip |= 1u << (t.p2 & 7u);
+        uint32_t wr[4];
+        sum += int4_x_word(xb + 4 * i, e, skip, wr);
+        if (ok) xw[(4 * (j >> 2) + (j & 3)) * gp + grp] = make_uint4(wr[0], wr[1], wr[2], wr[3]);
+    }
+#pragma unroll
+    for (int d = 1; d < L; d <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, d);
+    if (ok && (w & 15) == 0) {
+        const uint32_t n = (o1 ? 1u : 0u) + (o2 ? 1u : 0u);
+        const uint32_t list = (o1 ? t.p1 : 0u) | ((o2 ? t.p2 : 0u) << 8) | (n << 16) |
+                              (static_cast<uint32_t>(e + 128) << 24);
+        // |sum| <= 128 * 32640 < 2^23: exact in binary32
+        xw[16 * gp + grp] = make_uint4(__float_as_uint(static_cast<float>(sum)), list,
+                                       __float_as_uint(bf16_bits_to_f32(t.v1)), __float_as_uint(bf16_bits_to_f32(t.v2)));
     }
 }
 
-// Batched INT4 (MV > 1): the MV vectors (x0 + v K, padding vectors repeating
-// the last given one) converted in one pass over MV * U units, vector v into
-// its region xs0 + v * x_stride; K % 128 == 0 keeps each group's four lanes
-// within one vector.
-template <int CW, int MV>
-__device__ __forceinline__ void gemv_convert_x_batched(const GemvParams &a, const uint16_t *x0, unsigned char *xs0,
-                                                       int warp, int lane) {
-    const int units = a.K >> 5;
-    const int gp = gemv_x_gp(a.G);
-    const int rot = 4 * static_cast<int>((blockIdx.x * 7u) % static_cast<unsigned>(units >> 2));
-    for (int u0 = warp * 32; u0 < MV * units; u0 += CW * 32) {  // warp-uniform
-        const bool ok = u0 + lane < MV * units;
-        const int v = ok ? (u0 + lane) / units : 0;
-        int u = u0 + lane - v * units + rot;
-        if (u >= units) u -= units;
-        gemv_convert_unit<false>(a, x0 + static_cast<int64_t>(min(v, a.mv_valid - 1)) * a.K, xs0 + v * a.x_stride,
-                                 u, ok, units, gp);
+// INT4 activation of K values with W words per thread (one round of the
+// warps covers K <= 4 * 8 * 32 * nwarps, the most W = 4 allows).
+template <int W>
+__device__ __forceinline__ void gemv_convert_int4(const uint16_t *x, unsigned char *xs, int K, int warp, int nwarps,
+                                                  int lane) {
+    const int items = (K >> 3) / W;  // W words each; a group is 16 / W items
+    const int rot = (16 / W) * static_cast<int>((blockIdx.x * 7u) % static_cast<unsigned>(K >> 7));
+    const uint4 *x4 = reinterpret_cast<const uint4 *>(x);
+    for (int i0 = warp * 32; i0 < items; i0 += nwarps * 32) {  // warp-uniform
+        const bool ok = i0 + lane < items;                      // the lanes of a group share ok
+        int i = i0 + lane + rot;
+        if (i >= items) i -= items;
+        uint32_t v[4 * W];
+#pragma unroll
+        for (int q = 0; q < W; ++q) {
+            const uint4 u = ok ? __ldcg(x4 + i * W + q) : make_uint4(0u, 0u, 0u, 0u);  // L2 only, as load_x_unit
+            v[4 * q] = u.x;
+            v[4 * q + 1] = u.y;
+            v[4 * q + 2] = u.z;
+            v[4 * q + 3] = u.w;
+        }
+        gemv_convert_int4_words<W>(v, xs, i * W, ok, K);
+    }
+}
+
+// The whole activation x (K values) by consumer warps warp, warp + nwarps,
+// ...  Every CTA reads the same few KB at the same moment; starting each CTA
+// at a different group (a rotation by whole groups) spreads the requests
+// over the L2 slices.  INT4 takes 8, 16 or 32 values a thread as K grows, so
+// that one round of loads covers the activation.
+template <bool FP4>
+__device__ __forceinline__ void gemv_convert_vector(const uint16_t *x, unsigned char *xs, int K, int warp, int nwarps,
+                                                    int lane) {
+    if constexpr (FP4) {
+        const int units = K >> 5;
+        const int rot = static_cast<int>((blockIdx.x * 7u) % static_cast<unsigned>(units));
+        for (int u0 = warp * 32; u0 < units; u0 += nwarps * 32) {  // warp-uniform
+            const bool ok = u0 + lane < units;
+            int u = u0 + lane + rot;
+            if (u >= units) u -= units;
+            gemv_convert_fp4_unit(x, xs, u, ok, units);
+        }
+    } else {
+        const int words = K >> 3;
+        if (words <= nwarps * 32)
+            gemv_convert_int4<1>(x, xs, K, warp, nwarps, lane);
+        else if (words <= 2 * nwarps * 32)
+            gemv_convert_int4<2>(x, xs, K, warp, nwarps, lane);
+        else
+            gemv_convert_int4<4>(x, xs, K, warp, nwarps, lane);
+    }
+}
+
+// A consumer thread's INT4 activation: its group's 64 words of hi pairs (four
+// sub-units, in the thread's rotated order) and constants.
+struct Int4X {
+    uint32_t xh[4][16];
+    float sum, pw;
+    uint32_t list;           // set-aside positions and count (plane 16 layout)
+    const uint4 *consts;     // the group's plane-16 entry (the set-aside x, read when needed)
+};
+
+__device__ __forceinline__ void int4_load_x(const unsigned char *xs, int gp, int gs, int rot, bool valid, Int4X &r) {
+    const uint4 *xw = reinterpret_cast<const uint4 *>(xs);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int sub = (q + rot) & 3;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 v4 = xw[(4 * sub + i) * gp + gs];
+            r.xh[q][4 * i] = v4.x;
+            r.xh[q][4 * i + 1] = v4.y;
+            r.xh[q][4 * i + 2] = v4.z;
+            r.xh[q][4 * i + 3] = v4.w;
+        }
+    }
+    r.consts = xw + 16 * gp + gs;
+    const uint4 c = *r.consts;
+    r.sum = __uint_as_float(c.x);
+    r.list = valid ? c.y : 0u;
+    r.pw = valid ? pow2f(static_cast<int>(c.y >> 24) - 128 - 14) : 0.0f;
+}
+
+// One stage's work of a consumer thread: RPT rows (from rbase) of its group
+// g; codes at st + row * half_k + 64 g, the 16-byte sub-units taken in
+// rotated order; ss / sz: the stage's scale and zero rows (sz unused when
+// sym).  Adds each row's contribution to part[].
+template <int RPT>
+__device__ __forceinline__ void int4_group_rows(const Int4X &x, const unsigned char *st, int half_k, int rbase, int g,
+                                                int rot, const uint16_t *ss, const uint16_t *sz, bool sym, int G,
+                                                float (&part)[RPT]) {
+    int lo[RPT], hi[RPT];
+#pragma unroll
+    for (int rr = 0; rr < RPT; ++rr) lo[rr] = hi[rr] = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int sub = (q + rot) & 3;
+        uint4 wv[RPT];
+#pragma unroll
+        for (int rr = 0; rr < RPT; ++rr)
+            wv[rr] = *reinterpret_cast<const uint4 *>(st + static_cast<size_t>(rbase + rr) * half_k + 64 * g + 16 * sub);
+#pragma unroll
+        for (int rr = 0; rr < RPT; ++rr) {
+            const uint32_t words[4] = {wv[rr].x, wv[rr].y, wv[rr].z, wv[rr].w};
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                // even codes as bytes c (one logic op), odd codes as bytes
+                // 16c (one logic op, no shift)
+                const uint32_t ev = words[m] & 0x0F0F0F0Fu, od = words[m] & 0xF0F0F0F0u;
+                lo[rr] = dp2a_lo(x.xh[q][4 * m + 0], ev, lo[rr]);
+                lo[rr] = dp2a_hi(x.xh[q][4 * m + 1], ev, lo[rr]);
+                hi[rr] = dp2a_lo(x.xh[q][4 * m + 2], od, hi[rr]);
+                hi[rr] = dp2a_hi(x.xh[q][4 * m + 3], od, hi[rr]);
+            }
+        }
+    }
+    const uint32_t n = (x.list >> 16) & 3u;
+#pragma unroll
+    for (int rr = 0; rr < RPT; ++rr) {
+        // hi is a multiple of 16 (exact shift); |dot| < 2^26 (the conversion
+        // to binary32 rounds it by at most 2^-24 of itself)
+        const int dot = lo[rr] + (hi[rr] >> 4);
+        const int gi = (rbase + rr) * G + g;
+        const float sv = f16_bits_to_f32(ss[gi]);
+        const float zf = sym ? 8.0f : f16_bits_to_f32(sz[gi]);  // symmetric: the midpoint 8
+        float acc = (sv * x.pw) * fmaf(-zf, x.sum, static_cast<float>(dot));
+        if (n) {
+            // the set-aside values: s (q - z) x, each product exact in binary32
+            const unsigned char *row = st + static_cast<size_t>(rbase + rr) * half_k + 64 * g;
+            const uint4 c = *x.consts;  // (the activation region is not rewritten during the op)
+            const uint32_t p1 = x.list & 127u;
+            const float c1 = static_cast<float>((row[p1 >> 1] >> ((p1 & 1u) * 4u)) & 15u);
+            acc = fmaf(sv * (c1 - zf), __uint_as_float(c.z), acc);
+            if (n > 1) {
+                const uint32_t p2 = (x.list >> 8) & 127u;
+                const float c2 = static_cast<float>((row[p2 >> 1] >> ((p2 & 1u) * 4u)) & 15u);
+                acc = fmaf(sv * (c2 - zf), __uint_as_float(c.w), acc);
+            }
+        }
+        part[rr] += acc;
+    }
+}
+
+// The activation (MV == 1), or the MV activation vectors x0 + v K of a
+// batched pass (padding vectors, v >= a.mv_valid, repeat the last given one),
+// vector v into xs0 + v * x_stride.
+template <bool FP4, int CW, int MV>
+__device__ __forceinline__ void gemv_convert_x(const GemvParams &a, const uint16_t *x0, unsigned char *xs0, int warp,
+                                               int lane) {
+    if constexpr (MV == 1) {
+        gemv_convert_vector<FP4>(x0, xs0, a.K, warp, CW, lane);
+    } else {
+#pragma unroll 1
+        for (int v = 0; v < MV; ++v)
+            gemv_convert_vector<FP4>(x0 + static_cast<int64_t>(min(v, a.mv_valid - 1)) * a.K, xs0 + v * a.x_stride,
+                                     a.K, warp, CW, lane);
     }
 }
 
@@ -383,11 +522,11 @@ __device__ __forceinline__ void gemv_release_stage(GemvHeader<CW, RPT> &h, const
 
 // INT4 consumer.  A thread owns one 128-code group g of RPT rows per stage:
 // 64 bytes of packed codes per row, read as four 16-byte sub-units (u = 4g+s).
-// Lanes start at different sub-units (rotation by (j >> 1) & 3) so that the
+// Lanes start at different sub-units (rotation (g >> 1) & 3) so that the
 // eight lanes of each 128-byte shared-memory wavefront hit distinct banks;
 // the x registers are loaded in the same rotated order, so indexing stays
-// static.  Products are exact integer dot products (DP2A); per (row, group):
-//   y += s * 2^(e-14) * (dot - z * xsum).
+// static.  Products are exact integer dot products (dp2a); per (row, group):
+//   y += s * 2^(e-14) * (dot - z * sum_hi) + sum over set-aside x of s * (q - z) * x.
 template <int CW, int TT, int RPT, bool SYM, int MV>
 __device__ __forceinline__ void gemv_consume_int4(const GemvParams &a, GemvHeader<CW, RPT> &h,
                                                   const unsigned char *stage0, const unsigned char *xs0,
@@ -403,22 +542,8 @@ __device__ __forceinline__ void gemv_consume_int4(const GemvParams &a, GemvHeade
     const bool valid = g < a.G;
     const int gs = valid ? g : 0;
     const int rot = (g >> 1) & 3;
-    const uint4 *xw = reinterpret_cast<const uint4 *>(xs);
-    const int gp = gemv_x_gp(a.G);
-    uint32_t xr[4][16];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint4 v4 = xw[(4 * ((q + rot) & 3) + i) * gp + gs];
-            xr[q][4 * i] = v4.x;
-            xr[q][4 * i + 1] = v4.y;
-            xr[q][4 * i + 2] = v4.z;
-            xr[q][4 * i + 3] = v4.w;
-        }
-    }
-    const float2 xc = reinterpret_cast<const float2 *>(xs + gemv_x_consts(a.K))[gs];
-    const float xsum = xc.x, pw = valid ? xc.y : 0.0f;
+    Int4X x;
+    int4_load_x(xs, gemv_x_gp(a.K), gs, rot, valid, x);
     const int half_k = a.K >> 1;
 
     const int rbase = team * RPT;
@@ -433,42 +558,7 @@ __device__ __forceinline__ void gemv_consume_int4(const GemvParams &a, GemvHeade
         float part[RPT];
 #pragma unroll
         for (int rr = 0; rr < RPT; ++rr) part[rr] = 0.0f;
-        if (valid) {
-            int lo[RPT], hi[RPT];
-#pragma unroll
-            for (int rr = 0; rr < RPT; ++rr) lo[rr] = hi[rr] = 0;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int sub = (q + rot) & 3;
-                uint4 wv[RPT];
-#pragma unroll
-                for (int rr = 0; rr < RPT; ++rr)
-                    wv[rr] = *reinterpret_cast<const uint4 *>(st + static_cast<size_t>(rbase + rr) * half_k +
-                                                              64 * g + 16 * sub);
-#pragma unroll
-                for (int rr = 0; rr < RPT; ++rr) {
-                    const uint32_t words[4] = {wv[rr].x, wv[rr].y, wv[rr].z, wv[rr].w};
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        // even codes as bytes c (one logic op), odd codes as
-                        // bytes 16c (one logic op, no shift)
-                        const uint32_t ev = words[m] & 0x0F0F0F0Fu, od = words[m] & 0xF0F0F0F0u;
-                        lo[rr] = dp2a_lo(xr[q][4 * m + 0], ev, lo[rr]);
-                        lo[rr] = dp2a_hi(xr[q][4 * m + 1], ev, lo[rr]);
-                        hi[rr] = dp2a_lo(xr[q][4 * m + 2], od, hi[rr]);
-                        hi[rr] = dp2a_hi(xr[q][4 * m + 3], od, hi[rr]);
-                    }
-                }
-            }
-#pragma unroll
-            for (int rr = 0; rr < RPT; ++rr) {
-                const int dot = lo[rr] + (hi[rr] >> 4);  // hi is a multiple of 16; |dot| < 2^24
-                const int gi = (rbase + rr) * a.G + g;
-                const float sf = f16_bits_to_f32(ss[gi]) * pw;
-                const float zf = SYM ? 8.0f : f16_bits_to_f32(sz[gi]);  // symmetric: the midpoint 8
-                part[rr] = sf * fmaf(-zf, xsum, static_cast<float>(dot));
-            }
-        }
+        if (valid) int4_group_rows<RPT>(x, st, half_k, rbase, gs, rot, ss, sz, SYM, a.G, part);
         gemv_release_stage<CW, RPT>(h, part, slot, phase, warp, lane);
         v += rows;
         if (++slot == a.stages) {
@@ -604,10 +694,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_stream_kernel(const Gem
     // test-only injection: the consumers take no stage, so the producer's
     // waits for free stages run out with its copies issued
     if (a.inject & kInjectStallConsumers) return;
-    if constexpr (MV == 1)
-        gemv_convert_x<FP4, CW>(a, a.x, smem + a.x_off, warp, lane);
-    else
-        gemv_convert_x_batched<CW, MV>(a, a.x, smem + a.x_off, warp, lane);
+    gemv_convert_x<FP4, CW, MV>(a, a.x, smem + a.x_off, warp, lane);
     named_bar_sync(1, CW * 32);
     if constexpr (FP4)
         gemv_consume_fp4<CW, TT, UPT, RPT>(a, h, stage0, smem + a.x_off, begin, end, warp, lane);
@@ -646,6 +733,14 @@ inline GemvShape gemv_choose_shape(int CW, int UPR, int row_bytes, int stage_tar
 }
 
 constexpr int kGemvCW = 16;             // consumer warps per CTA
+
+// Teams of an INT4 CTA at this K: the activation vectors one pass carries
+// (MV) split the teams into one set per vector, so MV must divide this.
+inline int gemv_int4_teams(int64_t K) {
+    int tt = 32;
+    while (tt < K / 128) tt *= 2;
+    return kGemvCW * 32 / tt;
+}
 constexpr int kGemvStageTarget = 32768; // packed weight bytes per stage (upper aim)
 
 template <bool FP4, int TT, int UPT, int RPT, bool SYM, int MV = 1>
@@ -654,7 +749,9 @@ cudaError_t gemv_launch(GemvParams a, cudaStream_t st, int device, int num_sms, 
     auto kern = gemv_stream_kernel<FP4, CW, TT, UPT, RPT, SYM, MV>;
     const int header = (static_cast<int>(sizeof(GemvHeader<CW, RPT>)) + 127) & ~127;
     a.x_off = header;
-    a.x_stride = (a.K / 32) * 72 + 256;  // converted x: planes, then (xsum, pw); a multiple of 16
+    // converted x per vector (a multiple of 16): FP4 planes, then (0, pw) per
+    // unit; INT4 hi and lo planes, then the per-half-group constants
+    a.x_stride = FP4 ? (a.K / 32) * 72 + 256 : gemv_int4_x_bytes(a.K);
     a.stage_off = (a.x_off + MV * a.x_stride + 1023) & ~1023;
     int stages = (max_smem - a.stage_off) / a.stage_bytes;
     if (stages > kGemvMaxStages) stages = kGemvMaxStages;
@@ -686,9 +783,9 @@ cudaError_t gemv_launch(GemvParams a, cudaStream_t st, int device, int num_sms, 
 }
 
 // Fill the stage geometry of `a` for K and launch the matching instance.
-//  INT4: a thread owns one 128-code group: TT = the smallest warp multiple
-//        covering K/128 groups; RPT = 2 rows per thread while a stage stays
-//        within the stage target, else 1.
+//  INT4: a thread owns one 128-code group: TT = the smallest power-of-two
+//        warp multiple covering K/128 groups; RPT = 2 rows per thread while a
+//        stage stays within the stage target, else 1.
 //  FP4:  TT threads x UPT units of 32 codes cover a row (gemv_choose_shape).
 // SYM: symmetric INT4 (no zero points), its own kernel instances so that the
 // asymmetric ones carry no test for it.  MV > 1 (INT4): MV activation vectors
@@ -703,7 +800,7 @@ cudaError_t gemv_dispatch(GemvParams a, cudaStream_t st, int device, int num_sms
         a.UPR = a.K / 32;
         sh = gemv_choose_shape(kGemvCW, a.UPR, row_bytes, kGemvStageTarget);
     } else {
-        a.UPR = a.G;
+        a.UPR = a.G;  // groups per row, one per thread
         for (int tt = 32; tt <= 128 && sh.TT == 0; tt *= 2)
             if (tt >= a.G) sh = {tt, 1, 0};
         if (sh.TT != 0) {

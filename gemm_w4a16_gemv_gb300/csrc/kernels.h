@@ -50,11 +50,38 @@ cudaError_t launch_gemv_int4(const uint16_t *x, const uint8_t *qw,
                              int64_t N, int64_t K, cudaStream_t st,
                              unsigned int *status, const DeviceInfo &dev);
 
+// Activation rows one INT4 streaming pass can share at this K (2 or more).
+int gemv_int4_max_mv(int64_t K);
+
 // M = 2..4 rows through the streaming GEMV (one pass over the weights).
 cudaError_t launch_gemv_int4_batched(const uint16_t *X, const uint8_t *qw,
                                      const uint16_t *s, const uint16_t *z, uint16_t *Y,
                                      int64_t M, int64_t N, int64_t K, cudaStream_t st,
                                      unsigned int *status, const DeviceInfo &dev);
+
+// One INT4 linear of a chain (M = 1), as the chain kernel reads it.
+struct ChainOp {
+    const uint16_t *x;
+    const uint8_t *qw;
+    const uint16_t *s;
+    const uint16_t *z;  // null: symmetric INT4
+    uint16_t *y;
+    int N, K;
+    int dep;                // op of the same launch that must be finished everywhere first (-1: none)
+    unsigned char tt_log2;  // log2 of the threads per row (one thread per 128-code group)
+    unsigned char rpt;      // rows per thread per stage (1 or 2)
+    unsigned char report;   // a later op of the launch depends on this one: count its completion
+    unsigned char pad;
+};
+constexpr int kChainMaxOps = 192;  // ops per launch (kernel parameter space)
+// The team shape of an op with K columns: threads per row (log2) and rows
+// per thread, as the single GEMV chooses them.
+void gemv_chain_shape(int64_t K, unsigned char &tt_log2, unsigned char &rpt);
+// A chain of count <= kChainMaxOps ops in one persistent launch; `done`:
+// count + 1 zeroed counters in device memory (left zeroed).  ops[i].dep and
+// ops[i].report index ops of this launch.
+cudaError_t launch_gemv_chain(const ChainOp *ops, int count, unsigned int *done, cudaStream_t st,
+                              unsigned int *status, const DeviceInfo &dev);
 
 cudaError_t launch_moe_fp4(const uint16_t *x, const uint8_t *qw,
                            const uint16_t *s, const int32_t *ids, int topk,

@@ -186,6 +186,37 @@ int w4a16_linear_sequence(const w4a16_linear *ops, int count, int group,
                           void *stream);
 
 /*
+ * A chain of M = 1 INT4 linears in ONE persistent launch ("Lab 5", sections
+ * "CUDA Graph" and "Performance analysis": a decode step is 328 short
+ * bandwidth-bound GEMVs plus the vocabulary GEMV, and what separates them --
+ * launch overhead, each grid's ramp and drain -- is time the step loses).
+ * Computes what w4a16_linear_sequence computes for the same ops, with the
+ * same results bit for bit: each op reads its x only after every earlier op
+ * that writes it has finished, and writes its y only after every earlier op
+ * that reads or writes it has finished.  The packed weights of later ops
+ * stream into shared memory while earlier ops finish, so ops must not write
+ * any op's weights (refused).  Every op must have M == 1 (else
+ * W4A16_ERR_UNSUPPORTED) and pass the checks of w4a16_gemv; an op whose y
+ * overlaps its own x is refused.  The dependencies are found on the host
+ * from the address ranges of x and y.  Ops are launched in pieces of up to
+ * 192 per kernel (a dependency across pieces is met by the stream order).
+ *   scratch       : device memory of at least
+ *                   w4a16_linear_chain_scratch_bytes(count) bytes, 4-byte
+ *                   aligned, caller-owned, ALL ZERO before its first use
+ *                   (cudaMemset); the kernel keeps one completion counter per
+ *                   op there and every call leaves it all zero again (also
+ *                   one whose waits timed out), so the next call on the same
+ *                   stream may reuse it as is.  Calls that may run at the
+ *                   same time (other streams) need separate scratch.
+ *   scratch_bytes : its size in bytes.
+ * One CTA per SM; a launch in which some op depends on another is
+ * cooperative (all CTAs resident at once).  count == 0 launches nothing.
+ */
+int64_t w4a16_linear_chain_scratch_bytes(int count);
+int w4a16_linear_chain(const w4a16_linear *ops, int count, int group,
+                       void *scratch, int64_t scratch_bytes, void *stream);
+
+/*
  * The same sequence captured once into a CUDA graph and replayed by
  * w4a16_graph_launch: one host call per decode step, with the launches
  * chained on the device.

@@ -22,7 +22,7 @@ def declared_functions():
     for fn in os.listdir(inc):
         if fn.endswith(".h"):
             text = open(os.path.join(inc, fn)).read()
-            names += re.findall(r"^(?:int|const char \*)\s*(\w+)\s*\(", text, re.M)
+            names += re.findall(r"^(?:int64_t|int|const char \*)\s*(\w+)\s*\(", text, re.M)
     return names
 
 
@@ -31,7 +31,8 @@ def test_header_declares_the_entry_points():
     for n in ("w4a16_gemv", "w4a16_gemm", "fp4_moe_gemv", "w4a16_dequant", "w4a16_bf16_gemm",
               "w4a16_check_device_error", "w4a16_last_error_string", "w4a16_version",
               "w4a16_debug_inject", "w4a16_linear_sequence", "w4a16_graph_create",
-              "w4a16_graph_launch", "w4a16_graph_destroy"):
+              "w4a16_graph_launch", "w4a16_graph_destroy", "w4a16_linear_chain",
+              "w4a16_linear_chain_scratch_bytes"):
         assert n in names
 
 
@@ -133,3 +134,40 @@ def test_binding_checks_prebuilt_op_arrays():
         w4.w4a16_linear_sequence(arr, count=-1)
     with pytest.raises(TypeError):
         w4.w4a16_linear_sequence((ctypes.c_int64 * 8)(), count=1)
+
+
+def test_chain_host_validation(libw4):
+    # every case fails (or has nothing to do) before any CUDA call
+    import gemm_w4a16_gemv_gb300 as w4
+    A = 1 << 20
+    assert _call(libw4, "w4a16_linear_chain_scratch_bytes", 0) == 0
+    assert _call(libw4, "w4a16_linear_chain_scratch_bytes", 2) == 12           # 2 counters + exit
+    assert _call(libw4, "w4a16_linear_chain_scratch_bytes", 192) == 4 * 193
+    assert _call(libw4, "w4a16_linear_chain_scratch_bytes", 193) == 4 * (193 + 2)  # two launches
+    ops = (w4.w4a16_linear * 2)()
+    base = [(A, A + 0x100000, A + 0x200000, A + 0x300000, A + 0x400000),
+            (A + 0x500000, A + 0x600000, A + 0x700000, A + 0x800000, A + 0x900000)]
+    for i in range(2):
+        ops[i].x, ops[i].qw, ops[i].s, ops[i].z, ops[i].y = base[i]
+        ops[i].M, ops[i].N, ops[i].K = 1, 64, 256
+    S = A + 0xA00000
+    assert _call(libw4, "w4a16_linear_chain", ops, 0, 128, None, 0, None) == 0  # nothing to launch
+    assert _call(libw4, "w4a16_linear_chain", ops, 2, 128, None, 64, None) == 1  # null scratch
+    assert _call(libw4, "w4a16_linear_chain", ops, 2, 128, S, 8, None) == 1      # too small
+    assert "needed" in _call(libw4, "w4a16_last_error_string").decode()
+    assert _call(libw4, "w4a16_linear_chain", ops, 2, 128, S + 2, 64, None) == 3  # misaligned
+    ops[1].M = 2
+    assert _call(libw4, "w4a16_linear_chain", ops, 2, 128, S, 64, None) == 2      # M = 1 only
+    assert "op 1" in _call(libw4, "w4a16_last_error_string").decode()
+    ops[1].M = 1
+    ops[1].y = ops[1].x + 64                                                      # y inside its own x
+    assert _call(libw4, "w4a16_linear_chain", ops, 2, 128, S, 64, None) == 1
+    assert "own input" in _call(libw4, "w4a16_last_error_string").decode()
+    ops[1].y = base[0][1] + 256                                                   # y inside op 0's codes
+    assert _call(libw4, "w4a16_linear_chain", ops, 2, 128, S, 64, None) == 1
+    assert "weights of op 0" in _call(libw4, "w4a16_last_error_string").decode()
+    ops[1].y = S                                                                  # y on the scratch
+    assert _call(libw4, "w4a16_linear_chain", ops, 2, 128, S, 64, None) == 1
+    ops[1].y = base[1][4]
+    ops[0].K = 320
+    assert _call(libw4, "w4a16_linear_chain", ops, 2, 128, S, 64, None) == 1      # the GEMV's checks
