@@ -291,7 +291,8 @@ __device__ __forceinline__ bool chain_consume_op(const ChainOp &o, int nblocks, 
             const int sz_bytes = (((CW * 32) >> o.tt_log2) * R * G * 2 + 32 + 15) & ~15;
             const uint16_t *ss = reinterpret_cast<const uint16_t *>(st + w_bytes) + soff;
             const uint16_t *sz = reinterpret_cast<const uint16_t *>(st + w_bytes + sz_bytes) + soff;
-            int4_group_rows<R>(x, st, half_k, rbase, gs, rot, ss, sz, sym, G, part);
+            int4_group_rows<R>(x, st, half_k, rbase, gs, rot, ss, sz, sym, G,
+                               reinterpret_cast<const uint4 *>(xs) + 16 * gemv_x_gp(o.K) + gs, part);
         }
         const float red = warp_reduce_rows<R>(part, lane);
         if ((lane & (32 / R - 1)) == 0) h.psum[slot][phase][warp][reduced_row<R>(lane)] = red;
@@ -370,7 +371,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_chain_kernel(const __gr
         // (long since, as a rule): the region may be rewritten
         if (done_ops > 0 && !mbar_wait(&h.loaded, (done_ops - 1) & 1, a.status)) return;
         // the activation, converted once per CTA by all consumer warps
-        gemv_convert_vector<false>(o.x, xs, o.K, warp, CW, lane);
+        gemv_convert_vector<false, true>(o.x, xs, o.K, warp, CW, lane);
         __syncwarp();
         if (lane == 0) mbar_arrive(&h.sync_b);
         if (!mbar_wait(&h.sync_b, done_ops & 1, a.status)) return;

@@ -198,28 +198,51 @@ __device__ __forceinline__ int count_at_least(const uint32_t (&xb)[N], uint32_t 
     return c;
 }
 
-// INT4 activation word: 8 BF16 values (4 words of pairs, codes k..k+7 of a
-// packed word, whose bytes hold codes (k+2i, k+2i+1)), group exponent e and a
-// mask of set-aside values -> 4 words of signed 16-bit pairs hi = rint(x *
-// 2^(14-e)) (0 where masked) in the order the integer dot products meet
-// them: the even codes come as bytes (c0, c2, c4, c6) and the odd ones as
-// (16 c1, 16 c3, 16 c5, 16 c7), so the pairs are (x0, x2), (x4, x6), (x1, x3),
-// (x5, x7).  |hi| <= 32640.  Returns the sum of the 8 hi.
-__device__ __forceinline__ int int4_x_word(const uint32_t *xb, int e, uint32_t skip, uint32_t (&xr)[4]) {
+// INT4 activation unit: 32 BF16 values (as 16 words of pairs) and the
+// group exponent e -> 16 words of signed 16-bit pairs hi = rint(x *
+// 2^(14-e)) in the order the integer dot products meet them: for word m of a
+// packed unit (codes 8m..8m+7; its bytes hold codes (8m+2i, 8m+2i+1)), the
+// even codes come as bytes (c0, c2, c4, c6) and the odd ones as (16 c1,
+// 16 c3, 16 c5, 16 c7), so the pairs are (x0, x2), (x4, x6), (x1, x3),
+// (x5, x7).  |hi| <= 32640 for the values below 2^(e+1).  Returns the sum of
+// the 32 hi, taken modulo 2^32 (a value at or above 2^(e+1), to be set aside,
+// may round to anything: int4_x_drop takes exactly that back out).
+__device__ __forceinline__ uint32_t int4_x_unit(const uint32_t (&xb)[16], int e, uint32_t (&xr)[16]) {
     const float inv = pow2f(14 - e);
-    int v[8];
-    int sum = 0;
+    uint32_t sum = 0;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        const float x = bf16_bits_to_f32((q & 1) ? xb[q >> 1] >> 16 : xb[q >> 1] & 0xFFFFu);
-        v[q] = (skip >> q) & 1u ? 0 : rint_scaled(x, inv);  // x * inv is exact
-        sum += v[q];
+    for (int m = 0; m < 4; ++m) {
+        int v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            v[q] = rint_scaled(bf16_elem(xb, 8 * m + q), inv);  // x * inv is exact
+            sum += static_cast<uint32_t>(v[q]);
+        }
+        xr[4 * m + 0] = pack_i16x2(v[0], v[2]);
+        xr[4 * m + 1] = pack_i16x2(v[4], v[6]);
+        xr[4 * m + 2] = pack_i16x2(v[1], v[3]);
+        xr[4 * m + 3] = pack_i16x2(v[5], v[7]);
     }
-    xr[0] = pack_i16x2(v[0], v[2]);
-    xr[1] = pack_i16x2(v[4], v[6]);
-    xr[2] = pack_i16x2(v[1], v[3]);
-    xr[3] = pack_i16x2(v[5], v[7]);
     return sum;
+}
+
+// Take value k (0..31) of a unit converted by int4_x_unit with exponent e
+// out again: zero its 16-bit slot and return exactly what int4_x_unit added
+// to the sum for it (modulo 2^32).  k = 32: nothing to take out (returns 0).
+__device__ __forceinline__ uint32_t int4_x_drop(uint32_t (&xr)[16], const uint32_t (&xb)[16], uint32_t k, int e) {
+    const uint32_t m = k >> 3, q = k & 7;  // word m of the unit, value q of the word
+    const uint32_t slot = 4 * m + ((q & 1) ? 2 : 0) + ((q >> 2) & 1);  // (x0,x2) (x4,x6) (x1,x3) (x5,x7)
+    const bool high = (q >> 1) & 1;                                      // second of its pair
+    const uint32_t clear = high ? 0x0000FFFFu : 0xFFFF0000u;
+    uint32_t pair = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {  // static indices and selects: the arrays stay in registers
+        const bool at = static_cast<uint32_t>(i) == slot;
+        xr[i] &= at ? clear : 0xFFFFFFFFu;
+        pair = static_cast<uint32_t>(i) == (k >> 1) ? xb[i] : pair;
+    }
+    const uint32_t b = (k & 1) ? pair >> 16 : pair & 0xFFFFu;  // its BF16 bits
+    return k < 32 ? static_cast<uint32_t>(rint_scaled(bf16_bits_to_f32(b), pow2f(14 - e))) : 0u;
 }
 
 // FP4 activation unit: 32 BF16 values -> 16 f16x2 natural pairs (x[2i],

@@ -254,8 +254,8 @@ __device__ __forceinline__ void gemv_prefetch_groups(const GemvParams &a, int64_
 // Activation conversion, once per CTA, into shared memory at xs, laid out as
 // uint4 "planes" so that the threads' later register loads are free of bank
 // conflicts.
-//  INT4: one 8-value word per thread (K/8 words; the 16 words of a group are
-//        16 neighbouring lanes, K % 128 == 0 keeps every group whole).
+//  INT4: one 32-value unit per thread (K/32 units; the four units of a group
+//        are four neighbouring lanes, K % 128 == 0 keeps every group whole).
 //        Plane p = 4s + i (s: 32-value unit within the group, i: word within
 //        the unit) holds Gp = G rounded up to even entries, one per group;
 //        plane 16 holds per group (sum of hi, set-aside list, x of the first
@@ -288,36 +288,47 @@ __device__ __forceinline__ void gemv_convert_fp4_unit(const uint16_t *x, unsigne
     }
 }
 
-// INT4: W consecutive 8-value words (their BF16 bits v, zero on padding
-// lanes), starting at word w of an activation of K values, into the planes
-// at xs (the layout above).  The 16 / W lanes of a group are neighbours; all
-// 32 lanes of the warp call it together (the group shuffles); `ok` false: a
-// padding lane (of a whole padding group), which stores nothing.
-template <int W>
-__device__ __forceinline__ void gemv_convert_int4_words(const uint32_t (&xb)[4 * W], unsigned char *xs, int w, bool ok,
-                                                        int K) {
-    constexpr int L = 16 / W;  // lanes of a group
+// INT4: one 32-value unit u (= 4 words) of an activation of K values into
+// the planes at xs (the layout above).  The four units of a group are four
+// neighbouring lanes; all 32 lanes of the warp call it together (the group
+// shuffles); `ok` false: a padding lane (of a whole padding group), which
+// stores nothing.  CG: load through L2 only (in a chain of linears the
+// activation may have been written by another CTA of the same launch).
+template <bool CG>
+__device__ __forceinline__ void gemv_convert_int4_unit(const uint16_t *x, unsigned char *xs, int u, bool ok, int K) {
     uint4 *xw = reinterpret_cast<uint4 *>(xs);
     const int lane = threadIdx.x & 31;
+    uint32_t xb[16];
+    if (ok) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(x + 32 * u);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 v = CG ? __ldcg(p + q) : p[q];
+            xb[4 * q] = v.x;
+            xb[4 * q + 1] = v.y;
+            xb[4 * q + 2] = v.z;
+            xb[4 * q + 3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) xb[i] = 0u;
+    }
     // the group's largest |x| (exponent e1) and how many values have an
     // exponent of at least e1 - 1
-    uint32_t m2 = 0;
-#pragma unroll
-    for (int i = 0; i < 4 * W; ++i) m2 = __vmaxu2(m2, xb[i] & 0x7FFF7FFFu);
-    uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
-#pragma unroll
-    for (int d = 1; d < L; d <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, d));
+    uint32_t m = unit_absmax_bits(xb);
+    m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
     int e = exponent_of_absmax(m);
-    int c = (m & 0x7F80u) > 0x0080u ? count_at_least<4 * W>(xb, (m & 0x7F80u) - 0x0080u) : 3;
-#pragma unroll
-    for (int d = 1; d < L; d <<= 1) c += __shfl_xor_sync(0xffffffffu, c, d);
+    int c = (m & 0x7F80u) > 0x0080u ? count_at_least<16>(xb, (m & 0x7F80u) - 0x0080u) : 3;
+    c += __shfl_xor_sync(0xffffffffu, c, 1);
+    c += __shfl_xor_sync(0xffffffffu, c, 2);
     Top3 t = {0u, 0u, 0u, 0u, 0u, 0u, 0u};
     bool o1 = false, o2 = false;
     // the third largest more than one binade below the largest: the largest
     // one or two may lie above the third largest's binade (warp-uniform
     // branch: the group search shuffles)
     if (__any_sync(0xffffffffu, c < 3)) {
-        t = group_top3<W>(xb, lane);
+        t = group_top3<4>(xb, lane);
         if (c < 3) {
             const bool few = t.a3 == 0u;  // at most two nonzero values: set them aside
             e = few ? 0 : exponent_of_absmax(t.a3);
@@ -326,65 +337,43 @@ __device__ __forceinline__ void gemv_convert_int4_words(const uint32_t (&xb)[4 *
             o2 = t.a2 != 0u && (few || t.a2 >= thr);  // implies o1
         }
     }
-    const int gp = gemv_x_gp(K), grp = w >> 4;
-    int sum = 0;
-#pragma unroll
-    for (int i = 0; i < W; ++i) {
-        const uint32_t j = static_cast<uint32_t>((w + i) & 15);  // word within the group
-        uint32_t skip = 0u;
-        if (o1 && (t.p1 >> 3) == j) skip |= 1u << (t.p1 & 7u);
-        if (o2 && (t.p2 >> 3) == j) skip |= 1u << (t.p2 & 7u);
-        uint32_t wr[4];
-        sum += int4_x_word(xb + 4 * i, e, skip, wr);
-        if (ok) xw[(4 * (j >> 2) + (j & 3)) * gp + grp] = make_uint4(wr[0], wr[1], wr[2], wr[3]);
+    uint32_t w[16];
+    uint32_t usum = int4_x_unit(xb, e, w);
+    // the set-aside values among this lane's 32: out of the integer part
+    const uint32_t mine = static_cast<uint32_t>(u & 3);
+    if (__any_sync(0xffffffffu, o1)) {  // rare: keep the common path free of it
+        usum -= int4_x_drop(w, xb, o1 && (t.p1 >> 5) == mine ? t.p1 & 31u : 32u, e);
+        usum -= int4_x_drop(w, xb, o2 && (t.p2 >> 5) == mine ? t.p2 & 31u : 32u, e);
     }
+    int sum = static_cast<int>(usum);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    if (ok) {
+        const int gp = gemv_x_gp(K), grp = u >> 2, sub = u & 3;
 #pragma unroll
-    for (int d = 1; d < L; d <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, d);
-    if (ok && (w & 15) == 0) {
-        const uint32_t n = (o1 ? 1u : 0u) + (o2 ? 1u : 0u);
-        const uint32_t list = (o1 ? t.p1 : 0u) | ((o2 ? t.p2 : 0u) << 8) | (n << 16) |
-                              (static_cast<uint32_t>(e + 128) << 24);
-        // |sum| <= 128 * 32640 < 2^23: exact in binary32
-        xw[16 * gp + grp] = make_uint4(__float_as_uint(static_cast<float>(sum)), list,
-                                       __float_as_uint(bf16_bits_to_f32(t.v1)), __float_as_uint(bf16_bits_to_f32(t.v2)));
-    }
-}
-
-// INT4 activation of K values with W words per thread (one round of the
-// warps covers K <= 4 * 8 * 32 * nwarps, the most W = 4 allows).
-template <int W>
-__device__ __forceinline__ void gemv_convert_int4(const uint16_t *x, unsigned char *xs, int K, int warp, int nwarps,
-                                                  int lane) {
-    const int items = (K >> 3) / W;  // W words each; a group is 16 / W items
-    const int rot = (16 / W) * static_cast<int>((blockIdx.x * 7u) % static_cast<unsigned>(K >> 7));
-    const uint4 *x4 = reinterpret_cast<const uint4 *>(x);
-    for (int i0 = warp * 32; i0 < items; i0 += nwarps * 32) {  // warp-uniform
-        const bool ok = i0 + lane < items;                      // the lanes of a group share ok
-        int i = i0 + lane + rot;
-        if (i >= items) i -= items;
-        uint32_t v[4 * W];
-#pragma unroll
-        for (int q = 0; q < W; ++q) {
-            const uint4 u = ok ? __ldcg(x4 + i * W + q) : make_uint4(0u, 0u, 0u, 0u);  // L2 only, as load_x_unit
-            v[4 * q] = u.x;
-            v[4 * q + 1] = u.y;
-            v[4 * q + 2] = u.z;
-            v[4 * q + 3] = u.w;
+        for (int i = 0; i < 4; ++i)
+            xw[(4 * sub + i) * gp + grp] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        if (sub == 0) {
+            const uint32_t n = (o1 ? 1u : 0u) + (o2 ? 1u : 0u);
+            const uint32_t list = (o1 ? t.p1 : 0u) | ((o2 ? t.p2 : 0u) << 8) | (n << 16) |
+                                  (static_cast<uint32_t>(e + 128) << 24);
+            // |sum| <= 128 * 32640 < 2^23: exact in binary32
+            xw[16 * gp + grp] = make_uint4(__float_as_uint(static_cast<float>(sum)), list,
+                                           __float_as_uint(bf16_bits_to_f32(t.v1)),
+                                           __float_as_uint(bf16_bits_to_f32(t.v2)));
         }
-        gemv_convert_int4_words<W>(v, xs, i * W, ok, K);
     }
 }
 
 // The whole activation x (K values) by consumer warps warp, warp + nwarps,
-// ...  Every CTA reads the same few KB at the same moment; starting each CTA
-// at a different group (a rotation by whole groups) spreads the requests
-// over the L2 slices.  INT4 takes 8, 16 or 32 values a thread as K grows, so
-// that one round of loads covers the activation.
-template <bool FP4>
+// ..., one 32-value unit a thread.  Every CTA reads the same few KB at the
+// same moment; starting each CTA at a different group (a rotation by whole
+// groups) spreads the requests over the L2 slices.
+template <bool FP4, bool CG = false>
 __device__ __forceinline__ void gemv_convert_vector(const uint16_t *x, unsigned char *xs, int K, int warp, int nwarps,
                                                     int lane) {
+    const int units = K >> 5;
     if constexpr (FP4) {
-        const int units = K >> 5;
         const int rot = static_cast<int>((blockIdx.x * 7u) % static_cast<unsigned>(units));
         for (int u0 = warp * 32; u0 < units; u0 += nwarps * 32) {  // warp-uniform
             const bool ok = u0 + lane < units;
@@ -393,13 +382,13 @@ __device__ __forceinline__ void gemv_convert_vector(const uint16_t *x, unsigned 
             gemv_convert_fp4_unit(x, xs, u, ok, units);
         }
     } else {
-        const int words = K >> 3;
-        if (words <= nwarps * 32)
-            gemv_convert_int4<1>(x, xs, K, warp, nwarps, lane);
-        else if (words <= 2 * nwarps * 32)
-            gemv_convert_int4<2>(x, xs, K, warp, nwarps, lane);
-        else
-            gemv_convert_int4<4>(x, xs, K, warp, nwarps, lane);
+        const int rot = 4 * static_cast<int>((blockIdx.x * 7u) % static_cast<unsigned>(units >> 2));
+        for (int u0 = warp * 32; u0 < units; u0 += nwarps * 32) {  // warp-uniform
+            const bool ok = u0 + lane < units;                     // the four lanes of a group share ok
+            int u = u0 + lane + rot;
+            if (u >= units) u -= units;
+            gemv_convert_int4_unit<CG>(x, xs, u, ok, K);
+        }
     }
 }
 
@@ -407,9 +396,8 @@ __device__ __forceinline__ void gemv_convert_vector(const uint16_t *x, unsigned 
 // sub-units, in the thread's rotated order) and constants.
 struct Int4X {
     uint32_t xh[4][16];
-    float sum, pw;
-    uint32_t list;           // set-aside positions and count (plane 16 layout)
-    const uint4 *consts;     // the group's plane-16 entry (the set-aside x, read when needed)
+    float sum;
+    float pw;  // 2^(e-14), negated when the group has set-aside values (their list stays in shared memory)
 };
 
 __device__ __forceinline__ void int4_load_x(const unsigned char *xs, int gp, int gs, int rot, bool valid, Int4X &r) {
@@ -426,21 +414,21 @@ __device__ __forceinline__ void int4_load_x(const unsigned char *xs, int gp, int
             r.xh[q][4 * i + 3] = v4.w;
         }
     }
-    r.consts = xw + 16 * gp + gs;
-    const uint4 c = *r.consts;
+    const uint4 c = xw[16 * gp + gs];
     r.sum = __uint_as_float(c.x);
-    r.list = valid ? c.y : 0u;
-    r.pw = valid ? pow2f(static_cast<int>(c.y >> 24) - 128 - 14) : 0.0f;
+    const float pw = valid ? pow2f(static_cast<int>(c.y >> 24) - 128 - 14) : 0.0f;
+    r.pw = (valid && ((c.y >> 16) & 3u)) ? -pw : pw;
 }
 
 // One stage's work of a consumer thread: RPT rows (from rbase) of its group
 // g; codes at st + row * half_k + 64 g, the 16-byte sub-units taken in
 // rotated order; ss / sz: the stage's scale and zero rows (sz unused when
-// sym).  Adds each row's contribution to part[].
+// sym); xc: the group's plane-16 entry.  Adds each row's contribution to
+// part[].
 template <int RPT>
 __device__ __forceinline__ void int4_group_rows(const Int4X &x, const unsigned char *st, int half_k, int rbase, int g,
                                                 int rot, const uint16_t *ss, const uint16_t *sz, bool sym, int G,
-                                                float (&part)[RPT]) {
+                                                const uint4 *xc, float (&part)[RPT]) {
     int lo[RPT], hi[RPT];
 #pragma unroll
     for (int rr = 0; rr < RPT; ++rr) lo[rr] = hi[rr] = 0;
@@ -466,7 +454,6 @@ __device__ __forceinline__ void int4_group_rows(const Int4X &x, const unsigned c
             }
         }
     }
-    const uint32_t n = (x.list >> 16) & 3u;
 #pragma unroll
     for (int rr = 0; rr < RPT; ++rr) {
         // hi is a multiple of 16 (exact shift); |dot| < 2^26 (the conversion
@@ -475,16 +462,18 @@ __device__ __forceinline__ void int4_group_rows(const Int4X &x, const unsigned c
         const int gi = (rbase + rr) * G + g;
         const float sv = f16_bits_to_f32(ss[gi]);
         const float zf = sym ? 8.0f : f16_bits_to_f32(sz[gi]);  // symmetric: the midpoint 8
-        float acc = (sv * x.pw) * fmaf(-zf, x.sum, static_cast<float>(dot));
-        if (n) {
+        float acc = (sv * fabsf(x.pw)) * fmaf(-zf, x.sum, static_cast<float>(dot));
+        if (x.pw < 0.0f) {
             // the set-aside values: s (q - z) x, each product exact in binary32
+            // (the activation region is not rewritten while the rows run)
             const unsigned char *row = st + static_cast<size_t>(rbase + rr) * half_k + 64 * g;
-            const uint4 c = *x.consts;  // (the activation region is not rewritten during the op)
-            const uint32_t p1 = x.list & 127u;
+            const uint4 c = *xc;
+            const uint32_t n = (c.y >> 16) & 3u;
+            const uint32_t p1 = c.y & 127u;
             const float c1 = static_cast<float>((row[p1 >> 1] >> ((p1 & 1u) * 4u)) & 15u);
             acc = fmaf(sv * (c1 - zf), __uint_as_float(c.z), acc);
             if (n > 1) {
-                const uint32_t p2 = (x.list >> 8) & 127u;
+                const uint32_t p2 = (c.y >> 8) & 127u;
                 const float c2 = static_cast<float>((row[p2 >> 1] >> ((p2 & 1u) * 4u)) & 15u);
                 acc = fmaf(sv * (c2 - zf), __uint_as_float(c.w), acc);
             }
@@ -558,7 +547,9 @@ __device__ __forceinline__ void gemv_consume_int4(const GemvParams &a, GemvHeade
         float part[RPT];
 #pragma unroll
         for (int rr = 0; rr < RPT; ++rr) part[rr] = 0.0f;
-        if (valid) int4_group_rows<RPT>(x, st, half_k, rbase, gs, rot, ss, sz, SYM, a.G, part);
+        if (valid)
+            int4_group_rows<RPT>(x, st, half_k, rbase, gs, rot, ss, sz, SYM, a.G,
+                                 reinterpret_cast<const uint4 *>(xs) + 16 * gemv_x_gp(a.K) + gs, part);
         gemv_release_stage<CW, RPT>(h, part, slot, phase, warp, lane);
         v += rows;
         if (++slot == a.stages) {
