@@ -23,7 +23,7 @@ __all__ = [
     "w4a16_check_device_error", "w4a16_last_error_string", "w4a16_version",
     "w4a16_debug_inject", "INJECT_STALL_PIPELINE", "INJECT_STALL_CONSUMERS",
     "w4a16_linear", "w4a16_linear_array", "w4a16_linear_sequence", "w4a16_graph_create", "w4a16_graph_launch",
-    "w4a16_linear_chain", "w4a16_linear_chain_scratch_bytes", "chain_scratch",
+    "w4a16_linear_chain", "w4a16_linear_chain_scratch_bytes", "chain_scratch", "w4a16_linear_chain_noalloc",
     "w4a16_graph_destroy", "W4A16Graph",
     "library_path", "W4A16Error", "STATUS", "FMT_INT4", "FMT_FP4",
     "OUT_F32", "OUT_BF16",
@@ -62,6 +62,7 @@ SIGNATURES = {
     "w4a16_linear_sequence": ([_OPS, _INT, _INT, _P], _INT),
     "w4a16_linear_chain": ([_OPS, _INT, _INT, _P, _I64, _P], _INT),
     "w4a16_linear_chain_scratch_bytes": ([_INT], _I64),
+    "w4a16_linear_chain_noalloc": ([_OPS, _INT, _INT, _P], _INT),
     "w4a16_graph_create": ([_OPS, _INT, _INT, ctypes.POINTER(ctypes.c_void_p)], _INT),
     "w4a16_graph_launch": ([_P, _P], _INT),
     "w4a16_graph_destroy": ([_P], _INT),
@@ -296,6 +297,25 @@ def w4a16_linear_chain(ops, scratch, group: int = 128, stream=None, count=None):
     with torch.cuda.device(dev):  # the library launches on the current device
         _check(lib().w4a16_linear_chain(arr, n, group, ctypes.c_void_p(scratch.data_ptr()), nbytes,
                                         _stream(stream, dev)))
+
+
+def w4a16_linear_chain_noalloc(ops, group: int = 128, stream=None, count=None):
+    """w4a16_linear_chain with the library's built-in counters instead of
+    caller scratch: nothing is allocated (for callers that may not allocate
+    device memory).  At most 4032 linears; calls that can overlap on the GPU
+    race on the shared counters, so keep them on one stream."""
+    if isinstance(ops, ctypes.Array):
+        if ops._type_ is not w4a16_linear:
+            raise TypeError("ops must be an array of w4a16_linear")
+        arr, n = ops, len(ops) if count is None else int(count)
+        if not 0 <= n <= len(ops):
+            raise ValueError("count %d outside 0..%d (the array's length)" % (n, len(ops)))
+        dev = torch.cuda.current_device()
+    else:
+        arr, n = w4a16_linear_array(ops, group), len(ops)
+        dev = ops[0][1].device if ops else torch.cuda.current_device()
+    with torch.cuda.device(dev):  # the library launches on the current device
+        _check(lib().w4a16_linear_chain_noalloc(arr, n, group, _stream(stream, dev)))
 
 
 class W4A16Graph:

@@ -265,6 +265,94 @@ int64_t chain_scratch_bytes(int count) {
     return 4 * (static_cast<int64_t>(count) + launches);
 }
 
+// Built-in scratch of w4a16_linear_chain_noalloc, for callers that cannot
+// allocate device memory: 16 KB (4096 words) of completion counters; a chain
+// of n linears needs n + ceil(n / 192) of them, so at most kNoAllocMaxOps.
+// It exists once per device that loads this library, for as long as the
+// library stays loaded.  In host code its name is not a device address: the
+// address comes from cudaGetSymbolAddress, looked up once per device.
+constexpr int kNoAllocMaxOps = 4032;
+constexpr int kNoAllocWords = 4096;
+static_assert(kNoAllocMaxOps + (kNoAllocMaxOps + w4::kChainMaxOps - 1) / w4::kChainMaxOps <= kNoAllocWords,
+              "built-in scratch too small");
+static __device__ __align__(256) unsigned int g_chain_noalloc_scratch[kNoAllocWords];
+
+struct NoAllocScratch {
+    std::atomic<bool> ready{false};
+    unsigned int *ptr = nullptr;
+};
+NoAllocScratch g_noalloc[64];
+std::mutex g_noalloc_mu;
+
+// The built-in scratch's device address on `device` (the current device).
+int noalloc_scratch(int device, unsigned int *&ptr) {
+    NoAllocScratch &c = g_noalloc[device & 63];
+    if (!c.ready.load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lk(g_noalloc_mu);
+        if (!c.ready.load(std::memory_order_relaxed)) {
+            void *p = nullptr;
+            const cudaError_t e = cudaGetSymbolAddress(&p, g_chain_noalloc_scratch);
+            if (e != cudaSuccess)
+                return fail(W4A16_ERR_CUDA, "w4a16_linear_chain_noalloc: scratch address: %s", cudaGetErrorString(e));
+            c.ptr = static_cast<unsigned int *>(p);
+            c.ready.store(true, std::memory_order_release);
+        }
+    }
+    ptr = c.ptr;
+    return W4A16_OK;
+}
+
+// plan_chain for the ops c0 .. c0 + n - 1 of a chain of `count` (the piece
+// one launch takes), with no scratch of the caller's to protect: the
+// dependencies are sought within the piece (an earlier piece is finished by
+// the stream order) and the indices are the piece's own.
+int plan_chain_piece(const w4a16_linear *ops, int count, int c0, int n, w4::ChainOp *plan) {
+    for (int i = 0; i < n; ++i) {
+        const int oi = c0 + i;
+        const w4a16_linear &o = ops[oi];
+        if (o.M != 1)
+            return fail(W4A16_ERR_UNSUPPORTED, "w4a16_linear_chain_noalloc: op %d has M=%lld (M = 1 ops only)", oi,
+                        (long long)o.M);
+        if (o.N > 0x7FFFFFFF)
+            return fail(W4A16_ERR_UNSUPPORTED, "w4a16_linear_chain_noalloc: op %d N=%lld too large", oi,
+                        (long long)o.N);
+        const Range xi = range_of(o.x, 2 * o.K), yi = range_of(o.y, 2 * o.N);
+        if (overlap(xi, yi))
+            return fail(W4A16_ERR_INVALID_ARG, "w4a16_linear_chain_noalloc: op %d writes its own input", oi);
+        for (int j = 0; j < count; ++j) {
+            const w4a16_linear &w = ops[j];
+            const int64_t Gj = w.K / 128;
+            if (overlap(yi, range_of(w.qw, w.N * w.K / 2)) || overlap(yi, range_of(w.s, 2 * w.N * Gj)) ||
+                (w.z && overlap(yi, range_of(w.z, 2 * w.N * Gj))))
+                return fail(W4A16_ERR_INVALID_ARG, "w4a16_linear_chain_noalloc: op %d writes the weights of op %d", oi,
+                            j);
+        }
+        w4::ChainOp &c = plan[i];
+        c.x = o.x;
+        c.qw = o.qw;
+        c.s = o.s;
+        c.z = o.z;
+        c.y = o.y;
+        c.N = static_cast<int>(o.N);
+        c.K = static_cast<int>(o.K);
+        w4::gemv_chain_shape(o.K, c.tt_log2, c.rpt);
+        c.dep = -1;
+        c.report = 0;
+        c.pad = 0;
+        for (int j = i - 1; j >= 0; --j) {
+            const w4a16_linear &p = ops[c0 + j];
+            const Range xj = range_of(p.x, 2 * p.K), yj = range_of(p.y, 2 * p.N);
+            if (overlap(yj, xi) || overlap(xj, yi) || overlap(yj, yi)) {
+                c.dep = j;
+                break;
+            }
+        }
+    }
+    for (int i = 0; i < n; ++i)
+        if (plan[i].dep >= 0) plan[plan[i].dep].report = 1;
+    return W4A16_OK;
+}
+
 // Launches a planned chain in pieces of at most kChainMaxOps ops, each with
 // its own counters in the scratch; a dependency on an op of an earlier piece
 // is met by the stream order.
@@ -416,6 +504,43 @@ int w4a16_linear_chain(const w4a16_linear *ops, int count, int group, void *scra
     }
     delete[] plan;
     return r;
+}
+
+int w4a16_linear_chain_noalloc(const w4a16_linear *ops, int count, int group, void *stream) {
+    if (int r = check_sequence(ops, count, group, "w4a16_linear_chain_noalloc")) return r;
+    if (count == 0) return ok();
+    if (count > kNoAllocMaxOps)
+        return fail(W4A16_ERR_UNSUPPORTED,
+                    "w4a16_linear_chain_noalloc: %d linears; its built-in scratch holds the counters of at most %d "
+                    "(use w4a16_linear_chain with scratch of your own)",
+                    count, kNoAllocMaxOps);
+    w4::DeviceInfo dev;
+    unsigned int *status = nullptr;
+    if (int r = device_state(dev, status)) return r;
+    if (int r = check_sequence_ptrs(ops, count, dev.device, "w4a16_linear_chain_noalloc")) return r;
+    unsigned int *scratch = nullptr;
+    if (int r = noalloc_scratch(dev.device, scratch)) return r;
+    // every op checked (and its dependencies found) before anything is queued
+    w4::ChainOp piece[w4::kChainMaxOps];
+    for (int c0 = 0; c0 < count; c0 += w4::kChainMaxOps) {
+        const int n = count - c0 < w4::kChainMaxOps ? count - c0 : w4::kChainMaxOps;
+        if (int r = plan_chain_piece(ops, count, c0, n, piece)) return r;
+    }
+    // the counters must start at zero; the array keeps whatever the last call
+    // left, so clear them in stream order before the launches
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(scratch, 0, static_cast<size_t>(chain_scratch_bytes(count)), st);
+    if (e != cudaSuccess)
+        return fail(W4A16_ERR_CUDA, "w4a16_linear_chain_noalloc: clearing the counters: %s", cudaGetErrorString(e));
+    unsigned int *done = scratch;
+    for (int c0 = 0; c0 < count; c0 += w4::kChainMaxOps) {
+        const int n = count - c0 < w4::kChainMaxOps ? count - c0 : w4::kChainMaxOps;
+        plan_chain_piece(ops, count, c0, n, piece);  // checked above
+        e = w4::launch_gemv_chain(piece, n, done, st, status, dev);
+        if (e != cudaSuccess) return launched(e, "w4a16_linear_chain_noalloc");
+        done += n + 1;
+    }
+    return ok();
 }
 
 int w4a16_linear_sequence(const w4a16_linear *ops, int count, int group, void *stream) {

@@ -217,6 +217,29 @@ int w4a16_linear_chain(const w4a16_linear *ops, int count, int group,
                        void *scratch, int64_t scratch_bytes, void *stream);
 
 /*
+ * w4a16_linear_chain without caller scratch: the same computation, for
+ * callers that cannot allocate device memory of their own -- for instance an
+ * engine that hands every byte of the GPU to its own memory pool and gives
+ * plug-in code only the tensors it works on, or code that must not call
+ * cudaMalloc because of the device-wide synchronisation it can cause.  (The
+ * pages have no counterpart: this is an interface choice of this library.)
+ * The per-linear completion counters live in a 16 KB array that the library
+ * holds on every device that loads it, until the library is unloaded; this
+ * call allocates nothing.
+ *   Limit: at most 4032 linears per call (W4A16_ERR_UNSUPPORTED beyond).
+ *   The first call on a device looks up the array's device address (once
+ *   per device); make that first call before any stream capture.
+ *   Every call clears the counters it uses (a memset on `stream`) before its
+ *   launches.  All calls on a device share the one array: two calls whose
+ *   work can overlap on the GPU (different streams without ordering between
+ *   them) race on it and may compute wrong results or time out; serialise
+ *   them (one stream, or events).
+ * ops, count, group and stream are as for w4a16_linear_chain.
+ */
+int w4a16_linear_chain_noalloc(const w4a16_linear *ops, int count, int group,
+                               void *stream);
+
+/*
  * The same sequence captured once into a CUDA graph and replayed by
  * w4a16_graph_launch: one host call per decode step, with the launches
  * chained on the device.

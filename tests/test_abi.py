@@ -32,7 +32,7 @@ def test_header_declares_the_entry_points():
               "w4a16_check_device_error", "w4a16_last_error_string", "w4a16_version",
               "w4a16_debug_inject", "w4a16_linear_sequence", "w4a16_graph_create",
               "w4a16_graph_launch", "w4a16_graph_destroy", "w4a16_linear_chain",
-              "w4a16_linear_chain_scratch_bytes"):
+              "w4a16_linear_chain_scratch_bytes", "w4a16_linear_chain_noalloc"):
         assert n in names
 
 
@@ -171,3 +171,18 @@ def test_chain_host_validation(libw4):
     ops[1].y = base[1][4]
     ops[0].K = 320
     assert _call(libw4, "w4a16_linear_chain", ops, 2, 128, S, 64, None) == 1      # the GEMV's checks
+
+
+def test_chain_noalloc_host_validation(libw4):
+    # every case fails (or has nothing to do) before any CUDA call
+    import gemm_w4a16_gemv_gb300 as w4
+    A = 1 << 20
+    ops = (w4.w4a16_linear * 4033)()
+    for i in range(4033):
+        ops[i].x, ops[i].qw, ops[i].s, ops[i].z, ops[i].y = A, A, A, A, A
+        ops[i].M, ops[i].N, ops[i].K = 1, 16, 128
+    assert _call(libw4, "w4a16_linear_chain_noalloc", ops, 0, 128, None) == 0    # nothing to do
+    assert _call(libw4, "w4a16_linear_chain_noalloc", ops, 4033, 128, None) == 2  # beyond the built-in limit
+    assert "4032" in _call(libw4, "w4a16_last_error_string").decode()
+    ops[3].K = 320
+    assert _call(libw4, "w4a16_linear_chain_noalloc", ops, 8, 128, None) == 1     # the GEMV's checks
