@@ -32,8 +32,8 @@
 //
 // One CTA computes a tile of 112 output columns n x 128 rows m; each CTA
 // loads its own X tiles (from L2 after the first CTA that needs them):
-//  * warp 0 (one lane): one bulk copy each of the tile's scale and zero rows;
-//    per group its X rows (two TMA boxes, 128-byte swizzle);
+//  * warp 0: the tile's scale and zero rows (16-byte cp.async chunks); then,
+//    from one lane, per group its X rows (two TMA boxes, 128-byte swizzle);
 //  * warp 2 (one lane): every two groups the packed codes of the tile's rows,
 //    128 bytes each (TMA), on a ring of its own;
 //  * warps 8-11 (even groups) and 16-19 (odd groups), TMEM lane quarters
@@ -145,7 +145,7 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     const int n0 = blockIdx.x * BNW;
     const int m0 = blockIdx.y * BM;
     const int ngroups = a.G;
-    const int rows_n = max(0, min(BNW, a.N - n0));  // a multiple of 16 (0 in padding CTAs)
+    const int rows_n = max(0, min(BNW, a.N - n0));  // weight rows of this tile
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < XP; ++i) {
@@ -164,7 +164,7 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             mbar_init(&bar.accfull[i], 1);
             mbar_init(&bar.accempty[i], EPI_WARPS);
         }
-        mbar_init(&bar.szfull, 1);
+        mbar_init(&bar.szfull, 32);  // the 32 lanes of the producer warp (cp.async arrivals)
         mbar_init(&bar.done, EPI_WARPS + PREP_WARPS);
         mbar_init(&bar.drained, 2);
         fence_barrier_init();
@@ -198,13 +198,23 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         if (lane == 0) {
             tma_prefetch_desc(&tmW);
             tma_prefetch_desc(&tmX);
-            const uint32_t szb = static_cast<uint32_t>(rows_n) * a.G * 2;
-            mbar_arrive_expect_tx(&bar.szfull, SYM ? szb : 2 * szb);  // symmetric: scales only
-            if (szb) {
-                bulk_g2s(smem + a.off_sz, a.s + static_cast<size_t>(n0) * a.G, szb, &bar.szfull, pol);
-                if (!SYM)
-                    bulk_g2s(smem + a.off_sz + a.sz_bytes, a.z + static_cast<size_t>(n0) * a.G, szb, &bar.szfull, pol);
+        }
+        {
+            // the tile's scale (and zero) rows: one contiguous byte range
+            // starting 16-byte aligned (n0 is a multiple of 112), copied in
+            // 16-byte chunks by the warp's lanes; a chunk past the tensor's
+            // end (any N) reads only the bytes before it and zero-fills the rest
+            const uint64_t b0 = static_cast<uint64_t>(n0) * a.G * 2;
+            const uint64_t b1 = b0 + static_cast<uint64_t>(rows_n) * a.G * 2;
+            const uint64_t total = static_cast<uint64_t>(a.N) * a.G * 2;
+            const unsigned char *gs = reinterpret_cast<const unsigned char *>(a.s);
+            const unsigned char *gz = reinterpret_cast<const unsigned char *>(a.z);
+            for (uint64_t o = b0 + 16 * static_cast<uint64_t>(lane); o < b1; o += 16 * 32) {
+                const uint32_t n = total - o < 16 ? static_cast<uint32_t>(total - o) : 16u;
+                cp_async_16_zfill(smem + a.off_sz + (o - b0), gs + o, n);
+                if (!SYM) cp_async_16_zfill(smem + a.off_sz + a.sz_bytes + (o - b0), gz + o, n);
             }
+            cp_async_arrive_noinc(&bar.szfull);  // counts once per lane
         }
         int xs = 0, xph = 0;  // X stage and its phase
         // test-only injection: no X stage is ever issued, so the waits on it
@@ -552,7 +562,7 @@ cudaError_t launch_gemm_int4(const uint16_t *X, const uint8_t *qw, const uint16_
     a.N = static_cast<int>(N);
     a.K = static_cast<int>(K);
     a.G = static_cast<int>(K / 128);
-    a.sz_bytes = (BNW * a.G * 2 + 15) & ~15;
+    a.sz_bytes = (BNW * a.G * 2 + 15) & ~15;  // whole 16-byte chunks of the tile's rows
     // as many X stages (groups) as shared memory allows (3 .. MAX_XP; the MMA
     // issuers step their ring positions by two groups and order their waits
     // by the ring depth)

@@ -92,8 +92,9 @@ int w4a16_gemv(const uint16_t *x, const uint8_t *qw, const uint16_t *s,
  * BF16 weight matrix is written to HBM).
  *   X : bfloat16 [M, K];  qw, s, z as for w4a16_gemv (z may be NULL:
  *       symmetric INT4);  Y : bfloat16 [M, N].
- * Requires group == 128, K % 128 == 0, 128 <= K <= 16384, N % 16 == 0.  Any
- * M >= 1 is accepted (rows past M in the last tile are masked).  Decode-sized
+ * Requires group == 128, K % 128 == 0, 128 <= K <= 16384, N >= 1.  Any
+ * M >= 1 and any N are accepted (rows past M and N in the last tiles are
+ * masked).  Decode-sized
  * batches run as the streaming GEMV instead: M <= 4 rows share one pass over
  * the weights, 5 <= M <= 8 take two passes (four rows, then the rest);
  * larger M runs on the tensor cores.

@@ -67,7 +67,7 @@ def test_host_validation_codes(libw4):
     assert _call(libw4, "w4a16_gemv", A, A, A, A, A, 16, 320, 128, None) == 1
     assert _call(libw4, "w4a16_gemv", A, A, A, A, A, 16, 32768, 128, None) == 2
     assert _call(libw4, "w4a16_gemv", A + 8, A, A, A, A, 16, 256, 128, None) == 3
-    assert _call(libw4, "w4a16_gemm", A, A, A, A, A, 4, 24, 256, 128, None) == 2
+    assert _call(libw4, "w4a16_gemm", A, A, A, A, A, 4, 24, 32768, 128, None) == 2  # K beyond 16384
     assert _call(libw4, "fp4_moe_gemv", A, A, A, A, 0, A, 4, 8, 128, 32, None) == 1
     assert _call(libw4, "fp4_moe_gemv", A, A, A, A, 2, A, 4, 8, 96, 32, None) == 1
     assert _call(libw4, "fp4_moe_gemv", A, A, A, A + 2, 2, A, 4, 8, 128, 32, None) == 3
@@ -101,11 +101,10 @@ def test_sequence_and_graph_host_validation(libw4):
     assert _call(libw4, "w4a16_linear_sequence", ops, 3, 128, None) == 1
     assert "op 2" in _call(libw4, "w4a16_last_error_string").decode()
     ops[2].K = 384
-    ops[0].N = 24                       # M = 1: the GEMV's rules, any N
-    ops[1].N = 24                       # M > 1: the GEMM's rules, N % 16
+    ops[1].K = 32768                    # M > 1: the GEMM's rules, K <= 16384
     assert _call(libw4, "w4a16_linear_sequence", ops, 3, 128, None) == 2
     assert "op 1" in _call(libw4, "w4a16_last_error_string").decode()
-    ops[1].N = 32
+    ops[1].K = 256
     ops[1].y = A + 8
     assert _call(libw4, "w4a16_linear_sequence", ops, 3, 128, None) == 3
     ops[1].y = A

@@ -27,6 +27,18 @@ def test_gemm_small_and_ragged(M, N, K):
     assert_close(_run(w4, torch, p), ref, "gemm %dx%dx%d" % (M, N, K))
 
 
+# small batches on the tensor cores (M = 9..63) and N of any size: odd N with
+# an odd group count, so the tile's scale and zero rows end inside a 16-byte
+# chunk that must be zero-filled past the tensors' end
+@pytest.mark.parametrize("M,N,K", [(9, 113, 384), (16, 225, 640), (31, 1001, 1920), (33, 7, 256),
+                                   (63, 337, 3840), (130, 241, 384), (64, 15360, 3840)])
+def test_gemm_small_m_and_any_n(M, N, K):
+    torch, w4 = cuda_or_skip()
+    p = synth.int4_problem(N, K, M=M, seed=M * 13 + N + K)
+    ref = oracle.gemm_int4(p["x"], p["qw"], p["s"], p["z"], K=K)
+    assert_close(_run(w4, torch, p), ref, "gemm %dx%dx%d" % (M, N, K))
+
+
 @pytest.mark.parametrize("M", [128, 2048])
 def test_gemm_full_size_sampled(M):
     # M x 15360 x 3840 on the GPU; the oracle checks sampled rows and columns
