@@ -17,7 +17,9 @@ What it computes (page titles as published):
     in GPTQ's form: z = None means the implicit zero point 8;
   * the OCP MX definition of E2M1 for the FP4 value table;
   * the dense BF16 product of the unfused two-pass path ("Triton dequant +
-    cuBLAS"), for the fusion ablation.
+    cuBLAS"), for the fusion ablation;
+  * the batched-expert FP4 GEMM for M tokens routed to topk experts each (the
+    pages' FP4 expert GEMMs at M > 1).
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against
 hand-written fixtures, closed forms, brute force and library routines.
@@ -85,6 +87,9 @@ def _load():
         lib.oracle_moe_fp4.restype = None
         lib.oracle_gemm_bf16.argtypes = [P, P, I64, I64, I64, P]
         lib.oracle_gemm_bf16.restype = None
+        lib.oracle_moe_fp4_gemm.argtypes = [P, P, P, P, I64, I64, I64, I64, I64, I64, P,
+                                            ctypes.POINTER(ctypes.c_int)]
+        lib.oracle_moe_fp4_gemm.restype = None
         lib.oracle_set_threads.argtypes = [ctypes.c_int]
         lib.oracle_set_threads.restype = None
         _lib = lib
@@ -226,6 +231,27 @@ def moe_fp4(x, qw, s, ids, E: int, N: int, K: int, group: int = 32):
     bad = ctypes.c_int(0)
     _load().oracle_moe_fp4(_ptr(x), _ptr(qw), _ptr(s), _ptr(ids), topk, E, N,
                            K, group, _ptr(Y), ctypes.byref(bad))
+    return Y, int(bad.value)
+
+
+def moe_fp4_gemm(X, qw, s, ids, E: int, N: int, K: int, group: int = 32):
+    """Y[M, topk, N] (float64) and the count of ids outside [0, E).
+
+    X: bfloat16 bits [M, K]; ids: [M, topk] expert ids (row (m, j) of Y uses
+    expert ids[m, j]); qw the [E, N, K/2] expert stack, s its [E, N, K/group]
+    scales."""
+    X = _c(np.asarray(X).reshape(-1, K), np.uint16)
+    M = X.shape[0]
+    ids = _c(np.asarray(ids, dtype=np.int32).reshape(M, -1), np.int32)
+    topk = ids.shape[1]
+    qw = _c(qw, np.uint8)
+    s = _c(s, np.uint16)
+    if qw.size != E * N * (K // 2) or s.size != E * N * (K // group):
+        raise ValueError("inconsistent MoE shapes")
+    Y = np.empty((M, topk, N), dtype=np.float64)
+    bad = ctypes.c_int(0)
+    _load().oracle_moe_fp4_gemm(_ptr(X), _ptr(qw), _ptr(s), _ptr(ids), M, topk, E, N,
+                                K, group, _ptr(Y), ctypes.byref(bad))
     return Y, int(bad.value)
 
 

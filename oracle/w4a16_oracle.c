@@ -238,6 +238,47 @@ void oracle_moe_fp4(const uint16_t *x, const uint8_t *qw, const uint16_t *s,
     }
 }
 
+/* Batched-expert FP4 GEMM for M tokens ([DSV4] the fused FP4 expert GEMMs:
+ * every token is routed to topk experts, each a separate weight matrix; M > 1
+ * is the prefill / batched case).  Output row (m, j) uses expert
+ * ids[m*topk + j]: y[m, j, n] = sum_k X[m, k] * W_{ids[m*topk+j]}[n, k], with
+ * W_e the binary32 values of oracle_dequant_fp4 on expert e's slice, every
+ * product and the running sum in binary64, k ascending.
+ * X: [M, K] bfloat16; ids: [M, topk]; qw: [E, N, K/2]; s: [E, N, K/g];
+ * Y: [M, topk, N] binary64.  An id outside [0, E) gives a zero row and
+ * increments *bad. */
+void oracle_moe_fp4_gemm(const uint16_t *X, const uint8_t *qw, const uint16_t *s,
+                         const int32_t *ids, int64_t M, int64_t topk, int64_t E,
+                         int64_t N, int64_t K, int64_t g, double *Y, int *bad)
+{
+    int64_t G = K / g;
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t j = 0; j < topk; ++j) {
+            int64_t e = ids[m * topk + j];
+            double *y = Y + (m * topk + j) * N;
+            if (e < 0 || e >= E) {
+                for (int64_t n = 0; n < N; ++n)
+                    y[n] = 0.0;
+                if (bad)
+                    *bad += 1;
+                continue;
+            }
+#pragma omp parallel for schedule(static) num_threads(g_threads) if (g_threads > 1)
+            for (int64_t n = 0; n < N; ++n) {
+                int64_t r = e * N + n;   /* row of the [E*N, K] stack */
+                double acc = 0.0;
+                for (int64_t k = 0; k < K; ++k) {
+                    float v = (float)oracle_e2m1_value(oracle_code(qw, K, r, k));
+                    float sf = (float)oracle_f16_to_f64(s[r * G + k / g]);
+                    float w = v * sf;
+                    acc += (double)w * oracle_bf16_to_f64(X[m * K + k]);
+                }
+                y[n] = acc;
+            }
+        }
+    }
+}
+
 /* ---------------------------------------------------- two-pass ablation */
 
 /* Dense product of bfloat16 matrices, the second pass of the unfused path

@@ -26,7 +26,7 @@ import numpy as np
 
 __all__ = [
     "Stream", "packed_codes", "uniform_f16", "int_f16", "normal_bf16",
-    "sample_experts", "int4_problem", "fp4_moe_problem", "CONFIGS",
+    "sample_experts", "int4_problem", "fp4_moe_problem", "fp4_moe_batch_problem", "CONFIGS",
 ]
 
 
@@ -118,6 +118,23 @@ def fp4_moe_problem(E: int, N: int, K: int, topk: int, group: int = 32,
     x = normal_bf16(st, (K,))
     ids = sample_experts(st, E, topk)
     return {"qw": qw, "s": s, "x": x, "ids": ids, "E": E, "N": N, "K": K,
+            "topk": topk, "group": group}
+
+
+def fp4_moe_batch_problem(E: int, N: int, K: int, M: int, topk: int, group: int = 32,
+                          seed: int = 0, s_range=(0.01, 0.1)) -> dict:
+    """FP4 E2M1 expert stack, per-group FP16 scales and M BF16 tokens, each
+    routed to topk distinct experts.
+
+    qw uint8 [E, N, K/2]; s FP16 bits [E, N, K/group]; X BF16 bits [M, K];
+    ids int32 [M, topk] (row m: the experts of token m, sampled without
+    replacement)."""
+    st = Stream(seed)
+    qw = packed_codes(st, E * N, K).reshape(E, N, K // 2)
+    s = uniform_f16(st, (E, N, K // group), *s_range)
+    X = normal_bf16(st, (M, K))
+    ids = np.stack([sample_experts(st, E, topk) for _ in range(M)]).astype(np.int32)
+    return {"qw": qw, "s": s, "x": X, "ids": ids, "E": E, "N": N, "K": K, "M": M,
             "topk": topk, "group": group}
 
 

@@ -31,6 +31,8 @@ MUTATIONS = {
     "symmetric_zero_point": ("z ? (float)oracle_f16_to_f64(z[n * G + k / g]) : 8.0f;\n                float sf",
                              "z ? (float)oracle_f16_to_f64(z[n * G + k / g]) : 7.0f;\n                float sf"),
     "bf16_weight_transposed": ("oracle_bf16_to_f64(W[n * K + k])", "oracle_bf16_to_f64(W[k * N + n])"),
+    "moe_gemm_id_index": ("int64_t e = ids[m * topk + j];", "int64_t e = ids[j * M + m];"),
+    "moe_gemm_output_row": ("double *y = Y + (m * topk + j) * N;", "double *y = Y + (j * M + m) * N;"),
     "fp4_scale_index": ("s[r * G + k / g]);\n            W[r * K + k] = v * sf;",
                         "s[r * G]);\n            W[r * K + k] = v * sf;"),
 }

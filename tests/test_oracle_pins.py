@@ -338,6 +338,56 @@ def test_moe_equals_per_expert_dequantise_then_matvec():
         assert np.allclose(Y[i], ref, rtol=1e-12, atol=1e-12)
 
 
+def test_moe_gemm_closed_form_per_token_and_slot():
+    """All codes 1.0 and scales (e+1)(n+1)(j+1)/64: every output row (m, slot)
+    is (e+1)(n+1)/64 times the token's own weighted sum, e = its expert."""
+    rng = np.random.default_rng(13)
+    E, N, K, g, qw, s = _moe_closed_form_case()
+    M = 3
+    X = np.stack([rand_bf16(rng, K) for _ in range(M)])
+    ids = np.array([[4, 0], [2, 2], [1, 3]], np.int32)
+    Y, bad = oracle.moe_fp4_gemm(X, qw, s, ids, E=E, N=N, K=K, group=g)
+    assert bad == 0 and Y.shape == (M, 2, N)
+    for m in range(M):
+        xv = bf16_vals(X[m])
+        base = math.fsum(xv[:32]) + 2.0 * math.fsum(xv[32:])
+        for j in range(2):
+            for n in range(N):
+                assert math.isclose(Y[m, j, n], (ids[m, j] + 1) * (n + 1) / 64.0 * base,
+                                    rel_tol=1e-12, abs_tol=1e-12)
+
+
+def test_moe_gemm_equals_dequantise_then_matmul():
+    rng = np.random.default_rng(14)
+    E, N, K, g = 5, 7, 128, 32
+    qw = rng.integers(0, 256, size=(E, N, K // 2), dtype=np.uint8)
+    s = f16_arr(rng.uniform(0.01, 0.1, size=(E, N, K // g)))
+    M = 4
+    X = np.stack([rand_bf16(rng, K) for _ in range(M)])
+    ids = np.array([[0, 4], [3, 1], [1, 1], [2, 0]], np.int32)
+    Y, bad = oracle.moe_fp4_gemm(X, qw, s, ids, E=E, N=N, K=K, group=g)
+    assert bad == 0
+    W = oracle.dequant_fp4(qw, s, K=K, group=g).reshape(E, N, K).astype(np.float64)
+    for m in range(M):
+        for j in range(2):
+            assert np.allclose(Y[m, j], W[ids[m, j]] @ bf16_vals(X[m]), rtol=1e-12, atol=1e-12)
+
+
+def test_moe_gemm_out_of_range_ids_zero_rows_and_single_token_reduction():
+    rng = np.random.default_rng(15)
+    E, N, K, g, qw, s = _moe_closed_form_case()
+    X = np.stack([rand_bf16(rng, K) for _ in range(2)])
+    ids = np.array([[1, 5], [-1, 0]], np.int32)
+    Y, bad = oracle.moe_fp4_gemm(X, qw, s, ids, E=E, N=N, K=K, group=g)
+    assert bad == 2
+    assert np.all(Y[0, 1] == 0.0) and np.all(Y[1, 0] == 0.0)
+    assert np.all(Y[0, 0] != 0.0) and np.all(Y[1, 1] != 0.0)
+    # one token: the batched definition is the single-token one, bit for bit
+    y1, _ = oracle.moe_fp4(X[1], qw, s, np.array([0, 2], np.int32), E=E, N=N, K=K, group=g)
+    Yb, _ = oracle.moe_fp4_gemm(X[1:], qw, s, np.array([[0, 2]], np.int32), E=E, N=N, K=K, group=g)
+    assert np.array_equal(Yb[0].view(np.uint64), y1.view(np.uint64))
+
+
 @pytest.mark.parametrize("byte", [0x00, 0x5A, 0xA5, 0xFF])
 def test_dequant_fp4_matches_table_for_every_byte_pair(byte):
     table = {int(c): float(v) for c, v in read_golden("e2m1_table.txt")}

@@ -40,3 +40,12 @@ def test_expert_sampling_without_replacement():
     for seed in range(200):
         seen.update(synth.sample_experts(synth.Stream(seed), 64, 6).tolist())
     assert len(seen) == 64
+
+
+def test_moe_batch_problem_routes_each_token_to_distinct_experts():
+    p = synth.fp4_moe_batch_problem(E=16, N=8, K=64, M=5, topk=4, seed=3)
+    q = synth.fp4_moe_batch_problem(E=16, N=8, K=64, M=5, topk=4, seed=3)
+    assert p["ids"].shape == (5, 4) and p["x"].shape == (5, 64)
+    assert all(len(set(row.tolist())) == 4 for row in p["ids"])
+    assert p["ids"].min() >= 0 and p["ids"].max() < 16
+    assert all(np.array_equal(p[k], q[k]) for k in ("qw", "s", "x", "ids"))
