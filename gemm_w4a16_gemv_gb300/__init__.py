@@ -19,7 +19,8 @@ import threading
 import torch
 
 __all__ = [
-    "w4a16_gemv", "w4a16_gemm", "fp4_moe_gemv", "w4a16_dequant", "w4a16_bf16_gemm",
+    "w4a16_gemv", "w4a16_gemm", "fp4_moe_gemv", "fp4_moe_gemm", "fp4_moe_gemm_scratch_bytes",
+    "w4a16_dequant", "w4a16_bf16_gemm",
     "w4a16_check_device_error", "w4a16_last_error_string", "w4a16_version",
     "w4a16_debug_inject", "INJECT_STALL_PIPELINE", "INJECT_STALL_CONSUMERS",
     "w4a16_linear", "w4a16_linear_array", "w4a16_linear_sequence", "w4a16_graph_create", "w4a16_graph_launch",
@@ -58,6 +59,8 @@ SIGNATURES = {
     "w4a16_gemm": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _INT, _P], _INT),
     "w4a16_bf16_gemm": ([_P, _P, _P, _I64, _I64, _I64, _P], _INT),
     "fp4_moe_gemv": ([_P, _P, _P, _P, _INT, _P, _I64, _I64, _I64, _INT, _P], _INT),
+    "fp4_moe_gemm": ([_P, _P, _P, _P, _INT, _INT, _P, _I64, _I64, _I64, _INT, _P, _I64, _P], _INT),
+    "fp4_moe_gemm_scratch_bytes": ([_INT, _INT, _I64, _I64], _I64),
     "w4a16_dequant": ([_INT, _P, _P, _P, _P, _INT, _I64, _I64, _INT, _P], _INT),
     "w4a16_linear_sequence": ([_OPS, _INT, _INT, _P], _INT),
     "w4a16_linear_chain": ([_OPS, _INT, _INT, _P, _I64, _P], _INT),
@@ -202,6 +205,40 @@ def fp4_moe_gemv(x, qw, s, expert_ids, y=None, group: int = 32, stream=None):
     with torch.cuda.device(dev):  # the library launches on the current device
         _check(lib().fp4_moe_gemv(px, pq, ps, pi, topk, py, E, N, K, group, _stream(stream, dev)))
     return y
+
+
+def fp4_moe_gemm_scratch_bytes(M: int, topk: int, E: int, K: int) -> int:
+    """Bytes of scratch memory fp4_moe_gemm needs for M tokens x topk."""
+    return int(lib().fp4_moe_gemm_scratch_bytes(int(M), int(topk), int(E), int(K)))
+
+
+def fp4_moe_gemm(X, qw, s, expert_ids, Y=None, scratch=None, group: int = 32, stream=None):
+    """Y[M, topk, N]: Y[m, j] = X[m] W_{expert_ids[m, j]}^T for the FP4 stack
+    qw [E, N, K/2].  `scratch`: a device tensor of at least
+    fp4_moe_gemm_scratch_bytes(M, topk, E, K) bytes (allocated per call when
+    None)."""
+    E, N = qw.shape[0], qw.shape[1]
+    K = 2 * qw.shape[2]
+    M = X.numel() // K if K else 0
+    topk = expert_ids.numel() // M if M else 0
+    dev = qw.device
+    pX = _need(X, "X", torch.bfloat16, M * K, dev)
+    pq = _need(qw, "qw", torch.uint8, E * N * K // 2, dev)
+    ps = _need(s, "s", torch.float16, E * N * (K // group), dev)
+    pi = _need(expert_ids, "expert_ids", torch.int32, M * topk, dev)
+    if Y is None:
+        Y = torch.empty(M, topk, N, dtype=torch.bfloat16, device=dev)
+    pY = _need(Y, "Y", torch.bfloat16, M * topk * N, dev)
+    need = fp4_moe_gemm_scratch_bytes(M, topk, E, K)
+    if scratch is None:
+        scratch = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    if not isinstance(scratch, torch.Tensor) or scratch.device != dev or not scratch.is_contiguous():
+        raise ValueError("scratch must be a contiguous CUDA tensor on %s" % dev)
+    nbytes = scratch.numel() * scratch.element_size()
+    with torch.cuda.device(dev):  # the library launches on the current device
+        _check(lib().fp4_moe_gemm(pX, pq, ps, pi, M, topk, pY, E, N, K, group,
+                                  ctypes.c_void_p(scratch.data_ptr()), nbytes, _stream(stream, dev)))
+    return Y
 
 
 def w4a16_dequant(fmt: int, qw, s, z=None, out=None, out_dtype: int = OUT_F32,

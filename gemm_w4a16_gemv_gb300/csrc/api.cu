@@ -451,6 +451,42 @@ int fp4_moe_gemv(const uint16_t *x, const uint8_t *qw, const uint16_t *s,
                     "fp4_moe_gemv");
 }
 
+int64_t fp4_moe_gemm_scratch_bytes(int M, int topk, int64_t E, int64_t K) {
+    if (M < 1 || topk < 1 || E < 1 || K < 1) return 0;
+    return w4::moe_fp4_gemm_scratch(static_cast<int64_t>(M) * topk, E, K);
+}
+
+int fp4_moe_gemm(const uint16_t *X, const uint8_t *qw, const uint16_t *s, const int32_t *expert_ids, int M,
+                 int topk, uint16_t *Y, int64_t E, int64_t N, int64_t K, int group, void *scratch,
+                 int64_t scratch_bytes, void *stream) {
+    const char *fn = "fp4_moe_gemm";
+    if (!X || !qw || !s || !expert_ids || !Y || !scratch) return fail(W4A16_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (M < 1 || topk < 1 || E < 1 || N < 1 || K < 1)
+        return fail(W4A16_ERR_INVALID_ARG, "%s: M=%d topk=%d E=%lld N=%lld K=%lld must be >= 1", fn, M, topk,
+                    (long long)E, (long long)N, (long long)K);
+    if (group != 32) return fail(W4A16_ERR_UNSUPPORTED, "%s: group %d (only 32)", fn, group);
+    if (K % 256 != 0) return fail(W4A16_ERR_UNSUPPORTED, "%s: K=%lld not a multiple of 256", fn, (long long)K);
+    if (K > 65536 || E > 8192 || E * N > (int64_t(1) << 31) - 128 || static_cast<int64_t>(M) * topk > (1 << 20))
+        return fail(W4A16_ERR_UNSUPPORTED, "%s: sizes too large", fn);
+    if (!aligned16(X) || !aligned16(qw) || !aligned16(s) || !aligned16(Y))
+        return fail(W4A16_ERR_MISALIGNED, "%s: pointers must be 16-byte aligned", fn);
+    if ((reinterpret_cast<uintptr_t>(expert_ids) & 3u) != 0)
+        return fail(W4A16_ERR_MISALIGNED, "%s: expert_ids must be 4-byte aligned", fn);
+    if ((reinterpret_cast<uintptr_t>(scratch) & 255u) != 0)
+        return fail(W4A16_ERR_MISALIGNED, "%s: scratch must be 256-byte aligned", fn);
+    const int64_t need = w4::moe_fp4_gemm_scratch(static_cast<int64_t>(M) * topk, E, K);
+    if (scratch_bytes < need)
+        return fail(W4A16_ERR_INVALID_ARG, "%s: scratch of %lld bytes, %lld needed", fn, (long long)scratch_bytes,
+                    (long long)need);
+    w4::DeviceInfo dev;
+    unsigned int *status;
+    if (int r = device_state(dev, status)) return r;
+    if (int r = check_device_ptrs(fn, dev.device, {X, qw, s, expert_ids, Y, scratch})) return r;
+    return launched(w4::launch_moe_fp4_gemm(X, qw, s, expert_ids, M, topk, Y, E, N, K, scratch,
+                                            static_cast<cudaStream_t>(stream), status, dev),
+                    fn);
+}
+
 int w4a16_dequant(int fmt, const uint8_t *qw, const uint16_t *s,
                   const uint16_t *z, void *out, int out_dtype, int64_t rows,
                   int64_t K, int group, void *stream) {

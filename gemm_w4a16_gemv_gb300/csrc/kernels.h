@@ -83,6 +83,13 @@ void gemv_chain_shape(int64_t K, unsigned char &tt_log2, unsigned char &rpt);
 cudaError_t launch_gemv_chain(const ChainOp *ops, int count, unsigned int *done, cudaStream_t st,
                               unsigned int *status, const DeviceInfo &dev);
 
+// Batched-expert FP4 GEMM (M tokens x topk experts): scratch bytes needed
+// for P = M * topk pairs, and the three launches (route, gather, GEMM).
+int64_t moe_fp4_gemm_scratch(int64_t P, int64_t E, int64_t K);
+cudaError_t launch_moe_fp4_gemm(const uint16_t *X, const uint8_t *qw, const uint16_t *s, const int32_t *ids, int M,
+                                int topk, uint16_t *Y, int64_t E, int64_t N, int64_t K, void *scratch,
+                                cudaStream_t st, unsigned int *status, const DeviceInfo &dev);
+
 cudaError_t launch_moe_fp4(const uint16_t *x, const uint8_t *qw,
                            const uint16_t *s, const int32_t *ids, int topk,
                            uint16_t *y, int64_t E, int64_t N, int64_t K,

@@ -1,0 +1,509 @@
+// Batched-expert FP4 GEMM for M tokens, each routed to topk experts
+// ("DeepSeek V4 Triton FP4 optimisation in practice": the fused FP4
+// dequantise-and-multiply expert GEMMs; M > 1 is the prefill / batched case):
+//
+//   Y[m, j, n] = sum_k X[m, k] * e2m1(q[e, n, k]) * s[e, n, k/32],  e = ids[m, j]
+//
+// Three launches on the caller's stream, all state in caller scratch memory:
+//  1. route (one CTA): counts the (token, slot) pairs of each expert, gives
+//     every valid pair a position in its expert's contiguous row list, and
+//     writes the tile table (an expert's rows in tiles of up to 128); an id
+//     outside [0, E) sets the device status;
+//  2. gather: copies each routed token row into the scratch as binary16,
+//     scaled by a power of two per token so that its largest |x| lands in
+//     [2^14, 2^15) (exact for every value within 2^29 of that maximum); the
+//     output rows of invalid ids are written as zeros;
+//  3. the GEMM on the tcgen05 tensor cores: one CTA per (tile, 128 weight
+//     rows).  Builder warps decode the E2M1 codes exactly to binary16
+//     (cvt.rn.f16x2.e2m1x2) and multiply by the group scale in binary16 --
+//     the weight e2m1 * s rounded once to binary16, a relative error of at
+//     most 2^-11 (the only rounding of the operands) -- into the A operand in
+//     tensor memory; the gathered token rows are the B operand (TMA, 128-byte
+//     swizzle); one FP32 accumulator over all of K; the epilogue undoes each
+//     token's power-of-two scale, rounds to BF16 and scatters the rows to
+//     their (token, slot) places.
+// Every wait is bounded; on a timeout the status word is set, each role
+// still performs the arrivals the others wait for, and tensor memory is
+// released only after the MMAs issued have completed.
+#include "common.cuh"
+#include "gemv_common.cuh"
+#include "kernels.h"
+#include "tc_common.cuh"
+#include "tma_host.h"
+
+namespace w4 {
+namespace {
+
+constexpr int BR = 128;               // weight rows per CTA (the MMA's M; TMEM lanes)
+constexpr int BT = 128;               // token rows per tile at most (the MMA's N)
+constexpr int CK = 128;               // K per chunk: one A stage, one X stage
+constexpr int SCK = 256;              // K per weight stage: 128 code bytes and 8 scales per row
+constexpr int XS = 3;                 // X stages
+constexpr int WS = 2;                 // weight stages (codes + scales)
+constexpr int AP = 4;                 // TMEM operand stages (64 columns each)
+constexpr int X_BOX_ROWS = 16;        // rows per X TMA box (a tile loads as many boxes as it needs)
+constexpr int X_STAGE = BT * CK * 2;  // 32 KB: two 64-K boxes of up to 128 rows
+constexpr int W_STAGE = BR * 128;     // 16 KB of packed codes
+constexpr int S_STAGE = BR * 16;      // 2 KB of scales
+constexpr int THREADS = 384;          // 12 warps: 0 weights TMA, 1 tokens TMA, 2 MMA, 3 idle, 4-11 builders
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TM_ACC = 0;        // accumulator: columns 0 .. BT-1
+constexpr uint32_t TM_A = 128;        // operand stages after it
+constexpr int ROUTE_THREADS = 1024;
+constexpr int GATHER_THREADS = 256;
+
+struct MoeTile {
+    int expert;
+    int row0;   // first row of the tile in the gathered list
+    int rows;   // 1 .. BT
+    int pad;
+};
+
+// Scratch layout (byte offsets, 256-aligned), a function of P = M * topk,
+// E and K only.
+struct MoeScratch {
+    int64_t tiles_off, perm_off, posof_off, scale_off, xg_off, total;
+    int tmax;
+};
+
+__host__ __device__ inline int64_t align256(int64_t v) { return (v + 255) & ~int64_t(255); }
+
+__host__ __device__ inline MoeScratch moe_scratch_layout(int64_t P, int64_t E, int64_t K) {
+    MoeScratch l;
+    l.tmax = static_cast<int>((P + BT - 1) / BT + (E < P ? E : P));
+    l.tiles_off = 256;  // the tile count lives at offset 0
+    l.perm_off = align256(l.tiles_off + 16 * static_cast<int64_t>(l.tmax));
+    l.posof_off = align256(l.perm_off + 4 * P);
+    l.scale_off = align256(l.posof_off + 4 * P);
+    l.xg_off = align256(l.scale_off + 4 * P);
+    l.total = align256(l.xg_off + 2 * P * K);
+    return l;
+}
+
+// ------------------------------------------------------------ 1. routing
+// One CTA.  cnt[e]: pairs of expert e; off[e]: first position of its rows.
+__global__ void __launch_bounds__(ROUTE_THREADS) moe_route_kernel(const int32_t *__restrict__ ids, int P, int E,
+                                                                  unsigned char *scratch, unsigned int *status) {
+    extern __shared__ int sm[];
+    int *cnt = sm;           // [E]
+    int *off = sm + E;       // [E]
+    int *cur = sm + 2 * E;   // [E]
+    __shared__ int ntiles;
+    const MoeScratch l = moe_scratch_layout(P, E, 0);
+    MoeTile *tiles = reinterpret_cast<MoeTile *>(scratch + l.tiles_off);
+    int *perm = reinterpret_cast<int *>(scratch + l.perm_off);
+    int *posof = reinterpret_cast<int *>(scratch + l.posof_off);
+    pdl_wait();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = cur[e] = 0;
+    __syncthreads();
+    bool bad = false;
+    for (int p = threadIdx.x; p < P; p += blockDim.x) {
+        const int e = ids[p];
+        if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+        else bad = true;
+    }
+    if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(status, kDevBadExpert);
+    if (threadIdx.x == 0) {
+        // exclusive prefix sum and the tile table, experts in order
+        int acc = 0, t = 0;
+        for (int e = 0; e < E; ++e) {
+            off[e] = acc;
+            for (int r = 0; r < cnt[e]; r += BT) {
+                MoeTile tl;
+                tl.expert = e;
+                tl.row0 = acc + r;
+                tl.rows = cnt[e] - r < BT ? cnt[e] - r : BT;
+                tl.pad = 0;
+                tiles[t++] = tl;
+            }
+            acc += cnt[e];
+        }
+        ntiles = t;
+        *reinterpret_cast<int *>(scratch) = t;
+    }
+    __syncthreads();
+    // positions: within an expert in arrival order (each output row is
+    // computed on its own, so the order does not change any result)
+    for (int p = threadIdx.x; p < P; p += blockDim.x) {
+        const int e = ids[p];
+        int pos = -1;
+        if (e >= 0 && e < E) {
+            pos = off[e] + atomicAdd(&cur[e], 1);
+            perm[pos] = p;
+        }
+        posof[p] = pos;
+    }
+}
+
+// --------------------------------------------------------- 2. gathering
+// One CTA per (token, slot) pair p = m * topk + j.
+__global__ void __launch_bounds__(GATHER_THREADS) moe_gather_kernel(const uint16_t *__restrict__ X, int topk, int P,
+                                                                    int E, int K, int64_t N, uint16_t *Y,
+                                                                    unsigned char *scratch) {
+    const MoeScratch l = moe_scratch_layout(P, E, K);
+    const int p = blockIdx.x;
+    const int pos = reinterpret_cast<const int *>(scratch + l.posof_off)[p];
+    if (pos < 0) {
+        // an expert id out of range: its output row is zeros
+        for (int64_t n = threadIdx.x; n < N; n += blockDim.x) Y[p * N + n] = 0;
+        return;
+    }
+    const uint16_t *x = X + static_cast<int64_t>(p / topk) * K;
+    // largest |x| of the token (BF16 magnitude bit patterns order as values)
+    __shared__ uint32_t red[GATHER_THREADS / 32];
+    uint32_t m = 0;
+    for (int k = threadIdx.x; k < K; k += blockDim.x) m = max(m, static_cast<uint32_t>(x[k]) & 0x7FFFu);
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, d));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    m = 0;
+#pragma unroll
+    for (int w = 0; w < GATHER_THREADS / 32; ++w) m = max(m, red[w]);
+    const int e = exponent_of_absmax(m);  // 2^e <= max|x| < 2^(e+1)
+    const float inv = pow2f(14 - e);      // max|x| * inv in [2^14, 2^15): binary16 holds it
+    __half *xg = reinterpret_cast<__half *>(scratch + l.xg_off) + static_cast<int64_t>(pos) * K;
+    for (int k = threadIdx.x; k < K; k += blockDim.x) xg[k] = __float2half_rn(bf16_bits_to_f32(x[k]) * inv);
+    if (threadIdx.x == 0) reinterpret_cast<float *>(scratch + l.scale_off)[pos] = pow2f(e - 14);
+}
+
+// --------------------------------------------------------------- 3. GEMM
+struct MoeGemmArgs {
+    const unsigned char *scratch;
+    uint16_t *Y;
+    unsigned int *status;
+    int P, E, N, K, nchunks;
+    int off_w, off_s, off_bar;  // byte offsets in shared memory (X stages at 0)
+    unsigned int inject;
+};
+
+struct MoeBarriers {
+    uint64_t xfull[XS], xempty[XS];
+    uint64_t wfull[WS], wempty[WS];
+    uint64_t aready[AP], aempty[AP];
+    uint64_t accfull;
+    uint64_t done;      // builders finished with tensor memory
+    uint64_t drained;   // every MMA completed
+    uint32_t tmem_holder;
+};
+
+// Two E2M1 codes (the low byte of b) times a binary16 scale pair -> binary16
+// pair, low half from the low nibble (even k): decode exact, one rounding.
+__device__ __forceinline__ uint32_t e2m1x2_times(uint32_t b, uint32_t s2) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 t;\n\t.reg .b32 h;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 h, t;\n\t"
+        "mul.rn.f16x2 %0, h, %2;\n\t}"
+        : "=r"(r)
+        : "r"(b), "r"(s2));
+    return r;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+moe_fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS,
+                    const __grid_constant__ CUtensorMap tmX, const MoeGemmArgs a) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    MoeBarriers &bar = *reinterpret_cast<MoeBarriers *>(smem + a.off_bar);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // the tile: read after the routing launch has finished (stream order)
+    pdl_wait();
+    const MoeScratch l = moe_scratch_layout(a.P, a.E, a.K);
+    const int ntiles = *reinterpret_cast<const int *>(a.scratch);
+    if (static_cast<int>(blockIdx.x) >= ntiles) return;  // uniform over the CTA
+    const MoeTile tile = reinterpret_cast<const MoeTile *>(a.scratch + l.tiles_off)[blockIdx.x];
+    const int n0 = blockIdx.y * BR;
+    const int wrow0 = tile.expert * a.N + n0;               // first weight row in the [E*N] stack
+    const int nmma = ((tile.rows + 15) / 16) * 16;          // the MMA's N
+    const int xboxes = nmma / X_BOX_ROWS;
+    const int nch = a.nchunks;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < XS; ++i) {
+            mbar_init(&bar.xfull[i], 1);
+            mbar_init(&bar.xempty[i], 1);
+        }
+        for (int i = 0; i < WS; ++i) {
+            mbar_init(&bar.wfull[i], 1);
+            mbar_init(&bar.wempty[i], 8);  // the 8 builder warps
+        }
+        for (int i = 0; i < AP; ++i) {
+            mbar_init(&bar.aready[i], 4);  // the 4 builder warps of the chunk's parity
+            mbar_init(&bar.aempty[i], 1);
+        }
+        mbar_init(&bar.accfull, 1);
+        mbar_init(&bar.done, 8);
+        mbar_init(&bar.drained, 1);
+        fence_barrier_init();
+    }
+    if (warp == 2) {  // the MMA warp allocates tensor memory and frees it at the end
+        tmem_alloc(&bar.tmem_holder, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bar.tmem_holder;
+
+    if (warp == 0) {
+        // ---------------------------------------- codes and scales (TMA)
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            tma_prefetch_desc(&tmW);
+            tma_prefetch_desc(&tmS);
+            const int nsc = (nch + 1) / 2;
+            const int nissue = (a.inject & kInjectStallPipeline) ? 0 : nsc;
+            int issued = 0;
+            for (int sc = 0; sc < nissue; ++sc, ++issued) {
+                const int ws = sc % WS;
+                if (sc >= WS && !mbar_wait(&bar.wempty[ws], ((sc / WS) - 1) & 1, a.status)) break;
+                mbar_arrive_expect_tx(&bar.wfull[ws], W_STAGE + S_STAGE);
+                // rows past the stack's end read as zeros; rows of the next
+                // expert (tiles ending past N) are computed and not stored
+                tma_load_2d_hint(smem + a.off_w + ws * W_STAGE, &tmW, sc * 128, wrow0, &bar.wfull[ws], pol);
+                tma_load_2d_hint(smem + a.off_s + ws * S_STAGE, &tmS, sc * 8, wrow0, &bar.wfull[ws], pol);
+            }
+            // no copy in flight when the CTA exits
+            for (int it = issued > WS ? issued - WS : 0; it < issued; ++it)
+                mbar_wait(&bar.wfull[it % WS], (it / WS) & 1, nullptr);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------ token rows (TMA)
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_last();
+            tma_prefetch_desc(&tmX);
+            const int nissue = (a.inject & kInjectStallPipeline) ? 0 : nch;
+            int issued = 0;
+            for (int c = 0; c < nissue; ++c, ++issued) {
+                const int xs = c % XS;
+                if (c >= XS && !mbar_wait(&bar.xempty[xs], ((c / XS) - 1) & 1, a.status)) break;
+                mbar_arrive_expect_tx(&bar.xfull[xs], 2 * xboxes * X_BOX_ROWS * 128);
+                unsigned char *dst = smem + xs * X_STAGE;
+                for (int h = 0; h < 2; ++h)          // the chunk's two 64-K boxes
+                    for (int b = 0; b < xboxes; ++b)  // 16 rows each
+                        tma_load_2d_hint(dst + h * (X_STAGE / 2) + b * X_BOX_ROWS * 128, &tmX, c * CK + h * 64,
+                                         tile.row0 + b * X_BOX_ROWS, &bar.xfull[xs], pol);
+            }
+            for (int it = issued > XS ? issued - XS : 0; it < issued; ++it)
+                mbar_wait(&bar.xfull[it % XS], (it / XS) & 1, nullptr);
+        }
+    } else if (warp == 2) {
+        // -------------------------------------------------- MMA issuer
+        const uint32_t idesc = idesc_kind_f16(BR, nmma, 0u);  // FP16 x FP16 -> FP32, M = 128, N = nmma
+        bool ok = !(a.inject & kInjectStallConsumers);
+        for (int c = 0; ok && c < nch; ++c) {
+            const int ap = c % AP, xs = c % XS;
+            uint64_t *wbar = nullptr;
+            uint32_t par = 0;
+            if (lane == 0) {
+                wbar = &bar.aready[ap];
+                par = (c / AP) & 1;
+            } else if (lane == 1) {
+                wbar = &bar.xfull[xs];
+                par = (c / XS) & 1;
+            }
+            if (!mbar_wait_lanes(wbar, par, a.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t b_addr = smem_u32(smem + xs * X_STAGE);
+#pragma unroll
+                for (int k = 0; k < CK / 16; ++k)
+                    umma_f16_tmem_a(tmem + TM_ACC, tmem + TM_A + ap * 64 + 8 * k,
+                                    smem_desc_sw128_kmajor(b_addr + (k >> 2) * (X_STAGE / 2) + 32 * (k & 3)), idesc,
+                                    (c | k) != 0);
+                umma_commit(&bar.xempty[xs]);
+                umma_commit(&bar.aempty[ap]);
+            }
+            __syncwarp();
+        }
+        // the accumulator is complete once every MMA issued has completed (on
+        // a timeout: the epilogue's wait ends as well, with garbage it does
+        // not store)
+        if (lane == 0) {
+            umma_commit(&bar.accfull);
+            umma_commit(&bar.drained);
+        }
+        __syncwarp();
+        mbar_wait(&bar.drained, 0, nullptr);  // MMAs always complete: TMEM is never freed under one
+        mbar_wait(&bar.done, 0, a.status);
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    } else if (warp >= 4) {
+        // ------------------------------ operand builders, then the epilogue
+        const int q = warp & 3;                 // TMEM lane quarter: weight rows 32 q .. 32 q + 31
+        const int par = (warp - 4) >> 2;        // chunk parity
+        const int r = q * 32 + lane;            // weight row of this thread
+        const uint32_t t_lane = static_cast<uint32_t>(q * 32) << 16;
+        bool ok = true;
+        for (int c = par; ok && c < nch; c += 2) {
+            const int sc = c >> 1, ws = sc % WS, half = c & 1, ap = c % AP;
+            uint64_t *wbar = nullptr;
+            uint32_t wpar = 0;
+            if (lane == 0) {
+                wbar = &bar.wfull[ws];
+                wpar = (sc / WS) & 1;
+            } else if (lane == 1 && c >= AP) {
+                wbar = &bar.aempty[ap];
+                wpar = ((c - AP) / AP) & 1;
+            }
+            if (!mbar_wait_lanes(wbar, wpar, a.status)) {
+                ok = false;
+                break;
+            }
+            // this row's 64 code bytes of the chunk (16-byte chunks 4 half +
+            // 0..3 of the swizzled row, chunk j at j ^ (r mod 8)) and its four
+            // group scales (8 per 256-K stage)
+            const unsigned char *wrow = smem + a.off_w + ws * W_STAGE + r * 128;
+            uint32_t wds[16];
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(wrow + (((4 * half + c4) ^ (r & 7)) << 4));
+                wds[4 * c4] = v.x;
+                wds[4 * c4 + 1] = v.y;
+                wds[4 * c4 + 2] = v.z;
+                wds[4 * c4 + 3] = v.w;
+            }
+            const uint4 sv = *reinterpret_cast<const uint4 *>(smem + a.off_s + ws * S_STAGE + r * 16);
+            const uint32_t s01 = half ? sv.z : sv.x, s23 = half ? sv.w : sv.y;  // groups 4 half + 0..3
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                // 64 codes (groups 2 cc, 2 cc + 1 of the chunk) -> 32 columns
+                uint32_t cols[32];
+#pragma unroll
+                for (int g2 = 0; g2 < 2; ++g2) {
+                    const uint32_t sg = cc ? (g2 ? s23 >> 16 : s23 & 0xFFFFu) : (g2 ? s01 >> 16 : s01 & 0xFFFFu);
+                    const uint32_t s2 = sg | (sg << 16);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t w = wds[8 * cc + 4 * g2 + i];
+                        cols[16 * g2 + 4 * i + 0] = e2m1x2_times(w, s2);
+                        cols[16 * g2 + 4 * i + 1] = e2m1x2_times(w >> 8, s2);
+                        cols[16 * g2 + 4 * i + 2] = e2m1x2_times(w >> 16, s2);
+                        cols[16 * g2 + 4 * i + 3] = e2m1x2_times(w >> 24, s2);
+                    }
+                }
+                tmem_st_32x32b_x32(tmem + t_lane + TM_A + ap * 64 + 32 * cc, cols);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&bar.aready[ap]);
+                mbar_arrive(&bar.wempty[ws]);
+            }
+        }
+        // epilogue: builders of parity 0 store token columns 0..63, parity 1
+        // columns 64..127 (as far as the tile has tokens)
+        ok = ok && mbar_wait_lanes(lane == 0 ? &bar.accfull : nullptr, 0, a.status);
+        const int col0 = par * 64;
+        if (ok && col0 < tile.rows) {
+            tc_fence_after();
+            const float *rowscale = reinterpret_cast<const float *>(a.scratch + l.scale_off);
+            const int *perm = reinterpret_cast<const int *>(a.scratch + l.perm_off);
+            const bool nok = n0 + r < a.N;
+            for (int cb = 0; cb < 2 && col0 + 32 * cb < tile.rows; ++cb) {
+                uint32_t acc[32];
+                tmem_ld_32x32b_x32(tmem + t_lane + TM_ACC + col0 + 32 * cb, acc);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int col = col0 + 32 * cb + j;  // token row of the tile
+                    if (col < tile.rows && nok) {
+                        const int pos = tile.row0 + col;
+                        const float v = __uint_as_float(acc[j]) * rowscale[pos];
+                        a.Y[static_cast<int64_t>(perm[pos]) * a.N + n0 + r] = f32_to_bf16_bits(v);
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar.done);
+    }
+}
+
+}  // namespace
+
+int64_t moe_fp4_gemm_scratch(int64_t P, int64_t E, int64_t K) { return moe_scratch_layout(P, E, K).total; }
+
+cudaError_t launch_moe_fp4_gemm(const uint16_t *X, const uint8_t *qw, const uint16_t *s, const int32_t *ids, int M,
+                                int topk, uint16_t *Y, int64_t E, int64_t N, int64_t K, void *scratch,
+                                cudaStream_t st, unsigned int *status, const DeviceInfo &dev) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const int P = M * topk;
+    const MoeScratch l = moe_scratch_layout(P, E, K);
+    unsigned char *scr = static_cast<unsigned char *>(scratch);
+    // 1. routing
+    {
+        const int smem = static_cast<int>(3 * E * sizeof(int));
+        static SmemLimit limit;
+        if (cudaError_t e = limit.ensure(reinterpret_cast<const void *>(moe_route_kernel), dev.device, smem)) return e;
+        moe_route_kernel<<<1, ROUTE_THREADS, smem, st>>>(ids, P, static_cast<int>(E), scr, status);
+        if (cudaError_t e = cudaGetLastError()) return e;
+    }
+    // 2. gathering
+    moe_gather_kernel<<<P, GATHER_THREADS, 0, st>>>(X, topk, P, static_cast<int>(E), static_cast<int>(K), N, Y, scr);
+    if (cudaError_t e = cudaGetLastError()) return e;
+    // 3. the GEMM
+    CUtensorMap tmW, tmS, tmX;
+    {
+        // packed codes as bytes [E*N, K/2]: box 128 bytes (256 codes) x 128 rows, 128-byte swizzle
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(E * N)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
+        const cuuint32_t box[2] = {128, BR};
+        const cuuint32_t estr[2] = {1, 1};
+        if (enc(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(qw), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        // scales as binary16 [E*N, K/32]: box 8 (16 bytes, one 256-K stage) x 128 rows
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 32), static_cast<cuuint64_t>(E * N)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 32) * 2};
+        const cuuint32_t box[2] = {8, BR};
+        const cuuint32_t estr[2] = {1, 1};
+        if (enc(&tmS, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t *>(s), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        // gathered token rows, binary16 [P, K]: box 64 (128 bytes) x 16 rows, 128-byte swizzle
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(P)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+        const cuuint32_t box[2] = {64, X_BOX_ROWS};
+        const cuuint32_t estr[2] = {1, 1};
+        if (enc(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, scr + l.xg_off, dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    MoeGemmArgs a;
+    a.scratch = scr;
+    a.Y = Y;
+    a.status = status;
+    a.P = P;
+    a.E = static_cast<int>(E);
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    a.nchunks = static_cast<int>(K / CK);
+    a.inject = dev.inject;
+    a.off_w = XS * X_STAGE;
+    a.off_s = a.off_w + WS * W_STAGE;
+    a.off_bar = a.off_s + WS * S_STAGE;
+    const int smem = 1024 + a.off_bar + static_cast<int>(sizeof(MoeBarriers));
+    if (smem > dev.max_smem_optin) return cudaErrorNotSupported;
+    static SmemLimit limit;
+    if (cudaError_t e = limit.ensure(reinterpret_cast<const void *>(moe_fp4_gemm_kernel), dev.device, smem)) return e;
+    const dim3 grid(static_cast<unsigned>(l.tmax), static_cast<unsigned>((N + BR - 1) / BR));
+    moe_fp4_gemm_kernel<<<grid, THREADS, smem, st>>>(tmW, tmS, tmX, a);
+    return cudaGetLastError();
+}
+
+}  // namespace w4

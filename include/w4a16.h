@@ -136,6 +136,45 @@ int fp4_moe_gemv(const uint16_t *x, const uint8_t *qw, const uint16_t *s,
                  int64_t N, int64_t K, int group, void *stream);
 
 /*
+ * Batched-expert FP4 GEMM for M tokens, each routed to topk experts
+ * ("DeepSeek V4 Triton FP4 optimisation in practice": the fused FP4
+ * dequantise-and-multiply expert GEMMs; M > 1 is the prefill or batched
+ * decode case of the one-token fp4_moe_gemv):
+ *   Y[m, j, n] = sum_k X[m, k] * e2m1(qw[e, n, k]) * s[e, n, k/32],
+ *   e = expert_ids[m * topk + j].
+ *   X          : bfloat16 [M, K]
+ *   qw         : uint8    [E, N, K/2]     packed E2M1 codes (even k in the
+ *                                         low nibble) of every expert
+ *   s          : binary16 [E, N, K/group] scales
+ *   expert_ids : int32    [M, topk]       DEVICE array; repeats allowed
+ *   Y          : bfloat16 [M, topk, N]
+ *   scratch    : device memory of at least fp4_moe_gemm_scratch_bytes(M,
+ *                topk, E, K) bytes, 256-byte aligned, owned by the caller and
+ *                used by this call only while it runs on `stream` (the
+ *                routing table and the tokens gathered per expert); it need
+ *                not be zeroed.
+ * Three launches on `stream`: routing, gathering, the tensor-core GEMM.
+ * Arithmetic: each weight e2m1 * s is rounded once to binary16 (relative
+ * error at most 2^-11 for |s| in [2^-13, 10922]; smaller scales round to
+ * binary16 subnormals, larger ones overflow); each token row is scaled by
+ * a power of two into binary16 (exact for values within 2^28 of its
+ * largest magnitude); products and sums in binary32; output rounded to
+ * nearest even.  fp4_moe_gemv applies the scales in binary32 instead and
+ * has no range limit on s.
+ * Requires group == 32, K % 256 == 0, K <= 65536, M * topk <= 2^20,
+ * E <= 8192.  An id outside [0, E) cannot be checked on the host: that
+ * output row is written as zeros and the device status is set
+ * (W4A16_ERR_DEVICE).
+ */
+int fp4_moe_gemm(const uint16_t *X, const uint8_t *qw, const uint16_t *s,
+                 const int32_t *expert_ids, int M, int topk, uint16_t *Y,
+                 int64_t E, int64_t N, int64_t K, int group, void *scratch,
+                 int64_t scratch_bytes, void *stream);
+
+/* Scratch bytes fp4_moe_gemm needs (0 for sizes below 1). */
+int64_t fp4_moe_gemm_scratch_bytes(int M, int topk, int64_t E, int64_t K);
+
+/*
  * Debug dequantisation: writes the dequantised weight matrix (the step the
  * fused kernels keep in registers / shared memory; "Lab 5", section "Triton
  * dequant + cuBLAS", first pass).  Bit-exact contract:

@@ -32,7 +32,8 @@ def test_header_declares_the_entry_points():
               "w4a16_check_device_error", "w4a16_last_error_string", "w4a16_version",
               "w4a16_debug_inject", "w4a16_linear_sequence", "w4a16_graph_create",
               "w4a16_graph_launch", "w4a16_graph_destroy", "w4a16_linear_chain",
-              "w4a16_linear_chain_scratch_bytes", "w4a16_linear_chain_noalloc"):
+              "w4a16_linear_chain_scratch_bytes", "w4a16_linear_chain_noalloc", "fp4_moe_gemm",
+              "fp4_moe_gemm_scratch_bytes"):
         assert n in names
 
 
@@ -71,6 +72,20 @@ def test_host_validation_codes(libw4):
     assert _call(libw4, "fp4_moe_gemv", A, A, A, A, 0, A, 4, 8, 128, 32, None) == 1
     assert _call(libw4, "fp4_moe_gemv", A, A, A, A, 2, A, 4, 8, 96, 32, None) == 1
     assert _call(libw4, "fp4_moe_gemv", A, A, A, A + 2, 2, A, 4, 8, 128, 32, None) == 3
+    need = _call(libw4, "fp4_moe_gemm_scratch_bytes", 4, 2, 8, 512)
+    assert need > 4 * 2 * 512 * 2 and need % 256 == 0
+    assert _call(libw4, "fp4_moe_gemm_scratch_bytes", 0, 2, 8, 512) == 0
+    assert _call(libw4, "fp4_moe_gemm_scratch_bytes", 8, 2, 8, 512) > need
+    moe = lambda X, ids, M, K, g, scr, nb: _call(libw4, "fp4_moe_gemm", X, A, A, ids, M, 2, A, 8, 64, K, g,
+                                                   scr, nb, None)
+    assert moe(None, A, 4, 512, 32, A, need) == 1
+    assert moe(A, A, 0, 512, 32, A, need) == 1
+    assert moe(A, A, 4, 512, 16, A, need) == 2          # group other than 32
+    assert moe(A, A, 4, 384, 32, A, need) == 2          # K not a multiple of 256
+    assert moe(A + 8, A, 4, 512, 32, A, need) == 3
+    assert moe(A, A + 2, 4, 512, 32, A, need) == 3      # ids not 4-byte aligned
+    assert moe(A, A, 4, 512, 32, A + 16, need) == 3     # scratch not 256-byte aligned
+    assert moe(A, A, 4, 512, 32, A, need - 1) == 1      # scratch too small
     assert _call(libw4, "w4a16_dequant", 1, A, A, A, A, 0, 4, 128, 32, None) == 1
     assert _call(libw4, "w4a16_dequant", 0, A, A, A, A, 2, 4, 128, 128, None) == 1
     assert _call(libw4, "w4a16_dequant", 0, A, A, A, A, 0, 4, 128, 64, None) == 2
