@@ -538,6 +538,23 @@ def per_config(torch, w4, synth, dev, stream, hbm_peak, tf_peak):
     out["moe_fp4_64x4096x7168_top6"] = {"us": round(t * 1e6, 2), "GB/s": round(mb / t / 1e9, 1),
                                         "frac_hbm": round(mb / t / 1e9 / hbm_peak, 3),
                                         "each": spread(torch, fn, 100, stream)}
+    # the same resident experts for M tokens routed 6 ways (fp4_moe_gemm):
+    # bytes = the weights of every expert used (once) + tokens and outputs
+    for M in (16, 128):
+        g = synth.Stream(200 + M)
+        idm = torch.stack([torch.from_numpy(synth.sample_experts(g, E, topk)) for _ in range(M)]).to(dev)
+        X = torch.randn(M, K, device=dev).to(torch.bfloat16)
+        Y = torch.empty(M, topk, N, dtype=torch.bfloat16, device=dev)
+        scr = torch.empty(w4.fp4_moe_gemm_scratch_bytes(M, topk, E, K), dtype=torch.uint8, device=dev)
+        fn = lambda i: w4.fp4_moe_gemm(X, qw, s, idm, Y, scr)
+        t = time_launches(torch, fn, 20, stream)
+        used = int(torch.unique(idm).numel())
+        gb = used * (N * K // 2 + 2 * N * (K // 32)) + 2 * M * K + 2 * M * topk * N + 4 * M * topk
+        tf = 2.0 * M * topk * N * K / t / 1e12
+        out["moe_fp4_gemm_m%d_64x4096x7168_top6" % M] = {
+            "us": round(t * 1e6, 2), "experts_used": used, "GB/s": round(gb / t / 1e9, 1),
+            "frac_hbm": round(gb / t / 1e9 / hbm_peak, 3), "TFLOP/s": round(tf, 1),
+            "frac_bf16": round(tf / tf_peak, 4), "launches_per_call": 3}
     del qw, s
     torch.cuda.empty_cache()
     # prefill GEMM through the tensor cores
@@ -777,6 +794,72 @@ def run_ours(args):
     return 0
 
 
+def profile_cases(torch, w4, dev):
+    """One workload each, for a profiler to capture: name -> (setup, run).
+    Random weights and activations of the workload's shape (torch.randint /
+    randn: quick to make at full size)."""
+
+    def gemv(N, K):
+        def setup():
+            qw = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device=dev)
+            s = (torch.rand(N, K // 128, device=dev) * 0.02 + 0.001).half()
+            z = torch.randint(0, 16, (N, K // 128), device=dev).half()
+            x = torch.randn(K, device=dev).bfloat16()
+            y = torch.empty(N, dtype=torch.bfloat16, device=dev)
+            return lambda: w4.w4a16_gemv(x, qw, s, z, y)
+        return setup
+
+    def gemm(M, N, K):
+        def setup():
+            qw = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device=dev)
+            s = (torch.rand(N, K // 128, device=dev) * 0.02 + 0.001).half()
+            z = torch.randint(0, 16, (N, K // 128), device=dev).half()
+            X = torch.randn(M, K, device=dev).bfloat16()
+            Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+            return lambda: w4.w4a16_gemm(X, qw, s, z, Y)
+        return setup
+
+    def moe(M):
+        def setup():
+            E, N, K, topk = 64, 4096, 7168, 6
+            qw = torch.randint(0, 256, (E, N, K // 2), dtype=torch.uint8, device=dev)
+            s = (torch.rand(E, N, K // 32, device=dev) * 0.09 + 0.01).half()
+            g = torch.Generator().manual_seed(M)
+            ids = torch.stack([torch.randperm(E, generator=g)[:topk] for _ in range(M)]).int().to(dev)
+            X = torch.randn(M, K, device=dev).bfloat16()
+            if M == 1:
+                y = torch.empty(topk, N, dtype=torch.bfloat16, device=dev)
+                return lambda: w4.fp4_moe_gemv(X[0], qw, s, ids[0], y)
+            Y = torch.empty(M, topk, N, dtype=torch.bfloat16, device=dev)
+            scratch = torch.empty(w4.fp4_moe_gemm_scratch_bytes(M, topk, E, K), dtype=torch.uint8, device=dev)
+            return lambda: w4.fp4_moe_gemm(X, qw, s, ids, Y, scratch)
+        return setup
+
+    return {"gemv_3840x3840": gemv(3840, 3840), "gemv_up_15360x3840": gemv(*UP),
+            "gemv_down_3840x15360": gemv(*DOWN), "gemv_vocab_262144x3840": gemv(262144, 3840),
+            "gemm_m128_15360x3840": gemm(128, 15360, 3840), "gemm_m2048_15360x3840": gemm(2048, 15360, 3840),
+            "moe_fp4_64x4096x7168_top6": moe(1), "moe_fp4_gemm_m16_64x4096x7168_top6": moe(16),
+            "moe_fp4_gemm_m128_64x4096x7168_top6": moe(128)}
+
+
+def run_case(args):
+    """Run one workload --reps times, untimed (the command a profiler wraps)."""
+    import torch
+    import gemm_w4a16_gemv_gb300 as w4
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    cases = profile_cases(torch, w4, dev)
+    if args.case not in cases:
+        raise SystemExit("unknown --case %s; one of: %s" % (args.case, ", ".join(sorted(cases))))
+    run = cases[args.case]()
+    for _ in range(args.reps):
+        run()
+    torch.cuda.synchronize()
+    status = w4.w4a16_check_device_error()
+    print(json.dumps({"case": args.case, "reps": args.reps, "device_status": status}))
+    return 0 if status == 0 else 1
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -787,7 +870,11 @@ def main(argv=None):
     ap.add_argument("--no-configs", action="store_true", help="skip per-configuration timings")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--case", help="run one workload --reps times, untimed (for a profiler)")
+    ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args(argv)
+    if args.case:
+        return run_case(args)
     if args.steps < 1 or args.warmup < 0:
         ap.error("--steps must be >= 1 and --warmup >= 0")
     if args.impl == "reference":

@@ -19,7 +19,12 @@
 //     the weight e2m1 * s rounded once to binary16, a relative error of at
 //     most 2^-11 (the only rounding of the operands) -- into the A operand in
 //     tensor memory; the gathered token rows are the B operand (TMA, 128-byte
-//     swizzle); one FP32 accumulator over all of K; the epilogue undoes each
+//     swizzle).  The tile has few token rows (the MMA's N is 16 for a
+//     typical expert), and MMAs issued by one thread run one after another at
+//     about 100-150 SM cycles each whatever N is, while MMAs from different
+//     warps into different accumulators overlap.  So 4 issuer warps (2 for
+//     tiles of more than 64 rows) take turns by 128-K chunk, each into an
+//     FP32 accumulator of its own; the epilogue sums them, undoes each
 //     token's power-of-two scale, rounds to BF16 and scatters the rows to
 //     their (token, slot) places.
 // Every wait is bounded; on a timeout the status word is set, each role
@@ -38,17 +43,25 @@ constexpr int BR = 128;               // weight rows per CTA (the MMA's M; TMEM 
 constexpr int BT = 128;               // token rows per tile at most (the MMA's N)
 constexpr int CK = 128;               // K per chunk: one A stage, one X stage
 constexpr int SCK = 256;              // K per weight stage: 128 code bytes and 8 scales per row
-constexpr int XS = 3;                 // X stages
-constexpr int WS = 2;                 // weight stages (codes + scales)
-constexpr int AP = 4;                 // TMEM operand stages (64 columns each)
+constexpr int XS_MAX = 4;             // X stages: a multiple of the issuer count, so that each
+                                      // issuer waits on stages of its own chunks only (in order)
+constexpr int WS_MAX = 12;            // weight stages (codes + scales), as many as fit
+constexpr int BG = 2;                 // builder groups: chunk c is built by group c mod 2
+constexpr int AP = 4;                 // TMEM operand stages (64 columns each), two per group
+constexpr int MAX_ISS = 4;            // MMA issuer warps (each with its own accumulator)
 constexpr int X_BOX_ROWS = 16;        // rows per X TMA box (a tile loads as many boxes as it needs)
-constexpr int X_STAGE = BT * CK * 2;  // 32 KB: two 64-K boxes of up to 128 rows
 constexpr int W_STAGE = BR * 128;     // 16 KB of packed codes
 constexpr int S_STAGE = BR * 16;      // 2 KB of scales
-constexpr int THREADS = 384;          // 12 warps: 0 weights TMA, 1 tokens TMA, 2 MMA, 3 idle, 4-11 builders
+// Shared memory holds the X ring (stages of 256 bytes per token row of the
+// tile) and as many weight stages as fit after it (10 for a 16-row tile, 6
+// for a 128-row tile): the weight ring keeps the HBM reads in flight.
+constexpr int POOL = 208 * 1024;
+constexpr int THREADS = 512;          // 16 warps: 0 weights TMA, 1 tokens TMA, 2-5 MMA, 6 TMEM, 8-15 builders
+constexpr int ISS0 = 2;               // first issuer warp
+constexpr int BW0 = 8;                // first builder warp (warp & 3 = its TMEM lane quarter)
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_ACC = 0;        // accumulator: columns 0 .. BT-1
-constexpr uint32_t TM_A = 128;        // operand stages after it
+constexpr uint32_t TM_ACC = 0;        // accumulators: n_iss x nmma <= 256 columns
+constexpr uint32_t TM_A = 256;        // operand stages after them
 constexpr int ROUTE_THREADS = 1024;
 constexpr int GATHER_THREADS = 256;
 
@@ -173,17 +186,15 @@ struct MoeGemmArgs {
     uint16_t *Y;
     unsigned int *status;
     int P, E, N, K, nchunks;
-    int off_w, off_s, off_bar;  // byte offsets in shared memory (X stages at 0)
     unsigned int inject;
 };
 
 struct MoeBarriers {
-    uint64_t xfull[XS], xempty[XS];
-    uint64_t wfull[WS], wempty[WS];
+    uint64_t xfull[XS_MAX], xempty[XS_MAX];
+    uint64_t wfull[WS_MAX], wempty[WS_MAX];
     uint64_t aready[AP], aempty[AP];
-    uint64_t accfull;
+    uint64_t accfull;   // every issuer's MMAs completed (n_iss arrivals)
     uint64_t done;      // builders finished with tensor memory
-    uint64_t drained;   // every MMA completed
     uint32_t tmem_holder;
 };
 
@@ -203,7 +214,7 @@ moe_fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
                     const __grid_constant__ CUtensorMap tmX, const MoeGemmArgs a) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    MoeBarriers &bar = *reinterpret_cast<MoeBarriers *>(smem + a.off_bar);
+    MoeBarriers &bar = *reinterpret_cast<MoeBarriers *>(smem + POOL);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // the tile: read after the routing launch has finished (stream order)
@@ -217,26 +228,38 @@ moe_fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
     const int nmma = ((tile.rows + 15) / 16) * 16;          // the MMA's N
     const int xboxes = nmma / X_BOX_ROWS;
     const int nch = a.nchunks;
+    // issuers: as many as the accumulators fit in 256 columns, at most one
+    // per chunk (each issuer's first chunk initialises its accumulator)
+    int n_iss = nmma <= 64 ? MAX_ISS : 2;
+    n_iss = n_iss < nch ? n_iss : nch;
+    // the ring: X stages of nmma rows x 128 K (two 64-K halves), then the
+    // weight stages (codes, 1024-aligned, then their scales)
+    const int x_half = nmma * 128;
+    const int x_stage = 2 * x_half;
+    const int xs_n = XS_MAX;
+    const int off_w = xs_n * x_stage;
+    int ws_n = (POOL - off_w) / (W_STAGE + S_STAGE);
+    ws_n = ws_n < WS_MAX ? ws_n : WS_MAX;
+    const int off_s = off_w + ws_n * W_STAGE;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < XS; ++i) {
+        for (int i = 0; i < xs_n; ++i) {
             mbar_init(&bar.xfull[i], 1);
             mbar_init(&bar.xempty[i], 1);
         }
-        for (int i = 0; i < WS; ++i) {
+        for (int i = 0; i < ws_n; ++i) {
             mbar_init(&bar.wfull[i], 1);
-            mbar_init(&bar.wempty[i], 8);  // the 8 builder warps
+            mbar_init(&bar.wempty[i], 8);  // the stage's two chunks, four builder warps each
         }
         for (int i = 0; i < AP; ++i) {
-            mbar_init(&bar.aready[i], 4);  // the 4 builder warps of the chunk's parity
+            mbar_init(&bar.aready[i], 4);  // the 4 builder warps of the chunk's group
             mbar_init(&bar.aempty[i], 1);
         }
-        mbar_init(&bar.accfull, 1);
-        mbar_init(&bar.done, 8);
-        mbar_init(&bar.drained, 1);
+        mbar_init(&bar.accfull, n_iss);
+        mbar_init(&bar.done, 4 * BG);
         fence_barrier_init();
     }
-    if (warp == 2) {  // the MMA warp allocates tensor memory and frees it at the end
+    if (warp == 6) {  // this warp allocates tensor memory and frees it at the end
         tmem_alloc(&bar.tmem_holder, TMEM_COLS);
         tmem_relinquish();
     }
@@ -255,17 +278,17 @@ moe_fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
             const int nissue = (a.inject & kInjectStallPipeline) ? 0 : nsc;
             int issued = 0;
             for (int sc = 0; sc < nissue; ++sc, ++issued) {
-                const int ws = sc % WS;
-                if (sc >= WS && !mbar_wait(&bar.wempty[ws], ((sc / WS) - 1) & 1, a.status)) break;
+                const int ws = sc % ws_n;
+                if (sc >= ws_n && !mbar_wait(&bar.wempty[ws], ((sc / ws_n) - 1) & 1, a.status)) break;
                 mbar_arrive_expect_tx(&bar.wfull[ws], W_STAGE + S_STAGE);
                 // rows past the stack's end read as zeros; rows of the next
                 // expert (tiles ending past N) are computed and not stored
-                tma_load_2d_hint(smem + a.off_w + ws * W_STAGE, &tmW, sc * 128, wrow0, &bar.wfull[ws], pol);
-                tma_load_2d_hint(smem + a.off_s + ws * S_STAGE, &tmS, sc * 8, wrow0, &bar.wfull[ws], pol);
+                tma_load_2d_hint(smem + off_w + ws * W_STAGE, &tmW, sc * 128, wrow0, &bar.wfull[ws], pol);
+                tma_load_2d_hint(smem + off_s + ws * S_STAGE, &tmS, sc * 8, wrow0, &bar.wfull[ws], pol);
             }
             // no copy in flight when the CTA exits
-            for (int it = issued > WS ? issued - WS : 0; it < issued; ++it)
-                mbar_wait(&bar.wfull[it % WS], (it / WS) & 1, nullptr);
+            for (int it = issued > ws_n ? issued - ws_n : 0; it < issued; ++it)
+                mbar_wait(&bar.wfull[it % ws_n], (it / ws_n) & 1, nullptr);
         }
     } else if (warp == 1) {
         // ------------------------------------------ token rows (TMA)
@@ -275,24 +298,27 @@ moe_fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
             const int nissue = (a.inject & kInjectStallPipeline) ? 0 : nch;
             int issued = 0;
             for (int c = 0; c < nissue; ++c, ++issued) {
-                const int xs = c % XS;
-                if (c >= XS && !mbar_wait(&bar.xempty[xs], ((c / XS) - 1) & 1, a.status)) break;
+                const int xs = c % xs_n;
+                if (c >= xs_n && !mbar_wait(&bar.xempty[xs], ((c / xs_n) - 1) & 1, a.status)) break;
                 mbar_arrive_expect_tx(&bar.xfull[xs], 2 * xboxes * X_BOX_ROWS * 128);
-                unsigned char *dst = smem + xs * X_STAGE;
+                unsigned char *dst = smem + xs * x_stage;
                 for (int h = 0; h < 2; ++h)          // the chunk's two 64-K boxes
                     for (int b = 0; b < xboxes; ++b)  // 16 rows each
-                        tma_load_2d_hint(dst + h * (X_STAGE / 2) + b * X_BOX_ROWS * 128, &tmX, c * CK + h * 64,
+                        tma_load_2d_hint(dst + h * x_half + b * X_BOX_ROWS * 128, &tmX, c * CK + h * 64,
                                          tile.row0 + b * X_BOX_ROWS, &bar.xfull[xs], pol);
             }
-            for (int it = issued > XS ? issued - XS : 0; it < issued; ++it)
-                mbar_wait(&bar.xfull[it % XS], (it / XS) & 1, nullptr);
+            for (int it = issued > xs_n ? issued - xs_n : 0; it < issued; ++it)
+                mbar_wait(&bar.xfull[it % xs_n], (it / xs_n) & 1, nullptr);
         }
-    } else if (warp == 2) {
-        // -------------------------------------------------- MMA issuer
+    } else if (warp >= ISS0 && warp < ISS0 + n_iss) {
+        // ------------------------------------------------ MMA issuers
+        // issuer j takes the chunks c = j mod n_iss into accumulator j
+        const int j = warp - ISS0;
+        const uint32_t d_acc = tmem + TM_ACC + static_cast<uint32_t>(j * nmma);
         const uint32_t idesc = idesc_kind_f16(BR, nmma, 0u);  // FP16 x FP16 -> FP32, M = 128, N = nmma
         bool ok = !(a.inject & kInjectStallConsumers);
-        for (int c = 0; ok && c < nch; ++c) {
-            const int ap = c % AP, xs = c % XS;
+        for (int c = j; ok && c < nch; c += n_iss) {
+            const int ap = c % AP, xs = c % xs_n;
             uint64_t *wbar = nullptr;
             uint32_t par = 0;
             if (lane == 0) {
@@ -300,7 +326,7 @@ moe_fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
                 par = (c / AP) & 1;
             } else if (lane == 1) {
                 wbar = &bar.xfull[xs];
-                par = (c / XS) & 1;
+                par = (c / xs_n) & 1;
             }
             if (!mbar_wait_lanes(wbar, par, a.status)) {
                 ok = false;
@@ -308,44 +334,44 @@ moe_fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
             }
             tc_fence_after();
             if (lane == 0) {
-                const uint32_t b_addr = smem_u32(smem + xs * X_STAGE);
+                const uint32_t b_addr = smem_u32(smem + xs * x_stage);
 #pragma unroll
                 for (int k = 0; k < CK / 16; ++k)
-                    umma_f16_tmem_a(tmem + TM_ACC, tmem + TM_A + ap * 64 + 8 * k,
-                                    smem_desc_sw128_kmajor(b_addr + (k >> 2) * (X_STAGE / 2) + 32 * (k & 3)), idesc,
-                                    (c | k) != 0);
+                    umma_f16_tmem_a(d_acc, tmem + TM_A + ap * 64 + 8 * k,
+                                    smem_desc_sw128_kmajor(b_addr + (k >> 2) * x_half + 32 * (k & 3)), idesc,
+                                    (c != j) || (k != 0));
                 umma_commit(&bar.xempty[xs]);
                 umma_commit(&bar.aempty[ap]);
             }
             __syncwarp();
         }
-        // the accumulator is complete once every MMA issued has completed (on
-        // a timeout: the epilogue's wait ends as well, with garbage it does
-        // not store)
-        if (lane == 0) {
-            umma_commit(&bar.accfull);
-            umma_commit(&bar.drained);
-        }
+        // the accumulators are complete once every MMA issued has completed
+        // (on a timeout the epilogue's wait ends as well, with values it
+        // does not store)
+        if (lane == 0) umma_commit(&bar.accfull);
         __syncwarp();
-        mbar_wait(&bar.drained, 0, nullptr);  // MMAs always complete: TMEM is never freed under one
+    } else if (warp == 6) {
+        // tensor memory is freed only after every MMA has completed and the
+        // epilogue has read the accumulators
+        mbar_wait(&bar.accfull, 0, nullptr);
         mbar_wait(&bar.done, 0, a.status);
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
-    } else if (warp >= 4) {
+    } else if (warp >= BW0) {
         // ------------------------------ operand builders, then the epilogue
         const int q = warp & 3;                 // TMEM lane quarter: weight rows 32 q .. 32 q + 31
-        const int par = (warp - 4) >> 2;        // chunk parity
+        const int grp = (warp - BW0) >> 2;      // builder group: chunks grp, grp + BG, ...
         const int r = q * 32 + lane;            // weight row of this thread
         const uint32_t t_lane = static_cast<uint32_t>(q * 32) << 16;
         bool ok = true;
-        for (int c = par; ok && c < nch; c += 2) {
-            const int sc = c >> 1, ws = sc % WS, half = c & 1, ap = c % AP;
+        for (int c = grp; ok && c < nch; c += BG) {
+            const int sc = c >> 1, ws = sc % ws_n, half = c & 1, ap = c % AP;
             uint64_t *wbar = nullptr;
             uint32_t wpar = 0;
             if (lane == 0) {
                 wbar = &bar.wfull[ws];
-                wpar = (sc / WS) & 1;
+                wpar = (sc / ws_n) & 1;
             } else if (lane == 1 && c >= AP) {
                 wbar = &bar.aempty[ap];
                 wpar = ((c - AP) / AP) & 1;
@@ -357,7 +383,7 @@ moe_fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
             // this row's 64 code bytes of the chunk (16-byte chunks 4 half +
             // 0..3 of the swizzled row, chunk j at j ^ (r mod 8)) and its four
             // group scales (8 per 256-K stage)
-            const unsigned char *wrow = smem + a.off_w + ws * W_STAGE + r * 128;
+            const unsigned char *wrow = smem + off_w + ws * W_STAGE + r * 128;
             uint32_t wds[16];
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
@@ -367,7 +393,7 @@ moe_fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
                 wds[4 * c4 + 2] = v.z;
                 wds[4 * c4 + 3] = v.w;
             }
-            const uint4 sv = *reinterpret_cast<const uint4 *>(smem + a.off_s + ws * S_STAGE + r * 16);
+            const uint4 sv = *reinterpret_cast<const uint4 *>(smem + off_s + ws * S_STAGE + r * 16);
             const uint32_t s01 = half ? sv.z : sv.x, s23 = half ? sv.w : sv.y;  // groups 4 half + 0..3
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
@@ -396,26 +422,31 @@ moe_fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
                 mbar_arrive(&bar.wempty[ws]);
             }
         }
-        // epilogue: builders of parity 0 store token columns 0..63, parity 1
-        // columns 64..127 (as far as the tile has tokens)
+        // epilogue: group g stores the 16-column pieces p = g, g + BG, ... of
+        // the tile's token columns, each the sum of the n_iss accumulators
         ok = ok && mbar_wait_lanes(lane == 0 ? &bar.accfull : nullptr, 0, a.status);
-        const int col0 = par * 64;
-        if (ok && col0 < tile.rows) {
+        if (ok) {
             tc_fence_after();
             const float *rowscale = reinterpret_cast<const float *>(a.scratch + l.scale_off);
             const int *perm = reinterpret_cast<const int *>(a.scratch + l.perm_off);
             const bool nok = n0 + r < a.N;
-            for (int cb = 0; cb < 2 && col0 + 32 * cb < tile.rows; ++cb) {
-                uint32_t acc[32];
-                tmem_ld_32x32b_x32(tmem + t_lane + TM_ACC + col0 + 32 * cb, acc);
-                tmem_ld_wait();
+            for (int p = grp; 16 * p < tile.rows; p += BG) {
+                float acc[16];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int col = col0 + 32 * cb + j;  // token row of the tile
+                for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+                for (int j = 0; j < n_iss; ++j) {
+                    uint32_t v[16];
+                    tmem_ld_32x32b_x16(tmem + t_lane + TM_ACC + static_cast<uint32_t>(j * nmma + 16 * p), v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[i] += __uint_as_float(v[i]);
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int col = 16 * p + i;  // token row of the tile
                     if (col < tile.rows && nok) {
                         const int pos = tile.row0 + col;
-                        const float v = __uint_as_float(acc[j]) * rowscale[pos];
-                        a.Y[static_cast<int64_t>(perm[pos]) * a.N + n0 + r] = f32_to_bf16_bits(v);
+                        a.Y[static_cast<int64_t>(perm[pos]) * a.N + n0 + r] = f32_to_bf16_bits(acc[i] * rowscale[pos]);
                     }
                 }
             }
@@ -494,10 +525,7 @@ cudaError_t launch_moe_fp4_gemm(const uint16_t *X, const uint8_t *qw, const uint
     a.K = static_cast<int>(K);
     a.nchunks = static_cast<int>(K / CK);
     a.inject = dev.inject;
-    a.off_w = XS * X_STAGE;
-    a.off_s = a.off_w + WS * W_STAGE;
-    a.off_bar = a.off_s + WS * S_STAGE;
-    const int smem = 1024 + a.off_bar + static_cast<int>(sizeof(MoeBarriers));
+    const int smem = 1024 + POOL + static_cast<int>(sizeof(MoeBarriers));
     if (smem > dev.max_smem_optin) return cudaErrorNotSupported;
     static SmemLimit limit;
     if (cudaError_t e = limit.ensure(reinterpret_cast<const void *>(moe_fp4_gemm_kernel), dev.device, smem)) return e;
