@@ -19,7 +19,7 @@ import threading
 import torch
 
 __all__ = [
-    "w4a16_gemv", "w4a16_gemm", "fp4_moe_gemv", "fp4_moe_gemm", "fp4_moe_gemm_scratch_bytes",
+    "w4a16_gemv", "w4a16_gemm", "w4a16_gemm_f16", "fp4_moe_gemv", "fp4_moe_gemm", "fp4_moe_gemm_scratch_bytes",
     "w4a16_dequant", "w4a16_bf16_gemm",
     "w4a16_check_device_error", "w4a16_last_error_string", "w4a16_version",
     "w4a16_debug_inject", "INJECT_STALL_PIPELINE", "INJECT_STALL_CONSUMERS",
@@ -57,6 +57,7 @@ _OPS = ctypes.POINTER(w4a16_linear)
 SIGNATURES = {
     "w4a16_gemv": ([_P, _P, _P, _P, _P, _I64, _I64, _INT, _P], _INT),
     "w4a16_gemm": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _INT, _P], _INT),
+    "w4a16_gemm_f16": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _INT, _P], _INT),
     "w4a16_bf16_gemm": ([_P, _P, _P, _I64, _I64, _I64, _P], _INT),
     "fp4_moe_gemv": ([_P, _P, _P, _P, _INT, _P, _I64, _I64, _I64, _INT, _P], _INT),
     "fp4_moe_gemm": ([_P, _P, _P, _P, _INT, _INT, _P, _I64, _I64, _I64, _INT, _P, _I64, _P], _INT),
@@ -158,6 +159,16 @@ def w4a16_gemv(x, qw, s, z, y=None, group: int = 128, stream=None):
 def w4a16_gemm(X, qw, s, z, Y=None, group: int = 128, stream=None):
     """Y[M, N] = X[M, K] W^T with INT4 weights qw [N, K/2], s/z [N, K/group];
     z=None: symmetric INT4 (zero point 8)."""
+    return _gemm("w4a16_gemm", X, qw, s, z, Y, group, stream)
+
+
+def w4a16_gemm_f16(X, qw, s, z, Y=None, group: int = 128, stream=None):
+    """w4a16_gemm with binary16 operands (each weight rounded once to
+    binary16; see the header for the error bound)."""
+    return _gemm("w4a16_gemm_f16", X, qw, s, z, Y, group, stream)
+
+
+def _gemm(name, X, qw, s, z, Y, group, stream):
     N = qw.shape[0]
     K = 2 * qw.shape[-1]
     M = X.numel() // K
@@ -170,7 +181,7 @@ def w4a16_gemm(X, qw, s, z, Y=None, group: int = 128, stream=None):
         Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
     pY = _need(Y, "Y", torch.bfloat16, M * N, dev)
     with torch.cuda.device(dev):  # the library launches on the current device
-        _check(lib().w4a16_gemm(pX, pq, ps, pz, pY, M, N, K, group, _stream(stream, dev)))
+        _check(getattr(lib(), name)(pX, pq, ps, pz, pY, M, N, K, group, _stream(stream, dev)))
     return Y
 
 

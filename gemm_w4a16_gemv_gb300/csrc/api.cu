@@ -407,6 +407,18 @@ int w4a16_gemm(const uint16_t *X, const uint8_t *qw, const uint16_t *s,
                     "w4a16_gemm");
 }
 
+int w4a16_gemm_f16(const uint16_t *X, const uint8_t *qw, const uint16_t *s, const uint16_t *z, uint16_t *Y,
+                   int64_t M, int64_t N, int64_t K, int group, void *stream) {
+    const char *fn = "w4a16_gemm_f16";
+    if (int r = check_gemm_args(fn, X, qw, s, z, Y, M, N, K, group)) return r;
+    w4::DeviceInfo dev;
+    unsigned int *status;
+    if (int r = device_state(dev, status)) return r;
+    if (int r = check_device_ptrs(fn, dev.device, {X, qw, s, z, Y})) return r;
+    return launched(w4::launch_gemm_int4_f16(X, qw, s, z, Y, M, N, K, static_cast<cudaStream_t>(stream), status, dev),
+                    fn);
+}
+
 int w4a16_bf16_gemm(const uint16_t *X, const uint16_t *W, uint16_t *Y, int64_t M, int64_t N, int64_t K,
                     void *stream) {
     if (!X || !W || !Y) return fail(W4A16_ERR_INVALID_ARG, "w4a16_bf16_gemm: null pointer");

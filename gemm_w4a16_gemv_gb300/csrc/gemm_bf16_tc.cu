@@ -99,14 +99,14 @@ bf16_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
             const int st = kb % STAGES;
             if (!mbar_wait(&bar.full[st], (kb / STAGES) & 1, a.status)) break;
             tc_fence_after();
-            if (lane == 0) {
+            {
                 const uint32_t a_addr = smem_u32(smem + st * STAGE_BYTES);
                 const uint32_t b_addr = a_addr + BOX_BYTES;
 #pragma unroll
                 for (int k = 0; k < BK / 16; ++k)
-                    umma_f16(tmem, smem_desc_sw128_kmajor(a_addr + 32 * k), smem_desc_sw128_kmajor(b_addr + 32 * k),
-                             idesc, (kb | k) != 0);
-                umma_commit(&bar.empty[st]);
+                    umma_f16_w(tmem, smem_desc_sw128_kmajor(a_addr + 32 * k), smem_desc_sw128_kmajor(b_addr + 32 * k),
+                               idesc, (kb | k) != 0);
+                umma_commit_w(&bar.empty[st]);
             }
             __syncwarp();
         }
@@ -114,7 +114,7 @@ bf16_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
         // (also after a timeout, so that the epilogue's wait ends); MMAs
         // always complete, so this warp waits for it ignoring the status
         // word: tensor memory is never released under an MMA in flight
-        if (lane == 0) umma_commit(&bar.accfull);
+        umma_commit_w(&bar.accfull);
         __syncwarp();
         mbar_wait(&bar.accfull, 0, nullptr);
     } else if (warp >= 4) {

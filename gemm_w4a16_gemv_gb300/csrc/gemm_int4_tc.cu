@@ -304,17 +304,17 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                 break;
             }
             tc_fence_after();
-            if (lane == 0) {
+            {
                 const uint32_t t_acc = tmem + db * 128;
                 const uint32_t a_t = tmem + TM_A + ap * 64;
                 const uint32_t b_addr = smem_u32(smem + OFF_X + xs * 2 * X_BYTES);
 #pragma unroll
                 for (int k = 0; k < GK / 16; ++k)
-                    umma_f16_tmem_a(t_acc, a_t + 8 * k,
-                                    smem_desc_sw128_kmajor(b_addr + (k >> 2) * X_BYTES + 32 * (k & 3)), idesc, k != 0);
-                umma_commit(&bar.xempty[xs]);
-                umma_commit(&bar.aempty[ap]);
-                umma_commit(&bar.accfull[db]);
+                    umma_f16_tmem_a_w(t_acc, a_t + 8 * k,
+                                      smem_desc_sw128_kmajor(b_addr + (k >> 2) * X_BYTES + 32 * (k & 3)), idesc, k != 0);
+                umma_commit_w(&bar.xempty[xs]);
+                umma_commit_w(&bar.aempty[ap]);
+                umma_commit_w(&bar.accfull[db]);
             }
             __syncwarp();
             xs += 2;
@@ -336,9 +336,9 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         // Only after a timeout: one more commit so that the epilogue's wait
         // for this warp's group also ends once the MMAs already issued have
         // completed.
-        if (!ok && lane == 0) umma_commit(&bar.accfull[db]);
+        if (!ok) umma_commit_w(&bar.accfull[db]);
         // `drained` fires once every MMA of both warps has completed
-        if (lane == 0) umma_commit(&bar.drained);
+        umma_commit_w(&bar.drained);
         __syncwarp();
         if (warp == 1) {
             // MMAs always complete, so this wait ignores the status word: TMEM

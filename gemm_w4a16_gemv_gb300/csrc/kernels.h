@@ -96,6 +96,13 @@ cudaError_t launch_moe_fp4(const uint16_t *x, const uint8_t *qw,
                            cudaStream_t st, unsigned int *status,
                            const DeviceInfo &dev);
 
+// INT4 prefill GEMM with binary16 operands (pre-pass of X into
+// stream-ordered scratch, then one accumulator over all of K).
+int gemm_int4_f16_smem(int64_t M, int64_t K, bool sym);
+cudaError_t launch_gemm_int4_f16(const uint16_t *X, const uint8_t *qw, const uint16_t *s, const uint16_t *z,
+                                 uint16_t *Y, int64_t M, int64_t N, int64_t K, cudaStream_t st, unsigned int *status,
+                                 const DeviceInfo &dev);
+
 cudaError_t launch_gemm_int4(const uint16_t *X, const uint8_t *qw,
                              const uint16_t *s, const uint16_t *z, uint16_t *Y,
                              int64_t M, int64_t N, int64_t K, cudaStream_t st,

@@ -333,22 +333,22 @@ moe_fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
                 break;
             }
             tc_fence_after();
-            if (lane == 0) {
+            {
                 const uint32_t b_addr = smem_u32(smem + xs * x_stage);
 #pragma unroll
                 for (int k = 0; k < CK / 16; ++k)
-                    umma_f16_tmem_a(d_acc, tmem + TM_A + ap * 64 + 8 * k,
-                                    smem_desc_sw128_kmajor(b_addr + (k >> 2) * x_half + 32 * (k & 3)), idesc,
+                    umma_f16_tmem_a_w(d_acc, tmem + TM_A + ap * 64 + 8 * k,
+                                      smem_desc_sw128_kmajor(b_addr + (k >> 2) * x_half + 32 * (k & 3)), idesc,
                                     (c != j) || (k != 0));
-                umma_commit(&bar.xempty[xs]);
-                umma_commit(&bar.aempty[ap]);
+                umma_commit_w(&bar.xempty[xs]);
+                umma_commit_w(&bar.aempty[ap]);
             }
             __syncwarp();
         }
         // the accumulators are complete once every MMA issued has completed
         // (on a timeout the epilogue's wait ends as well, with values it
         // does not store)
-        if (lane == 0) umma_commit(&bar.accfull);
+        umma_commit_w(&bar.accfull);
         __syncwarp();
     } else if (warp == 6) {
         // tensor memory is freed only after every MMA has completed and the

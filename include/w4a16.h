@@ -104,6 +104,31 @@ int w4a16_gemm(const uint16_t *X, const uint8_t *qw, const uint16_t *s,
                int64_t K, int group, void *stream);
 
 /*
+ * The prefill GEMM of w4a16_gemm with binary16 operands ("Lab 5", section
+ * "Triton dequant + cuBLAS": the same product; here the weights are
+ * dequantised once per tile and never written to HBM):
+ *  - a pre-pass scales each row of X by a power of two into binary16 (every
+ *    value within 2^28 of the row's largest magnitude exact; the epilogue
+ *    undoes the scale);
+ *  - each weight is formed as fl16(fl16(q - z) * s): one rounding when z is
+ *    an integer, a relative error of at most 2^-11 (the BF16 weights of the
+ *    dequantise-then-GEMM path carry 2^-9);
+ *  - one binary32 accumulator runs over all of K, on tiles of 128 weight
+ *    rows x 256 token rows.
+ * So |Y - X W^T| <= 2^-10 sum_k |X[m,k] W[n,k]| plus the BF16 rounding of
+ * the output.  w4a16_gemm is exact in every product (the scale is applied
+ * per group to binary32 partial sums), which keeps outputs that cancel
+ * exact when activations carry outliers far above the rest; this entry is
+ * the faster one from M = 256 on.
+ * Layouts and requirements: those of w4a16_gemm (any M >= 1, any N).
+ * Scratch: M*K*2 + 4*M bytes, stream-ordered, from a memory pool that the
+ * library keeps per device (kept reserved between calls).
+ */
+int w4a16_gemm_f16(const uint16_t *X, const uint8_t *qw, const uint16_t *s,
+                   const uint16_t *z, uint16_t *Y, int64_t M, int64_t N,
+                   int64_t K, int group, void *stream);
+
+/*
  * Dense BF16 GEMM, Y[m, n] = sum_k X[m, k] * W[n, k] on the tensor cores:
  * the second pass of the unfused path ("Lab 5", section "Triton dequant +
  * cuBLAS": dequantise to a BF16 weight matrix in memory, then a dense GEMM).

@@ -28,7 +28,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("w4a16_gemv", "w4a16_gemm", "fp4_moe_gemv", "w4a16_dequant", "w4a16_bf16_gemm",
+    for n in ("w4a16_gemv", "w4a16_gemm", "w4a16_gemm_f16", "fp4_moe_gemv", "w4a16_dequant", "w4a16_bf16_gemm",
               "w4a16_check_device_error", "w4a16_last_error_string", "w4a16_version",
               "w4a16_debug_inject", "w4a16_linear_sequence", "w4a16_graph_create",
               "w4a16_graph_launch", "w4a16_graph_destroy", "w4a16_linear_chain",
@@ -69,6 +69,9 @@ def test_host_validation_codes(libw4):
     assert _call(libw4, "w4a16_gemv", A, A, A, A, A, 16, 32768, 128, None) == 2
     assert _call(libw4, "w4a16_gemv", A + 8, A, A, A, A, 16, 256, 128, None) == 3
     assert _call(libw4, "w4a16_gemm", A, A, A, A, A, 4, 24, 32768, 128, None) == 2  # K beyond 16384
+    assert _call(libw4, "w4a16_gemm_f16", A, A, A, A, A, 4, 24, 32768, 128, None) == 2
+    assert _call(libw4, "w4a16_gemm_f16", A, A, A, A, A, 4, 24, 3840, 64, None) == 2  # group
+    assert _call(libw4, "w4a16_gemm_f16", A + 8, A, A, A, A, 4, 24, 3840, 128, None) == 3
     assert _call(libw4, "fp4_moe_gemv", A, A, A, A, 0, A, 4, 8, 128, 32, None) == 1
     assert _call(libw4, "fp4_moe_gemv", A, A, A, A, 2, A, 4, 8, 96, 32, None) == 1
     assert _call(libw4, "fp4_moe_gemv", A, A, A, A + 2, 2, A, 4, 8, 128, 32, None) == 3

@@ -1,0 +1,102 @@
+"""The binary16-operand prefill GEMM (w4a16_gemm_f16) through the C ABI vs
+the binary64 oracle: the product tolerance on the synthetic workloads, and
+the error bound its arithmetic gives (each weight rounded once to binary16)
+on activations with outliers far above the rest."""
+import time
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests.gpu_helpers import assert_close, bf16_to_f64, cuda_or_skip, dev_tensor, host_bits16
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(w4, torch, p, sym=False):
+    z = None if sym else dev_tensor(p["z"], torch.float16)
+    Y = w4.w4a16_gemm_f16(dev_tensor(p["x"], torch.bfloat16).view(p["M"], p["K"]), dev_tensor(p["qw"], torch.uint8),
+                          dev_tensor(p["s"], torch.float16), z)
+    torch.cuda.synchronize()
+    return host_bits16(Y).reshape(p["M"], p["N"])
+
+
+# one token tile and several (256 rows each), ragged M and N, one group and the largest K
+@pytest.mark.parametrize("M,N,K", [(1, 16, 128), (9, 113, 384), (16, 225, 640), (64, 1024, 3840),
+                                   (128, 128, 128), (130, 256, 512), (257, 400, 384), (300, 129, 1920),
+                                   (513, 96, 768), (128, 16, 16384)])
+def test_gemm_f16_small_and_ragged(M, N, K):
+    torch, w4 = cuda_or_skip()
+    p = synth.int4_problem(N, K, M=M, seed=M * 5 + N + K)
+    ref = oracle.gemm_int4(p["x"], p["qw"], p["s"], p["z"], K=K)
+    assert_close(_run(w4, torch, p), ref, "gemm_f16 %dx%dx%d" % (M, N, K))
+
+
+@pytest.mark.parametrize("M,N,K", [(20, 200, 512), (300, 136, 1024)])
+def test_gemm_f16_symmetric(M, N, K):
+    torch, w4 = cuda_or_skip()
+    p = synth.int4_problem(N, K, M=M, seed=M + N + K)
+    ref = oracle.gemm_int4(p["x"], p["qw"], p["s"], None, K=K)
+    assert_close(_run(w4, torch, p, sym=True), ref, "gemm_f16 symmetric")
+
+
+def test_gemm_f16_full_size_sampled():
+    # the prefill shape: every output on the GPU, a sample of tokens on the oracle
+    torch, w4 = cuda_or_skip()
+    M, N, K = 2048, 15360, 3840
+    p = synth.int4_problem(N, K, M=M, seed=3)
+    y = _run(w4, torch, p)
+    rows = np.array([0, 1, 255, 256, 1000, 2047])
+    ref = oracle.gemm_int4(p["x"].reshape(M, K)[rows], p["qw"], p["s"], p["z"], K=K)
+    assert_close(y[rows], ref, "gemm_f16 2048x15360x3840 sampled")
+
+
+@pytest.mark.parametrize("ratio_log2", [10, 14])
+@pytest.mark.parametrize("M", [16, 300])
+def test_gemm_f16_outliers_within_the_bound(M, ratio_log2):
+    """One activation per group 2^10 or 2^14 above the N(0, 1) rest: the
+    error stays within the bound of one binary16 rounding per weight,
+    2^-10 sum_k |x_k w_k| (twice the unit roundoff 2^-11, for the binary32
+    sums), plus the BF16 rounding of the output (2^-8 |y|)."""
+    torch, w4 = cuda_or_skip()
+    N, K = 224, 3840
+    p = synth.int4_problem(N, K, M=M, seed=M + ratio_log2)
+    rng = np.random.default_rng(M + ratio_log2)
+    G = K // 128
+    cols = np.arange(G) * 128 + rng.integers(0, 128, G)
+    X = p["x"].reshape(M, K).copy()
+    signs = np.where(rng.integers(0, 2, (M, G)) == 0, -1.0, 1.0)
+    X[:, cols] = (np.asarray(signs * 2.0 ** ratio_log2, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    p["x"] = X
+    ref = oracle.gemm_int4(X, p["qw"], p["s"], p["z"], K=K)
+    W = oracle.dequant_int4(p["qw"], p["s"], p["z"], K=K).astype(np.float64)
+    bound = 2.0 ** -10 * (np.abs(bf16_to_f64(X)) @ np.abs(W).T) + 2.0 ** -8 * np.abs(ref) + 1e-30
+    y = bf16_to_f64(_run(w4, torch, p))
+    err = np.abs(y - ref)
+    i = int(np.argmax(err / bound))
+    assert np.all(err <= bound), "element %d: error %r, bound %r" % (i, err.flat[i], bound.flat[i])
+
+
+def test_gemm_f16_bounded_wait_reports_timeout_and_recovers():
+    """Stages issued but never taken: the producers' waits run out (K large
+    enough that every ring wraps), the status reports the timeout and the
+    next call is correct."""
+    torch, w4 = cuda_or_skip()
+    M, N, K = 130, 448, 2048
+    p = synth.int4_problem(N, K, M=M, seed=9)
+    ref = oracle.gemm_int4(p["x"], p["qw"], p["s"], p["z"], K=K)
+    for flag in (w4.INJECT_STALL_PIPELINE, w4.INJECT_STALL_CONSUMERS):
+        assert w4.w4a16_check_device_error() == 0
+        w4.w4a16_debug_inject(flag)
+        try:
+            t0 = time.monotonic()
+            _run(w4, torch, p)
+            status = w4.w4a16_check_device_error()
+            waited = time.monotonic() - t0
+        finally:
+            w4.w4a16_debug_inject(0)
+        assert status == 5  # W4A16_ERR_TIMEOUT
+        assert 1.5 < waited < 30.0, waited
+        assert_close(_run(w4, torch, p), ref, "gemm_f16 after recovery")
+        assert w4.w4a16_check_device_error() == 0
