@@ -571,6 +571,13 @@ def per_config(torch, w4, synth, dev, stream, hbm_peak, tf_peak):
             tf = 2.0 * M * N * K / t / 1e12
             out[name] = {"us": round(t * 1e6, 2), "TFLOP/s": round(tf, 1), "frac_bf16": round(tf / tf_peak, 3),
                          "weight_sets": ns, "each": spread(torch, fn, 50, stream)}
+            # the binary16-operand variant (w4a16_gemm_f16: pre-pass + GEMM, two launches)
+            fn16 = lambda i: w4.w4a16_gemm_f16(X, sets[i % ns]["qw"], sets[i % ns]["s"], sets[i % ns]["z"], Y)
+            t16 = time_launches(torch, fn16, 20, stream)
+            tf16 = 2.0 * M * N * K / t16 / 1e12
+            out["gemm_f16_m%d_15360x3840" % M] = {"us": round(t16 * 1e6, 2), "TFLOP/s": round(tf16, 1),
+                                                  "frac_bf16": round(tf16 / tf_peak, 3), "weight_sets": ns,
+                                                  "launches_per_call": 2}
             del sets
         except Exception as e:  # the tensor-core GEMM may be unavailable on this device
             out[name] = {"unavailable": str(e).splitlines()[0][:120]}
@@ -596,10 +603,12 @@ def per_config(torch, w4, synth, dev, stream, hbm_peak, tf_peak):
             t_mm = time_launches(torch, lambda i: w4.w4a16_bf16_gemm(X, Wb[i % nw], Y), 20, stream)
             t_two = time_launches(torch, lambda i: (deq(i), w4.w4a16_bf16_gemm(X, Wb[i % nw], Y)), 20, stream)
             fused = out.get("gemm_m%d_15360x3840" % M, {}).get("us")
+            fused16 = out.get("gemm_f16_m%d_15360x3840" % M, {}).get("us")
             out[name] = {"us": round(t_two * 1e6, 2), "dequant_us": round(t_deq * 1e6, 2),
                          "bf16_gemm_us": round(t_mm * 1e6, 2),
                          "bf16_gemm_TFLOP/s": round(2.0 * M * N * K / t_mm / 1e12, 1),
-                         "fused_speedup": round(t_two * 1e6 / fused, 2) if fused else None}
+                         "fused_speedup": round(t_two * 1e6 / fused, 2) if fused else None,
+                         "fused_f16_speedup": round(t_two * 1e6 / fused16, 2) if fused16 else None}
             del sets, Wb
         except Exception as e:
             out[name] = {"unavailable": str(e).splitlines()[0][:120]}
