@@ -818,14 +818,15 @@ def profile_cases(torch, w4, dev):
             return lambda: w4.w4a16_gemv(x, qw, s, z, y)
         return setup
 
-    def gemm(M, N, K):
+    def gemm(M, N, K, f16=False):
         def setup():
             qw = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device=dev)
             s = (torch.rand(N, K // 128, device=dev) * 0.02 + 0.001).half()
             z = torch.randint(0, 16, (N, K // 128), device=dev).half()
             X = torch.randn(M, K, device=dev).bfloat16()
             Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
-            return lambda: w4.w4a16_gemm(X, qw, s, z, Y)
+            fn = w4.w4a16_gemm_f16 if f16 else w4.w4a16_gemm
+            return lambda: fn(X, qw, s, z, Y)
         return setup
 
     def moe(M):
@@ -847,6 +848,8 @@ def profile_cases(torch, w4, dev):
     return {"gemv_3840x3840": gemv(3840, 3840), "gemv_up_15360x3840": gemv(*UP),
             "gemv_down_3840x15360": gemv(*DOWN), "gemv_vocab_262144x3840": gemv(262144, 3840),
             "gemm_m128_15360x3840": gemm(128, 15360, 3840), "gemm_m2048_15360x3840": gemm(2048, 15360, 3840),
+            "gemm_f16_m128_15360x3840": gemm(128, 15360, 3840, True),
+            "gemm_f16_m2048_15360x3840": gemm(2048, 15360, 3840, True),
             "moe_fp4_64x4096x7168_top6": moe(1), "moe_fp4_gemm_m16_64x4096x7168_top6": moe(16),
             "moe_fp4_gemm_m128_64x4096x7168_top6": moe(128)}
 
