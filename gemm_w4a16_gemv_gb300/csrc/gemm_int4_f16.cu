@@ -35,7 +35,8 @@
 //    taking the chunks c = j mod n_iss into accumulator j; NT = 256 uses
 //    one (a K = 16 MMA of N = 256 keeps the tensor pipe busy by itself);
 //  * at the end warps 8-23 sum the issuers' accumulators, undo the row
-//    scale of X, round to BF16 and store Y.
+//    scale of X, round to BF16 and store Y (for N % 8 == 0 through a
+//    shared-memory tile in the idle X ring and one TMA store).
 // Every wait is bounded; on a timeout the status word is set, each role
 // still performs the arrivals the others wait for, and tensor memory is
 // released only after every MMA issued has completed.
@@ -45,6 +46,7 @@
 #include "tc_common.cuh"
 #include "tma_host.h"
 
+#include <cstring>
 #include <mutex>
 
 namespace w4 {
@@ -79,6 +81,7 @@ struct GemmF16Args {
     int M, N, K, G, nt, ntn;  // ntn: tiles along N
     int xs_n;                 // X ring depth
     int off_w, off_sz, off_bar;  // shared-memory offsets (X ring at 0)
+    int y_tma;                // Y written by one TMA store per tile (N % 8 == 0)
     unsigned int inject;
 };
 
@@ -154,7 +157,7 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
 template <bool SYM>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_int4_f16_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                     const GemmF16Args a) {
+                     const __grid_constant__ CUtensorMap tmY, const GemmF16Args a) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint16_t *s_t = reinterpret_cast<uint16_t *>(smem + a.off_sz);  // [BR][G] binary16 scales of the tile's rows
@@ -362,6 +365,10 @@ gemm_int4_f16_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_const
         named_bar_sync(2, NBW * 32);  // the row scales are in shared memory
         ok = ok && mbar_wait_lanes(lane == 0 ? &bar.accfull : nullptr, 0, a.status);
         const int rows_m = min(nt, a.M - m0);
+        // With y_tma the tile goes to shared memory as [token][128 rows] BF16
+        // -- into the X ring, idle once every MMA has completed -- and leaves
+        // by one TMA store (rows past M and N are not written).
+        uint16_t *ytile = reinterpret_cast<uint16_t *>(smem);
         if (ok) {
             tc_fence_after();
             const bool nok = n0 + r < a.N;
@@ -377,12 +384,28 @@ gemm_int4_f16_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_const
 #pragma unroll
                     for (int i = 0; i < 16; ++i) acc[i] += __uint_as_float(v[i]);
                 }
+                if (a.y_tma) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int m = m0 + 16 * p + i;
-                    if (16 * p + i < rows_m && nok)
-                        yrow[static_cast<int64_t>(m) * a.N] = f32_to_bf16_bits(acc[i] * rs_t[16 * p + i]);
+                    for (int i = 0; i < 16; ++i)
+                        ytile[(16 * p + i) * BR + r] = f32_to_bf16_bits(acc[i] * rs_t[16 * p + i]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int m = m0 + 16 * p + i;
+                        if (16 * p + i < rows_m && nok)
+                            yrow[static_cast<int64_t>(m) * a.N] = f32_to_bf16_bits(acc[i] * rs_t[16 * p + i]);
+                    }
                 }
+            }
+        }
+        if (a.y_tma) {
+            // every builder's part written (generic proxy), then one store
+            fence_proxy_async_smem();
+            named_bar_sync(3, NBW * 32);
+            if (ok && threadIdx.x == BW0 * 32) {
+                tma_store_2d(&tmY, n0, m0, ytile);
+                bulk_commit_group();
+                bulk_wait_read_all();  // shared memory is read before the CTA ends
             }
         }
         tc_fence_before();
@@ -478,7 +501,9 @@ cudaError_t launch_gemm_int4_f16(const uint16_t *X, const uint8_t *qw, const uin
     cudaError_t err = cudaGetLastError();
 
     // 2. the GEMM
-    CUtensorMap tmW, tmX;
+    CUtensorMap tmW, tmX, tmY;
+    memset(&tmY, 0, sizeof(tmY));
+    const int y_tma = N % 8 == 0 ? 1 : 0;
     if (err == cudaSuccess) {
         // packed codes as bytes [N, K/2]: box 128 bytes (256 codes) x 128 rows, 128-byte swizzle
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(N)};
@@ -501,6 +526,17 @@ cudaError_t launch_gemm_int4_f16(const uint16_t *X, const uint8_t *qw, const uin
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             err = cudaErrorInvalidValue;
     }
+    if (err == cudaSuccess && y_tma) {
+        // Y [M, N] BF16: box 128 columns (256 bytes) x NT rows, no swizzle
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 2};
+        const cuuint32_t box[2] = {BR, static_cast<cuuint32_t>(nt)};
+        const cuuint32_t estr[2] = {1, 1};
+        if (enc(&tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Y, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            err = cudaErrorInvalidValue;
+    }
     if (err == cudaSuccess) {
         GemmF16Args a;
         a.s = s;
@@ -518,6 +554,7 @@ cudaError_t launch_gemm_int4_f16(const uint16_t *X, const uint8_t *qw, const uin
         a.off_w = lay.off_w;
         a.off_sz = lay.off_sz;
         a.off_bar = lay.off_bar;
+        a.y_tma = y_tma;
         a.inject = dev.inject;
         const void *kern = sym ? reinterpret_cast<const void *>(gemm_int4_f16_kernel<true>)
                                : reinterpret_cast<const void *>(gemm_int4_f16_kernel<false>);
@@ -526,9 +563,9 @@ cudaError_t launch_gemm_int4_f16(const uint16_t *X, const uint8_t *qw, const uin
         if (err == cudaSuccess) {
             const unsigned grid = static_cast<unsigned>(ntn * ntm);
             if (sym)
-                gemm_int4_f16_kernel<true><<<grid, THREADS, smem, st>>>(tmW, tmX, a);
+                gemm_int4_f16_kernel<true><<<grid, THREADS, smem, st>>>(tmW, tmX, tmY, a);
             else
-                gemm_int4_f16_kernel<false><<<grid, THREADS, smem, st>>>(tmW, tmX, a);
+                gemm_int4_f16_kernel<false><<<grid, THREADS, smem, st>>>(tmW, tmX, tmY, a);
             err = cudaGetLastError();
         }
     }

@@ -176,6 +176,18 @@ __device__ __forceinline__ void tma_load_2d_hint(void *dst, const CUtensorMap *t
         : "memory");
 }
 
+// TMA store of a 2-D box from this CTA's shared memory (bulk async group):
+// elements of the box outside the tensor are not written.  The coordinates
+// must not be negative; x times the element size a multiple of 16 bytes.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *tmap, int c0, int c1, const void *src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(tmap),
+                 "r"(c0), "r"(c1), "r"(smem_u32(src))
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Until every committed bulk store of this thread has read its shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
