@@ -111,3 +111,16 @@ def test_moe_gemm_full_size_sampled(full_moe, M):
     ref, bad = _ref(sub)
     assert bad == 0
     assert_close(y[toks][:, :, rows], ref, "moe gemm full M=%d" % M)
+
+
+@pytest.mark.parametrize("E,N,K,M,topk", [
+    (2, 64, 32768, 3, 2),       # long K: 128 chunks, the weight ring wrapping many times
+    (64, 256, 512, 1024, 8),    # 8192 (token, slot) pairs: tiles of 128 rows per expert, several each
+    (4096, 64, 256, 4, 2),      # many experts: the routing kernel's per-expert counters (48 KB)
+])
+def test_moe_gemm_large_sizes(E, N, K, M, topk):
+    torch, w4 = cuda_or_skip()
+    m = synth.fp4_moe_batch_problem(E, N, K, M, topk, seed=E + M)
+    ref, bad = _ref(m)
+    assert bad == 0
+    assert_close(_run(w4, torch, m), ref, "moe gemm E=%d M=%d K=%d" % (E, M, K))
