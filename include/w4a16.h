@@ -122,7 +122,8 @@ int w4a16_gemm(const uint16_t *X, const uint8_t *qw, const uint16_t *s,
  * the faster one from M = 256 on.
  * Layouts and requirements: those of w4a16_gemm (any M >= 1, any N).
  * Scratch: M*K*2 + 4*M bytes, stream-ordered, from a memory pool that the
- * library keeps per device (kept reserved between calls).
+ * library keeps per device (kept reserved between calls); under stream
+ * capture it becomes an allocation of the CUDA graph.
  */
 int w4a16_gemm_f16(const uint16_t *X, const uint8_t *qw, const uint16_t *s,
                    const uint16_t *z, uint16_t *Y, int64_t M, int64_t N,
@@ -178,7 +179,8 @@ int fp4_moe_gemv(const uint16_t *x, const uint8_t *qw, const uint16_t *s,
  *                used by this call only while it runs on `stream` (the
  *                routing table and the tokens gathered per expert); it need
  *                not be zeroed.
- * Three launches on `stream`: routing, gathering, the tensor-core GEMM.
+ * Three launches on `stream`: routing, gathering, the tensor-core GEMM (they
+ * can be captured in a CUDA graph; each replay routes the ids it finds).
  * Arithmetic: each weight e2m1 * s is rounded once to binary16 (relative
  * error at most 2^-11 for |s| in [2^-13, 10922]; smaller scales round to
  * binary16 subnormals, larger ones overflow); each token row is scaled by

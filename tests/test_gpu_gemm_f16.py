@@ -100,3 +100,29 @@ def test_gemm_f16_bounded_wait_reports_timeout_and_recovers():
         assert 1.5 < waited < 30.0, waited
         assert_close(_run(w4, torch, p), ref, "gemm_f16 after recovery")
         assert w4.w4a16_check_device_error() == 0
+
+
+def test_gemm_f16_in_a_captured_graph():
+    """The pre-pass scratch comes from a stream-ordered pool, so the call can
+    be captured: replays after the inputs change give the new result."""
+    torch, w4 = cuda_or_skip()
+    M, N, K = 300, 136, 512
+    p = synth.int4_problem(N, K, M=M, seed=21)
+    X = dev_tensor(p["x"], torch.bfloat16).view(M, K)
+    qw, s, z = dev_tensor(p["qw"], torch.uint8), dev_tensor(p["s"], torch.float16), dev_tensor(p["z"], torch.float16)
+    Y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        w4.w4a16_gemm_f16(X, qw, s, z, Y)  # warm-up outside capture
+        st.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            w4.w4a16_gemm_f16(X, qw, s, z, Y)
+    for seed in (22, 23):
+        q = synth.int4_problem(N, K, M=M, seed=seed)
+        X.copy_(dev_tensor(q["x"], torch.bfloat16).view(M, K))
+        g.replay()
+        torch.cuda.synchronize()
+        ref = oracle.gemm_int4(q["x"], p["qw"], p["s"], p["z"], K=K)
+        assert_close(host_bits16(Y).reshape(M, N), ref, "gemm_f16 graph replay")
+    assert w4.w4a16_check_device_error() == 0

@@ -124,3 +124,29 @@ def test_moe_gemm_large_sizes(E, N, K, M, topk):
     ref, bad = _ref(m)
     assert bad == 0
     assert_close(_run(w4, torch, m), ref, "moe gemm E=%d M=%d K=%d" % (E, M, K))
+
+
+def test_moe_gemm_in_a_captured_graph():
+    """Caller scratch and device ids: the three launches capture into a graph
+    and each replay routes the ids it finds."""
+    torch, w4 = cuda_or_skip()
+    m = synth.fp4_moe_batch_problem(8, 96, 512, 12, 3, seed=31)
+    X = dev_tensor(m["x"], torch.bfloat16)
+    qw, s = dev_tensor(m["qw"], torch.uint8), dev_tensor(m["s"], torch.float16)
+    ids = dev_tensor(m["ids"], torch.int32)
+    Y = torch.empty(12, 3, 96, dtype=torch.bfloat16, device="cuda")
+    scratch = torch.empty(w4.fp4_moe_gemm_scratch_bytes(12, 3, 8, 512), dtype=torch.uint8, device="cuda")
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        w4.fp4_moe_gemm(X, qw, s, ids, Y, scratch)
+        st.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            w4.fp4_moe_gemm(X, qw, s, ids, Y, scratch)
+    for new_ids in (m["ids"], np.ascontiguousarray(m["ids"][:, ::-1])):
+        ids.copy_(dev_tensor(new_ids, torch.int32))
+        g.replay()
+        torch.cuda.synchronize()
+        ref, bad = _ref(m, new_ids)
+        assert_close(host_bits16(Y), ref, "moe gemm graph replay")
+    assert w4.w4a16_check_device_error() == 0
