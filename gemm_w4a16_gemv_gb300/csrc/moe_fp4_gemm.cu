@@ -13,8 +13,12 @@
 //     scaled by a power of two per token so that its largest |x| lands in
 //     [2^14, 2^15) (exact for every value within 2^29 of that maximum); the
 //     output rows of invalid ids are written as zeros;
-//  3. the GEMM on the tcgen05 tensor cores: one CTA per (tile, 128 weight
-//     rows).  Builder warps decode the E2M1 codes exactly to binary16
+//  3. the GEMM on the tcgen05 tensor cores: one persistent CTA per SM,
+//     looping over the work items (tile, 128 weight rows), so that the
+//     weight stream runs on from one item into the next with no CTA launch,
+//     setup, pipeline fill or drain between them (each cost about a fifth of
+//     an item's time when every item was a CTA of its own).  Builder warps
+//     decode the E2M1 codes exactly to binary16
 //     (cvt.rn.f16x2.e2m1x2) and multiply by the group scale in binary16 --
 //     the weight e2m1 * s rounded once to binary16, a relative error of at
 //     most 2^-11 (the only rounding of the operands) -- into the A operand in
@@ -22,11 +26,12 @@
 //     swizzle).  The tile has few token rows (the MMA's N is 16 for a
 //     typical expert), and MMAs issued by one thread run one after another at
 //     about 100-150 SM cycles each whatever N is, while MMAs from different
-//     warps into different accumulators overlap.  So 4 issuer warps (2 for
-//     tiles of more than 64 rows) take turns by 128-K chunk, each into an
-//     FP32 accumulator of its own; the epilogue sums them, undoes each
-//     token's power-of-two scale, rounds to BF16 and scatters the rows to
-//     their (token, slot) places.
+//     warps into different accumulators overlap.  So issuer warps -- 4
+//     while the largest tile has at most 32 rows, 2 up to 64, else 1 -- take
+//     turns by 128-K chunk, each into an FP32 accumulator of its own; four epilogue warps sum them, undo each
+//     token's power-of-two scale, round to BF16 and scatter the rows to
+//     their (token, slot) places while the next item's MMAs run into the
+//     other accumulator set.
 // Every wait is bounded; on a timeout the status word is set, each role
 // still performs the arrivals the others wait for, and tensor memory is
 // released only after the MMAs issued have completed.
@@ -43,7 +48,7 @@ constexpr int BR = 128;               // weight rows per CTA (the MMA's M; TMEM 
 constexpr int BT = 128;               // token rows per tile at most (the MMA's N)
 constexpr int CK = 128;               // K per chunk: one A stage, one X stage
 constexpr int SCK = 256;              // K per weight stage: 128 code bytes and 8 scales per row
-constexpr int XS_MAX = 4;             // X stages: a multiple of the issuer count, so that each
+constexpr int XS_MAX = 8;             // X stages: a multiple of the issuer count, so that each
                                       // issuer waits on stages of its own chunks only (in order)
 constexpr int WS_MAX = 12;            // weight stages (codes + scales), as many as fit
 constexpr int BG = 2;                 // builder groups: chunk c is built by group c mod 2
@@ -53,14 +58,18 @@ constexpr int X_BOX_ROWS = 16;        // rows per X TMA box (a tile loads as man
 constexpr int W_STAGE = BR * 128;     // 16 KB of packed codes
 constexpr int S_STAGE = BR * 16;      // 2 KB of scales
 // Shared memory holds the X ring (stages of 256 bytes per token row of the
-// tile) and as many weight stages as fit after it (10 for a 16-row tile, 6
-// for a 128-row tile): the weight ring keeps the HBM reads in flight.
+// largest tile: 8 stages for tiles of up to 32 rows, 4 beyond) and as many
+// weight stages as fit after it: the weight ring keeps the HBM reads in
+// flight.
 constexpr int POOL = 208 * 1024;
-constexpr int THREADS = 512;          // 16 warps: 0 weights TMA, 1 tokens TMA, 2-5 MMA, 6 TMEM, 8-15 builders
+constexpr int THREADS = 640;          // 20 warps: 0 weights TMA, 1 tokens TMA, 2-5 MMA, 6 TMEM,
+                                      // 8-15 builders, 16-19 epilogue
 constexpr int ISS0 = 2;               // first issuer warp
 constexpr int BW0 = 8;                // first builder warp (warp & 3 = its TMEM lane quarter)
+constexpr int EW0 = 16;               // first epilogue warp (warp & 3 = its TMEM lane quarter)
+constexpr int NEW = 4;                // epilogue warps
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_ACC = 0;        // accumulators: n_iss x nmma <= 256 columns
+constexpr uint32_t TM_ACC = 0;        // two accumulator sets of n_iss x (largest tile's N) <= 128 columns
 constexpr uint32_t TM_A = 256;        // operand stages after them
 constexpr int ROUTE_THREADS = 1024;
 constexpr int GATHER_THREADS = 256;
@@ -84,7 +93,7 @@ __host__ __device__ inline int64_t align256(int64_t v) { return (v + 255) & ~int
 __host__ __device__ inline MoeScratch moe_scratch_layout(int64_t P, int64_t E, int64_t K) {
     MoeScratch l;
     l.tmax = static_cast<int>((P + BT - 1) / BT + (E < P ? E : P));
-    l.tiles_off = 256;  // the tile count lives at offset 0
+    l.tiles_off = 256;  // the tile count and the largest tile's rows live at offsets 0 and 4
     l.perm_off = align256(l.tiles_off + 16 * static_cast<int64_t>(l.tmax));
     l.posof_off = align256(l.perm_off + 4 * P);
     l.scale_off = align256(l.posof_off + 4 * P);
@@ -101,7 +110,6 @@ __global__ void __launch_bounds__(ROUTE_THREADS) moe_route_kernel(const int32_t 
     int *cnt = sm;           // [E]
     int *off = sm + E;       // [E]
     int *cur = sm + 2 * E;   // [E]
-    __shared__ int ntiles;
     const MoeScratch l = moe_scratch_layout(P, E, 0);
     MoeTile *tiles = reinterpret_cast<MoeTile *>(scratch + l.tiles_off);
     int *perm = reinterpret_cast<int *>(scratch + l.perm_off);
@@ -117,8 +125,9 @@ __global__ void __launch_bounds__(ROUTE_THREADS) moe_route_kernel(const int32_t 
     }
     if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(status, kDevBadExpert);
     if (threadIdx.x == 0) {
-        // exclusive prefix sum and the tile table, experts in order
-        int acc = 0, t = 0;
+        // exclusive prefix sum and the tile table, experts in order; the
+        // tile count and the largest tile's rows go to the scratch header
+        int acc = 0, t = 0, maxrows = 0;
         for (int e = 0; e < E; ++e) {
             off[e] = acc;
             for (int r = 0; r < cnt[e]; r += BT) {
@@ -128,11 +137,12 @@ __global__ void __launch_bounds__(ROUTE_THREADS) moe_route_kernel(const int32_t 
                 tl.rows = cnt[e] - r < BT ? cnt[e] - r : BT;
                 tl.pad = 0;
                 tiles[t++] = tl;
+                maxrows = tl.rows > maxrows ? tl.rows : maxrows;
             }
             acc += cnt[e];
         }
-        ntiles = t;
-        *reinterpret_cast<int *>(scratch) = t;
+        reinterpret_cast<int *>(scratch)[0] = t;
+        reinterpret_cast<int *>(scratch)[1] = maxrows;
     }
     __syncthreads();
     // positions: within an expert in arrival order (each output row is
@@ -193,22 +203,36 @@ struct MoeBarriers {
     uint64_t xfull[XS_MAX], xempty[XS_MAX];
     uint64_t wfull[WS_MAX], wempty[WS_MAX];
     uint64_t aready[AP], aempty[AP];
-    uint64_t accfull;   // every issuer's MMAs completed (n_iss arrivals)
-    uint64_t done;      // builders finished with tensor memory
+    uint64_t accfull[2];   // an item's accumulators complete (n_iss arrivals), by item parity
+    uint64_t accempty[2];  // ... read by the epilogue warps (NEW arrivals)
+    uint64_t drained;      // every MMA issued has completed (n_iss arrivals, at the end)
+    uint64_t done;         // the epilogue warps finished (NEW arrivals)
     uint32_t tmem_holder;
 };
 
-// Two E2M1 codes (the low byte of b) times a binary16 scale pair -> binary16
-// pair, low half from the low nibble (even k): decode exact, one rounding.
-__device__ __forceinline__ uint32_t e2m1x2_times(uint32_t b, uint32_t s2) {
-    uint32_t r;
-    asm("{\n\t.reg .b8 t;\n\t.reg .b32 h;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 h, t;\n\t"
-        "mul.rn.f16x2 %0, h, %2;\n\t}"
-        : "=r"(r)
-        : "r"(b), "r"(s2));
-    return r;
+// Eight E2M1 codes (the four bytes of w) times a binary16 scale pair -> four
+// binary16 pairs, o[i] from byte i, low half from its low nibble (even k):
+// decode exact, one rounding.  The word is split into its bytes by one
+// vector move, so no shift or mask precedes a conversion.
+__device__ __forceinline__ void e2m1x8_times(uint32_t w, uint32_t s2, uint32_t *o) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t.reg .b32 h0, h1, h2, h3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 h0, b0;\n\tcvt.rn.f16x2.e2m1x2 h1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 h2, b2;\n\tcvt.rn.f16x2.e2m1x2 h3, b3;\n\t"
+        "mul.rn.f16x2 %0, h0, %5;\n\tmul.rn.f16x2 %1, h1, %5;\n\t"
+        "mul.rn.f16x2 %2, h2, %5;\n\tmul.rn.f16x2 %3, h3, %5;\n\t}"
+        : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+        : "r"(w), "r"(s2));
 }
 
+// One persistent CTA per SM loops over the work items (tile t, block b of 128
+// weight rows), b fastest.  Every ring runs on across the items (its slot
+// and phase from a counter over all of this CTA's chunks or stages); the
+// accumulators alternate by item parity, so the epilogue warps drain item s
+// while the MMAs of item s + 1 run.  The layout (X stage rows, accumulator
+// columns, the issuer count, the ring depths) is set per launch from the
+// largest tile; each item loads only its own tile's token rows and
+// multiplies with its own N.
 __global__ void __launch_bounds__(THREADS, 1)
 moe_fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS,
                     const __grid_constant__ CUtensorMap tmX, const MoeGemmArgs a) {
@@ -217,30 +241,33 @@ moe_fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
     MoeBarriers &bar = *reinterpret_cast<MoeBarriers *>(smem + POOL);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // the tile: read after the routing launch has finished (stream order)
+    // the routing: read after the routing launch has finished (stream order)
     pdl_wait();
     const MoeScratch l = moe_scratch_layout(a.P, a.E, a.K);
-    const int ntiles = *reinterpret_cast<const int *>(a.scratch);
-    if (static_cast<int>(blockIdx.x) >= ntiles) return;  // uniform over the CTA
-    const MoeTile tile = reinterpret_cast<const MoeTile *>(a.scratch + l.tiles_off)[blockIdx.x];
-    const int n0 = blockIdx.y * BR;
-    const int wrow0 = tile.expert * a.N + n0;               // first weight row in the [E*N] stack
-    const int nmma = ((tile.rows + 15) / 16) * 16;          // the MMA's N
-    const int xboxes = nmma / X_BOX_ROWS;
-    const int nch = a.nchunks;
-    // issuers: as many as the accumulators fit in 256 columns, at most one
-    // per chunk (each issuer's first chunk initialises its accumulator)
-    int n_iss = nmma <= 64 ? MAX_ISS : 2;
-    n_iss = n_iss < nch ? n_iss : nch;
-    // the ring: X stages of nmma rows x 128 K (two 64-K halves), then the
-    // weight stages (codes, 1024-aligned, then their scales)
-    const int x_half = nmma * 128;
+    const int ntiles = reinterpret_cast<const int *>(a.scratch)[0];
+    const int maxrows = reinterpret_cast<const int *>(a.scratch)[1];
+    const MoeTile *tiles = reinterpret_cast<const MoeTile *>(a.scratch + l.tiles_off);
+    const int nblk = (a.N + BR - 1) / BR;
+    const int total = ntiles * nblk;
+    if (static_cast<int>(blockIdx.x) >= total) return;  // uniform over the CTA
+    const int nitems = (total - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                       static_cast<int>(gridDim.x);
+    // the largest tile sets the layout (X stage rows, accumulator columns);
+    // each item loads its own tile's rows and multiplies with its own N
+    const int nmax = ((maxrows + 15) / 16) * 16;
+    const int nch = a.nchunks;  // even (K % 256 == 0)
+    // issuers: as many as two accumulator sets fit in 256 columns; they take
+    // turns by chunk within an item, so their count divides the chunks
+    int n_iss = nmax <= 32 ? MAX_ISS : (nmax <= 64 ? 2 : 1);
+    if (nch % n_iss != 0) n_iss = 2;
+    const int x_half = nmax * 128;
     const int x_stage = 2 * x_half;
-    const int xs_n = XS_MAX;
+    const int xs_n = nmax <= 32 ? 8 : 4;  // a multiple of n_iss
     const int off_w = xs_n * x_stage;
     int ws_n = (POOL - off_w) / (W_STAGE + S_STAGE);
     ws_n = ws_n < WS_MAX ? ws_n : WS_MAX;
     const int off_s = off_w + ws_n * W_STAGE;
+    const int nsc = a.K / SCK;  // weight stages per item
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < xs_n; ++i) {
@@ -255,8 +282,12 @@ moe_fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
             mbar_init(&bar.aready[i], 4);  // the 4 builder warps of the chunk's group
             mbar_init(&bar.aempty[i], 1);
         }
-        mbar_init(&bar.accfull, n_iss);
-        mbar_init(&bar.done, 4 * BG);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar.accfull[i], n_iss);
+            mbar_init(&bar.accempty[i], NEW);
+        }
+        mbar_init(&bar.drained, n_iss);
+        mbar_init(&bar.done, NEW);
         fence_barrier_init();
     }
     if (warp == 6) {  // this warp allocates tensor memory and frees it at the end
@@ -274,169 +305,207 @@ moe_fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
             const uint64_t pol = policy_evict_first();
             tma_prefetch_desc(&tmW);
             tma_prefetch_desc(&tmS);
-            const int nsc = (nch + 1) / 2;
-            const int nissue = (a.inject & kInjectStallPipeline) ? 0 : nsc;
+            const int nissue = (a.inject & kInjectStallPipeline) ? 0 : nitems;
             int issued = 0;
-            for (int sc = 0; sc < nissue; ++sc, ++issued) {
-                const int ws = sc % ws_n;
-                if (sc >= ws_n && !mbar_wait(&bar.wempty[ws], ((sc / ws_n) - 1) & 1, a.status)) break;
-                mbar_arrive_expect_tx(&bar.wfull[ws], W_STAGE + S_STAGE);
+            bool ok = true;
+            for (int it = 0; ok && it < nissue; ++it) {
+                const int item = static_cast<int>(blockIdx.x) + it * static_cast<int>(gridDim.x);
+                const MoeTile tile = tiles[item / nblk];
                 // rows past the stack's end read as zeros; rows of the next
-                // expert (tiles ending past N) are computed and not stored
-                tma_load_2d_hint(smem + off_w + ws * W_STAGE, &tmW, sc * 128, wrow0, &bar.wfull[ws], pol);
-                tma_load_2d_hint(smem + off_s + ws * S_STAGE, &tmS, sc * 8, wrow0, &bar.wfull[ws], pol);
+                // expert (blocks ending past N) are computed and not stored
+                const int wrow0 = tile.expert * a.N + (item % nblk) * BR;
+                for (int sc = 0; sc < nsc; ++sc, ++issued) {
+                    const int ws = issued % ws_n;
+                    if (issued >= ws_n && !mbar_wait(&bar.wempty[ws], ((issued / ws_n) - 1) & 1, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&bar.wfull[ws], W_STAGE + S_STAGE);
+                    tma_load_2d_hint(smem + off_w + ws * W_STAGE, &tmW, sc * 128, wrow0, &bar.wfull[ws], pol);
+                    tma_load_2d_hint(smem + off_s + ws * S_STAGE, &tmS, sc * 8, wrow0, &bar.wfull[ws], pol);
+                }
             }
             // no copy in flight when the CTA exits
-            for (int it = issued > ws_n ? issued - ws_n : 0; it < issued; ++it)
-                mbar_wait(&bar.wfull[it % ws_n], (it / ws_n) & 1, nullptr);
+            for (int i = issued > ws_n ? issued - ws_n : 0; i < issued; ++i)
+                mbar_wait(&bar.wfull[i % ws_n], (i / ws_n) & 1, nullptr);
         }
     } else if (warp == 1) {
         // ------------------------------------------ token rows (TMA)
         if (lane == 0) {
             const uint64_t pol = policy_evict_last();
             tma_prefetch_desc(&tmX);
-            const int nissue = (a.inject & kInjectStallPipeline) ? 0 : nch;
+            const int nissue = (a.inject & kInjectStallPipeline) ? 0 : nitems;
             int issued = 0;
-            for (int c = 0; c < nissue; ++c, ++issued) {
-                const int xs = c % xs_n;
-                if (c >= xs_n && !mbar_wait(&bar.xempty[xs], ((c / xs_n) - 1) & 1, a.status)) break;
-                mbar_arrive_expect_tx(&bar.xfull[xs], 2 * xboxes * X_BOX_ROWS * 128);
-                unsigned char *dst = smem + xs * x_stage;
-                for (int h = 0; h < 2; ++h)          // the chunk's two 64-K boxes
-                    for (int b = 0; b < xboxes; ++b)  // 16 rows each
-                        tma_load_2d_hint(dst + h * x_half + b * X_BOX_ROWS * 128, &tmX, c * CK + h * 64,
-                                         tile.row0 + b * X_BOX_ROWS, &bar.xfull[xs], pol);
+            bool ok = true;
+            for (int it = 0; ok && it < nissue; ++it) {
+                const int item = static_cast<int>(blockIdx.x) + it * static_cast<int>(gridDim.x);
+                const MoeTile tile = tiles[item / nblk];
+                const int xboxes = (tile.rows + X_BOX_ROWS - 1) / X_BOX_ROWS;
+                for (int c = 0; c < nch; ++c, ++issued) {
+                    const int xs = issued % xs_n;
+                    if (issued >= xs_n && !mbar_wait(&bar.xempty[xs], ((issued / xs_n) - 1) & 1, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&bar.xfull[xs], 2 * xboxes * X_BOX_ROWS * 128);
+                    unsigned char *dst = smem + xs * x_stage;
+                    for (int h = 0; h < 2; ++h)          // the chunk's two 64-K boxes
+                        for (int b = 0; b < xboxes; ++b)  // 16 rows each
+                            tma_load_2d_hint(dst + h * x_half + b * X_BOX_ROWS * 128, &tmX, c * CK + h * 64,
+                                             tile.row0 + b * X_BOX_ROWS, &bar.xfull[xs], pol);
+                }
             }
-            for (int it = issued > xs_n ? issued - xs_n : 0; it < issued; ++it)
-                mbar_wait(&bar.xfull[it % xs_n], (it / xs_n) & 1, nullptr);
+            for (int i = issued > xs_n ? issued - xs_n : 0; i < issued; ++i)
+                mbar_wait(&bar.xfull[i % xs_n], (i / xs_n) & 1, nullptr);
         }
     } else if (warp >= ISS0 && warp < ISS0 + n_iss) {
         // ------------------------------------------------ MMA issuers
-        // issuer j takes the chunks c = j mod n_iss into accumulator j
+        // issuer j takes the chunks c = j mod n_iss of each item into
+        // accumulator j of the item's set
         const int j = warp - ISS0;
-        const uint32_t d_acc = tmem + TM_ACC + static_cast<uint32_t>(j * nmma);
-        const uint32_t idesc = idesc_kind_f16(BR, nmma, 0u);  // FP16 x FP16 -> FP32, M = 128, N = nmma
         bool ok = !(a.inject & kInjectStallConsumers);
-        for (int c = j; ok && c < nch; c += n_iss) {
-            const int ap = c % AP, xs = c % xs_n;
-            uint64_t *wbar = nullptr;
-            uint32_t par = 0;
-            if (lane == 0) {
-                wbar = &bar.aready[ap];
-                par = (c / AP) & 1;
-            } else if (lane == 1) {
-                wbar = &bar.xfull[xs];
-                par = (c / xs_n) & 1;
-            }
-            if (!mbar_wait_lanes(wbar, par, a.status)) {
+        for (int it = 0; ok && it < nitems; ++it) {
+            const int set = it & 1;
+            const int item = static_cast<int>(blockIdx.x) + it * static_cast<int>(gridDim.x);
+            const int nt = ((tiles[item / nblk].rows + 15) / 16) * 16;  // this item's MMA N
+            const uint32_t idesc = idesc_kind_f16(BR, nt, 0u);            // FP16 x FP16 -> FP32, M = 128
+            // the epilogue has read this set's accumulators of item it - 2
+            if (it >= 2 && !mbar_wait_lanes(lane == 0 ? &bar.accempty[set] : nullptr, ((it >> 1) - 1) & 1,
+                                            a.status)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            {
+            const uint32_t d_acc = tmem + TM_ACC + static_cast<uint32_t>(set * 128 + j * nmax);
+            for (int c = j; c < nch; c += n_iss) {
+                const int gc = it * nch + c;
+                const int ap = gc % AP, xs = gc % xs_n;
+                uint64_t *wbar = nullptr;
+                uint32_t par = 0;
+                if (lane == 0) {
+                    wbar = &bar.aready[ap];
+                    par = (gc / AP) & 1;
+                } else if (lane == 1) {
+                    wbar = &bar.xfull[xs];
+                    par = (gc / xs_n) & 1;
+                }
+                if (!mbar_wait_lanes(wbar, par, a.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
                 const uint32_t b_addr = smem_u32(smem + xs * x_stage);
 #pragma unroll
                 for (int k = 0; k < CK / 16; ++k)
                     umma_f16_tmem_a_w(d_acc, tmem + TM_A + ap * 64 + 8 * k,
                                       smem_desc_sw128_kmajor(b_addr + (k >> 2) * x_half + 32 * (k & 3)), idesc,
-                                    (c != j) || (k != 0));
+                                      (c != j) || (k != 0));
                 umma_commit_w(&bar.xempty[xs]);
                 umma_commit_w(&bar.aempty[ap]);
+                __syncwarp();
             }
+            // the item's accumulators are complete once its MMAs have
+            // completed (after a timeout too, so that the epilogue's wait ends)
+            umma_commit_w(&bar.accfull[set]);
             __syncwarp();
         }
-        // the accumulators are complete once every MMA issued has completed
-        // (on a timeout the epilogue's wait ends as well, with values it
-        // does not store)
-        umma_commit_w(&bar.accfull);
+        umma_commit_w(&bar.drained);
         __syncwarp();
     } else if (warp == 6) {
         // tensor memory is freed only after every MMA has completed and the
         // epilogue has read the accumulators
-        mbar_wait(&bar.accfull, 0, nullptr);
+        mbar_wait(&bar.drained, 0, nullptr);
         mbar_wait(&bar.done, 0, a.status);
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
-    } else if (warp >= BW0) {
-        // ------------------------------ operand builders, then the epilogue
-        const int q = warp & 3;                 // TMEM lane quarter: weight rows 32 q .. 32 q + 31
-        const int grp = (warp - BW0) >> 2;      // builder group: chunks grp, grp + BG, ...
-        const int r = q * 32 + lane;            // weight row of this thread
+    } else if (warp >= BW0 && warp < EW0) {
+        // -------------------------------------------- operand builders
+        const int q = warp & 3;            // TMEM lane quarter: weight rows 32 q .. 32 q + 31
+        const int grp = (warp - BW0) >> 2;  // chunks grp, grp + 2, ... of every item
+        const int r = q * 32 + lane;       // weight row of this thread
         const uint32_t t_lane = static_cast<uint32_t>(q * 32) << 16;
         bool ok = true;
-        for (int c = grp; ok && c < nch; c += BG) {
-            const int sc = c >> 1, ws = sc % ws_n, half = c & 1, ap = c % AP;
-            uint64_t *wbar = nullptr;
-            uint32_t wpar = 0;
-            if (lane == 0) {
-                wbar = &bar.wfull[ws];
-                wpar = (sc / ws_n) & 1;
-            } else if (lane == 1 && c >= AP) {
-                wbar = &bar.aempty[ap];
-                wpar = ((c - AP) / AP) & 1;
-            }
-            if (!mbar_wait_lanes(wbar, wpar, a.status)) {
-                ok = false;
-                break;
-            }
-            // this row's 64 code bytes of the chunk (16-byte chunks 4 half +
-            // 0..3 of the swizzled row, chunk j at j ^ (r mod 8)) and its four
-            // group scales (8 per 256-K stage)
-            const unsigned char *wrow = smem + off_w + ws * W_STAGE + r * 128;
-            uint32_t wds[16];
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
-                const uint4 v = *reinterpret_cast<const uint4 *>(wrow + (((4 * half + c4) ^ (r & 7)) << 4));
-                wds[4 * c4] = v.x;
-                wds[4 * c4 + 1] = v.y;
-                wds[4 * c4 + 2] = v.z;
-                wds[4 * c4 + 3] = v.w;
-            }
-            const uint4 sv = *reinterpret_cast<const uint4 *>(smem + off_s + ws * S_STAGE + r * 16);
-            const uint32_t s01 = half ? sv.z : sv.x, s23 = half ? sv.w : sv.y;  // groups 4 half + 0..3
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                // 64 codes (groups 2 cc, 2 cc + 1 of the chunk) -> 32 columns
-                uint32_t cols[32];
-#pragma unroll
-                for (int g2 = 0; g2 < 2; ++g2) {
-                    const uint32_t sg = cc ? (g2 ? s23 >> 16 : s23 & 0xFFFFu) : (g2 ? s01 >> 16 : s01 & 0xFFFFu);
-                    const uint32_t s2 = sg | (sg << 16);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint32_t w = wds[8 * cc + 4 * g2 + i];
-                        cols[16 * g2 + 4 * i + 0] = e2m1x2_times(w, s2);
-                        cols[16 * g2 + 4 * i + 1] = e2m1x2_times(w >> 8, s2);
-                        cols[16 * g2 + 4 * i + 2] = e2m1x2_times(w >> 16, s2);
-                        cols[16 * g2 + 4 * i + 3] = e2m1x2_times(w >> 24, s2);
-                    }
+        for (int it = 0; ok && it < nitems; ++it) {
+            for (int c = grp; c < nch; c += BG) {
+                const int gc = it * nch + c;
+                const int gs = gc >> 1, ws = gs % ws_n, half = c & 1, ap = gc % AP;
+                uint64_t *wbar = nullptr;
+                uint32_t wpar = 0;
+                if (lane == 0) {
+                    wbar = &bar.wfull[ws];
+                    wpar = (gs / ws_n) & 1;
+                } else if (lane == 1 && gc >= AP) {
+                    wbar = &bar.aempty[ap];
+                    wpar = ((gc - AP) / AP) & 1;
                 }
-                tmem_st_32x32b_x32(tmem + t_lane + TM_A + ap * 64 + 32 * cc, cols);
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&bar.aready[ap]);
-                mbar_arrive(&bar.wempty[ws]);
+                if (!mbar_wait_lanes(wbar, wpar, a.status)) {
+                    ok = false;
+                    break;
+                }
+                // this row's 64 code bytes of the chunk (16-byte chunks 4 half
+                // + 0..3 of the swizzled row, chunk j at j ^ (r mod 8)) and its
+                // four group scales (8 per 256-K stage)
+                const unsigned char *wrow = smem + off_w + ws * W_STAGE + r * 128;
+                uint32_t wds[16];
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(wrow + (((4 * half + c4) ^ (r & 7)) << 4));
+                    wds[4 * c4] = v.x;
+                    wds[4 * c4 + 1] = v.y;
+                    wds[4 * c4 + 2] = v.z;
+                    wds[4 * c4 + 3] = v.w;
+                }
+                const uint4 sv = *reinterpret_cast<const uint4 *>(smem + off_s + ws * S_STAGE + r * 16);
+                const uint32_t s01 = half ? sv.z : sv.x, s23 = half ? sv.w : sv.y;  // groups 4 half + 0..3
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    // 64 codes (groups 2 cc, 2 cc + 1 of the chunk) -> 32 columns
+                    uint32_t cols[32];
+#pragma unroll
+                    for (int g2 = 0; g2 < 2; ++g2) {
+                        const uint32_t sg =
+                            cc ? (g2 ? s23 >> 16 : s23 & 0xFFFFu) : (g2 ? s01 >> 16 : s01 & 0xFFFFu);
+                        const uint32_t s2 = sg | (sg << 16);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) e2m1x8_times(wds[8 * cc + 4 * g2 + i], s2, &cols[16 * g2 + 4 * i]);
+                    }
+                    tmem_st_32x32b_x32(tmem + t_lane + TM_A + ap * 64 + 32 * cc, cols);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&bar.aready[ap]);
+                    mbar_arrive(&bar.wempty[ws]);
+                }
             }
         }
-        // epilogue: group g stores the 16-column pieces p = g, g + BG, ... of
-        // the tile's token columns, each the sum of the n_iss accumulators
-        ok = ok && mbar_wait_lanes(lane == 0 ? &bar.accfull : nullptr, 0, a.status);
-        if (ok) {
+    } else if (warp >= EW0) {
+        // ----------------------------------------------------- epilogue
+        // the sum of the item's n_iss accumulators per 16-column piece, each
+        // token's power-of-two scale undone, scattered to (token, slot) rows
+        const int q = warp & 3;
+        const int r = q * 32 + lane;
+        const uint32_t t_lane = static_cast<uint32_t>(q * 32) << 16;
+        const float *rowscale = reinterpret_cast<const float *>(a.scratch + l.scale_off);
+        const int *perm = reinterpret_cast<const int *>(a.scratch + l.perm_off);
+        for (int it = 0; it < nitems; ++it) {
+            const int item = static_cast<int>(blockIdx.x) + it * static_cast<int>(gridDim.x);
+            const MoeTile tile = tiles[item / nblk];
+            const int n0 = (item % nblk) * BR;
+            const int set = it & 1;
+            if (!mbar_wait_lanes(lane == 0 ? &bar.accfull[set] : nullptr, (it >> 1) & 1, a.status)) break;
             tc_fence_after();
-            const float *rowscale = reinterpret_cast<const float *>(a.scratch + l.scale_off);
-            const int *perm = reinterpret_cast<const int *>(a.scratch + l.perm_off);
             const bool nok = n0 + r < a.N;
-            for (int p = grp; 16 * p < tile.rows; p += BG) {
+            for (int p = 0; 16 * p < tile.rows; ++p) {
                 float acc[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
-                for (int j = 0; j < n_iss; ++j) {
+                for (int jj = 0; jj < n_iss; ++jj) {
                     uint32_t v[16];
-                    tmem_ld_32x32b_x16(tmem + t_lane + TM_ACC + static_cast<uint32_t>(j * nmma + 16 * p), v);
+                    tmem_ld_32x32b_x16(tmem + t_lane + TM_ACC + static_cast<uint32_t>(set * 128 + jj * nmax + 16 * p),
+                                       v);
                     tmem_ld_wait();
 #pragma unroll
                     for (int i = 0; i < 16; ++i) acc[i] += __uint_as_float(v[i]);
@@ -450,6 +519,9 @@ moe_fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
                     }
                 }
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar.accempty[set]);
         }
         tc_fence_before();
         __syncwarp();
@@ -529,7 +601,9 @@ cudaError_t launch_moe_fp4_gemm(const uint16_t *X, const uint8_t *qw, const uint
     if (smem > dev.max_smem_optin) return cudaErrorNotSupported;
     static SmemLimit limit;
     if (cudaError_t e = limit.ensure(reinterpret_cast<const void *>(moe_fp4_gemm_kernel), dev.device, smem)) return e;
-    const dim3 grid(static_cast<unsigned>(l.tmax), static_cast<unsigned>((N + BR - 1) / BR));
+    // one persistent CTA per SM (at most one per possible work item)
+    const int64_t items_max = static_cast<int64_t>(l.tmax) * ((N + BR - 1) / BR);
+    const unsigned grid = static_cast<unsigned>(items_max < dev.num_sms ? items_max : dev.num_sms);
     moe_fp4_gemm_kernel<<<grid, THREADS, smem, st>>>(tmW, tmS, tmX, a);
     return cudaGetLastError();
 }
