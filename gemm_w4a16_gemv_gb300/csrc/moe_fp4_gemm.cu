@@ -54,7 +54,7 @@ constexpr int WS_MAX = 12;            // weight stages (codes + scales), as many
 constexpr int BG = 2;                 // builder groups: chunk c is built by group c mod 2
 constexpr int AP = 4;                 // TMEM operand stages (64 columns each), two per group
 constexpr int MAX_ISS = 4;            // MMA issuer warps (each with its own accumulator)
-constexpr int X_BOX_ROWS = 16;        // rows per X TMA box (a tile loads as many boxes as it needs)
+constexpr int NXMAPS = BT / 16;        // token tensor maps, one per tile height 16, 32, ..., 128
 constexpr int W_STAGE = BR * 128;     // 16 KB of packed codes
 constexpr int S_STAGE = BR * 16;      // 2 KB of scales
 // Shared memory holds the X ring (stages of 256 bytes per token row of the
@@ -199,6 +199,16 @@ struct MoeGemmArgs {
     unsigned int inject;
 };
 
+// One 3-D view of the gathered token rows per tile height h = 16 (i + 1):
+// [K/64][P][64] binary16, box 64 x h x 2, so that one TMA copy brings a
+// chunk's h rows x 128 K (both 64-K halves of the 128-byte swizzle).  Every
+// TMA copy costs the SM a fixed time whatever its size (measured at about
+// 0.14 us each on GB300 with the weight stream running), so the ring moves
+// each chunk with as few copies as its shape allows.
+struct MoeXMaps {
+    CUtensorMap m[NXMAPS];
+};
+
 struct MoeBarriers {
     uint64_t xfull[XS_MAX], xempty[XS_MAX];
     uint64_t wfull[WS_MAX], wempty[WS_MAX];
@@ -235,7 +245,7 @@ __device__ __forceinline__ void e2m1x8_times(uint32_t w, uint32_t s2, uint32_t *
 // multiplies with its own N.
 __global__ void __launch_bounds__(THREADS, 1)
 moe_fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS,
-                    const __grid_constant__ CUtensorMap tmX, const MoeGemmArgs a) {
+                    const __grid_constant__ MoeXMaps xm, const MoeGemmArgs a) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     MoeBarriers &bar = *reinterpret_cast<MoeBarriers *>(smem + POOL);
@@ -260,8 +270,7 @@ moe_fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
     // turns by chunk within an item, so their count divides the chunks
     int n_iss = nmax <= 32 ? MAX_ISS : (nmax <= 64 ? 2 : 1);
     if (nch % n_iss != 0) n_iss = 2;
-    const int x_half = nmax * 128;
-    const int x_stage = 2 * x_half;
+    const int x_stage = 2 * nmax * 128;
     const int xs_n = nmax <= 32 ? 8 : 4;  // a multiple of n_iss
     const int off_w = xs_n * x_stage;
     int ws_n = (POOL - off_w) / (W_STAGE + S_STAGE);
@@ -333,26 +342,24 @@ moe_fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
         // ------------------------------------------ token rows (TMA)
         if (lane == 0) {
             const uint64_t pol = policy_evict_last();
-            tma_prefetch_desc(&tmX);
+            for (int i = 0; i < NXMAPS; ++i) tma_prefetch_desc(&xm.m[i]);
             const int nissue = (a.inject & kInjectStallPipeline) ? 0 : nitems;
             int issued = 0;
             bool ok = true;
             for (int it = 0; ok && it < nissue; ++it) {
                 const int item = static_cast<int>(blockIdx.x) + it * static_cast<int>(gridDim.x);
                 const MoeTile tile = tiles[item / nblk];
-                const int xboxes = (tile.rows + X_BOX_ROWS - 1) / X_BOX_ROWS;
+                const int nt = ((tile.rows + 15) / 16) * 16;  // rows loaded: the item's MMA N
+                const CUtensorMap *map = &xm.m[nt / 16 - 1];
                 for (int c = 0; c < nch; ++c, ++issued) {
                     const int xs = issued % xs_n;
                     if (issued >= xs_n && !mbar_wait(&bar.xempty[xs], ((issued / xs_n) - 1) & 1, a.status)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&bar.xfull[xs], 2 * xboxes * X_BOX_ROWS * 128);
-                    unsigned char *dst = smem + xs * x_stage;
-                    for (int h = 0; h < 2; ++h)          // the chunk's two 64-K boxes
-                        for (int b = 0; b < xboxes; ++b)  // 16 rows each
-                            tma_load_2d_hint(dst + h * x_half + b * X_BOX_ROWS * 128, &tmX, c * CK + h * 64,
-                                             tile.row0 + b * X_BOX_ROWS, &bar.xfull[xs], pol);
+                    // the stage holds [2][nt][128 bytes]: the two 64-K halves of the chunk
+                    mbar_arrive_expect_tx(&bar.xfull[xs], 2 * nt * 128);
+                    tma_load_3d_hint(smem + xs * x_stage, map, 0, tile.row0, 2 * c, &bar.xfull[xs], pol);
                 }
             }
             for (int i = issued > xs_n ? issued - xs_n : 0; i < issued; ++i)
@@ -398,7 +405,7 @@ moe_fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
 #pragma unroll
                 for (int k = 0; k < CK / 16; ++k)
                     umma_f16_tmem_a_w(d_acc, tmem + TM_A + ap * 64 + 8 * k,
-                                      smem_desc_sw128_kmajor(b_addr + (k >> 2) * x_half + 32 * (k & 3)), idesc,
+                                      smem_desc_sw128_kmajor(b_addr + (k >> 2) * (nt * 128) + 32 * (k & 3)), idesc,
                                       (c != j) || (k != 0));
                 umma_commit_w(&bar.xempty[xs]);
                 umma_commit_w(&bar.aempty[ap]);
@@ -553,7 +560,8 @@ cudaError_t launch_moe_fp4_gemm(const uint16_t *X, const uint8_t *qw, const uint
     moe_gather_kernel<<<P, GATHER_THREADS, 0, st>>>(X, topk, P, static_cast<int>(E), static_cast<int>(K), N, Y, scr);
     if (cudaError_t e = cudaGetLastError()) return e;
     // 3. the GEMM
-    CUtensorMap tmW, tmS, tmX;
+    CUtensorMap tmW, tmS;
+    MoeXMaps xm;
     {
         // packed codes as bytes [E*N, K/2]: box 128 bytes (256 codes) x 128 rows, 128-byte swizzle
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(E * N)};
@@ -577,15 +585,19 @@ cudaError_t launch_moe_fp4_gemm(const uint16_t *X, const uint8_t *qw, const uint
             return cudaErrorInvalidValue;
     }
     {
-        // gathered token rows, binary16 [P, K]: box 64 (128 bytes) x 16 rows, 128-byte swizzle
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(P)};
-        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-        const cuuint32_t box[2] = {64, X_BOX_ROWS};
-        const cuuint32_t estr[2] = {1, 1};
-        if (enc(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, scr + l.xg_off, dims, strides, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
+        // gathered token rows, binary16 [P, K] seen as [K/64][P][64] (element
+        // (k0, row, kb) at byte row * 2K + kb * 128 + 2 k0): box 64 x h x 2,
+        // 128-byte swizzle, h = 16, 32, ..., 128
+        const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(P), static_cast<cuuint64_t>(K / 64)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 128};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        for (int i = 0; i < NXMAPS; ++i) {
+            const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(16 * (i + 1)), 2};
+            if (enc(&xm.m[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, scr + l.xg_off, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return cudaErrorInvalidValue;
+        }
     }
     MoeGemmArgs a;
     a.scratch = scr;
@@ -604,7 +616,7 @@ cudaError_t launch_moe_fp4_gemm(const uint16_t *X, const uint8_t *qw, const uint
     // one persistent CTA per SM (at most one per possible work item)
     const int64_t items_max = static_cast<int64_t>(l.tmax) * ((N + BR - 1) / BR);
     const unsigned grid = static_cast<unsigned>(items_max < dev.num_sms ? items_max : dev.num_sms);
-    moe_fp4_gemm_kernel<<<grid, THREADS, smem, st>>>(tmW, tmS, tmX, a);
+    moe_fp4_gemm_kernel<<<grid, THREADS, smem, st>>>(tmW, tmS, xm, a);
     return cudaGetLastError();
 }
 

@@ -176,6 +176,16 @@ __device__ __forceinline__ void tma_load_2d_hint(void *dst, const CUtensorMap *t
         : "memory");
 }
 
+// The same for a 3-D box (coordinates innermost first).
+__device__ __forceinline__ void tma_load_3d_hint(void *dst, const CUtensorMap *tmap, int c0, int c1, int c2,
+                                                 uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
+        "[%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 // TMA store of a 2-D box from this CTA's shared memory (bulk async group):
 // elements of the box outside the tensor are not written.  The coordinates
 // must not be negative; x times the element size a multiple of 16 bytes.
