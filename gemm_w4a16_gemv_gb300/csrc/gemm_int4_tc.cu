@@ -224,10 +224,9 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         for (int g = 0; g < xgroups; ++g, ++issued) {
             if (g >= XP && !mbar_wait<kHintProd>(&bar.xempty[xs], xph ^ 1, a.status)) break;
             if (lane == 0) {
-                mbar_arrive_expect_tx(&bar.xfull[xs], 2 * X_BYTES);  // both boxes
-                unsigned char *dst = smem + OFF_X + xs * 2 * X_BYTES;
-                for (int h = 0; h < 2; ++h)
-                    tma_load_2d_hint(dst + h * X_BYTES, &tmX, g * GK + h * BK, m0, &bar.xfull[xs], pol_x);
+                // the group's two 64-K halves in one copy: [2][128 rows][128 bytes]
+                mbar_arrive_expect_tx(&bar.xfull[xs], 2 * X_BYTES);
+                tma_load_3d_hint(smem + OFF_X + xs * 2 * X_BYTES, &tmX, 0, m0, 2 * g, &bar.xfull[xs], pol_x);
             }
             __syncwarp();
             if (++xs == XP) {
@@ -531,12 +530,16 @@ cudaError_t launch_gemm_int4(const uint16_t *X, const uint8_t *qw, const uint16_
     const unsigned gx = static_cast<unsigned>((N + BNW - 1) / BNW), gy = static_cast<unsigned>((M + BM - 1) / BM);
     CUtensorMap tmX, tmW;
     {
-        // X as BF16 [M, K]; box of 64 (one K block) x 128 rows, 128-byte swizzle
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
-        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-        const cuuint32_t box[2] = {BK, static_cast<cuuint32_t>(BM)};
-        const cuuint32_t estr[2] = {1, 1};
-        if (enc(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(X), dims, strides, box, estr,
+        // X as BF16 [M, K] seen as [K/64][M][64] (element (k0, row, kb) at byte
+        // row * 2K + kb * 128 + 2 k0; K % 128 == 0): box 64 x 128 rows x 2, so
+        // that one copy brings a group's two 64-K halves (128-byte swizzle).
+        // Each TMA copy costs the SM a roughly fixed time, whatever its size.
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(BK), static_cast<cuuint64_t>(M),
+                                    static_cast<cuuint64_t>(K / BK)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, BK * 2};
+        const cuuint32_t box[3] = {BK, static_cast<cuuint32_t>(BM), 2};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        if (enc(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(X), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
