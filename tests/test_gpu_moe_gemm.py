@@ -30,6 +30,8 @@ def _ref(m, ids=None):
     (2, 200, 512, 150, 2),      # 150 rows per expert: tiles of 128 and 22 rows
     (16, 1000, 7168, 40, 6),    # the expert FC's K
     (3, 130, 16384, 5, 3),      # long K
+    (5, 200, 768, 9, 3),        # K % 512 == 256: a half last weight stage in every item
+    (8, 256, 1280, 20, 4),      # the same after two full stages, several items per CTA
 ])
 def test_moe_gemm_small_and_ragged(E, N, K, M, topk):
     torch, w4 = cuda_or_skip()
