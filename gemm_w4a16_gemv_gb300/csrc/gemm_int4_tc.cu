@@ -65,14 +65,13 @@ namespace {
 
 constexpr int BNW = 112;              // weight rows per tile: 28 in each TMEM lane quarter
 constexpr int RQ = 28;                // weight rows per lane quarter (lanes 28-31: ones)
-constexpr int BM = 128;               // X rows per tile (the MMA's N)
+constexpr int BM = 128;               // X rows per tile at most (the MMA's N): M rounded up to 16 below 128
 constexpr int BK = 64;                // one TMA box of X (128 bytes of BF16 per row)
 constexpr int GK = 128;               // K per group = per hand-off
 constexpr int MAX_XP = 5;             // X ring depth in groups (runtime, from shared memory)
 constexpr int WS = 3;                 // packed-code ring (each load: two groups)
 constexpr int AP = 4;                 // TMEM operand stages (64 columns each)
 constexpr int DB = 2;                 // TMEM accumulators (128 columns each)
-constexpr int X_BYTES = BM * BK * 2;  // 16 KB: one box; a group takes two
 constexpr int W_BYTES = BNW * 128;    // 14 KB packed codes, two groups
 constexpr int THREADS = 640;          // 20 warps, five warpgroups
 constexpr int PREP_WARPS = 8;         // warps 8-11 (even groups) and 16-19 (odd groups)
@@ -106,9 +105,10 @@ struct GemmArgs {
     int sz_bytes;  // bytes of one staged scale (or zero) tile, 16-aligned
     int xp;        // X ring depth in groups
     int off_w, off_sz;
-    unsigned int inject;  // test-only injection flags (0 normally); kept last:
-                          // inserting it earlier shifted the hot fields and
-                          // measurably slowed the kernel
+    unsigned int inject;  // test-only injection flags (0 normally); kept after
+                          // the hot fields: inserting it earlier shifted them
+                          // and measurably slowed the kernel
+    int bm;               // X rows per tile: min(128, M rounded up to 16)
 };
 
 struct Barriers {
@@ -143,7 +143,9 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * BNW;
-    const int m0 = blockIdx.y * BM;
+    const int bm = a.bm;
+    const int x_stage = 2 * bm * BK * 2;  // a group's X: [2][bm rows][128 bytes]
+    const int m0 = blockIdx.y * bm;
     const int ngroups = a.G;
     const int rows_n = max(0, min(BNW, a.N - n0));  // weight rows of this tile
 
@@ -224,9 +226,9 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         for (int g = 0; g < xgroups; ++g, ++issued) {
             if (g >= XP && !mbar_wait<kHintProd>(&bar.xempty[xs], xph ^ 1, a.status)) break;
             if (lane == 0) {
-                // the group's two 64-K halves in one copy: [2][128 rows][128 bytes]
-                mbar_arrive_expect_tx(&bar.xfull[xs], 2 * X_BYTES);
-                tma_load_3d_hint(smem + OFF_X + xs * 2 * X_BYTES, &tmX, 0, m0, 2 * g, &bar.xfull[xs], pol_x);
+                // the group's two 64-K halves in one copy: [2][bm rows][128 bytes]
+                mbar_arrive_expect_tx(&bar.xfull[xs], 2 * bm * BK * 2);
+                tma_load_3d_hint(smem + OFF_X + xs * x_stage, &tmX, 0, m0, 2 * g, &bar.xfull[xs], pol_x);
             }
             __syncwarp();
             if (++xs == XP) {
@@ -277,7 +279,7 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         // MMAs done) before this issuer's accumulator wait for group g - 2
         // ended.  With XP = 3 (the largest K) the X stage is awaited only
         // after the accumulator, in a second round.
-        constexpr uint32_t idesc = idesc_kind_f16(128, BM, 1u);  // BF16, M = 128 lanes, N = 128 rows of X
+        const uint32_t idesc = idesc_kind_f16(128, bm, 1u);  // BF16, M = 128 lanes, N = bm rows of X
         const bool x_second = (XP & 1) && XP < DB + 2;
         // test-only injection: the issuers take nothing, so the producers'
         // waits for free stages run out with their copies issued
@@ -306,11 +308,12 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             {
                 const uint32_t t_acc = tmem + db * 128;
                 const uint32_t a_t = tmem + TM_A + ap * 64;
-                const uint32_t b_addr = smem_u32(smem + OFF_X + xs * 2 * X_BYTES);
+                const uint32_t b_addr = smem_u32(smem + OFF_X + xs * x_stage);
 #pragma unroll
                 for (int k = 0; k < GK / 16; ++k)
                     umma_f16_tmem_a_w(t_acc, a_t + 8 * k,
-                                      smem_desc_sw128_kmajor(b_addr + (k >> 2) * X_BYTES + 32 * (k & 3)), idesc, k != 0);
+                                      smem_desc_sw128_kmajor(b_addr + (k >> 2) * (bm * BK * 2) + 32 * (k & 3)), idesc,
+                                      k != 0);
                 umma_commit_w(&bar.xempty[xs]);
                 umma_commit_w(&bar.aempty[ap]);
                 umma_commit_w(&bar.accfull[db]);
@@ -453,6 +456,10 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         const int hc = warp >= 12 ? 1 : 0;     // column half: rows m of X
         const int n = q * RQ + lane;           // output column of this thread (lanes < 28)
         const uint32_t t_lane = static_cast<uint32_t>(q * 32) << 16;
+        // this warp's half of the accumulator holds X rows 64 hc .. 64 hc + 63
+        // of the tile: none when bm <= 64 and hc = 1 (it only hands the
+        // accumulator back)
+        const bool has_rows = hc * 64 < bm;
         float y[64];
 #pragma unroll
         for (int j = 0; j < 64; ++j) y[j] = 0.0f;
@@ -479,6 +486,16 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             const uint32_t t_acc = tmem + t_lane + db * 128 + hc * 64;
             // both halves into registers, then release the accumulator at
             // once: the MMAs of group g + DB need it, the arithmetic does not
+            if (!has_rows) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar.accempty[db]);
+                if (++db == DB) {
+                    db = 0;
+                    dph ^= 1;
+                }
+                continue;
+            }
             uint32_t r[2][32];
             tmem_ld_32x32b_x32(t_acc, r[0]);
             tmem_ld_32x32b_x32(t_acc + 32, r[1]);
@@ -527,17 +544,21 @@ cudaError_t launch_gemm_int4(const uint16_t *X, const uint8_t *qw, const uint16_
     if (K > MAX_K) return cudaErrorNotSupported;
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
-    const unsigned gx = static_cast<unsigned>((N + BNW - 1) / BNW), gy = static_cast<unsigned>((M + BM - 1) / BM);
+    // X rows per tile: M rounded up to 16 below 128, so that the X copies
+    // read no rows past M (a zero-filled row costs the copy as much as a
+    // loaded one) and the MMAs and the epilogue handle only those rows
+    const int bm = M >= BM ? BM : static_cast<int>((M + 15) / 16) * 16;
+    const unsigned gx = static_cast<unsigned>((N + BNW - 1) / BNW), gy = static_cast<unsigned>((M + bm - 1) / bm);
     CUtensorMap tmX, tmW;
     {
         // X as BF16 [M, K] seen as [K/64][M][64] (element (k0, row, kb) at byte
-        // row * 2K + kb * 128 + 2 k0; K % 128 == 0): box 64 x 128 rows x 2, so
+        // row * 2K + kb * 128 + 2 k0; K % 128 == 0): box 64 x bm rows x 2, so
         // that one copy brings a group's two 64-K halves (128-byte swizzle).
         // Each TMA copy costs the SM a roughly fixed time, whatever its size.
         const cuuint64_t dims[3] = {static_cast<cuuint64_t>(BK), static_cast<cuuint64_t>(M),
                                     static_cast<cuuint64_t>(K / BK)};
         const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, BK * 2};
-        const cuuint32_t box[3] = {BK, static_cast<cuuint32_t>(BM), 2};
+        const cuuint32_t box[3] = {BK, static_cast<cuuint32_t>(bm), 2};
         const cuuint32_t estr[3] = {1, 1, 1};
         if (enc(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(X), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -561,20 +582,22 @@ cudaError_t launch_gemm_int4(const uint16_t *X, const uint8_t *qw, const uint16_
     a.Y = Y;
     a.status = status;
     a.inject = dev.inject;
+    a.bm = bm;
     a.M = static_cast<int>(M);
     a.N = static_cast<int>(N);
     a.K = static_cast<int>(K);
     a.G = static_cast<int>(K / 128);
     a.sz_bytes = (BNW * a.G * 2 + 15) & ~15;  // whole 16-byte chunks of the tile's rows
-    // as many X stages (groups) as shared memory allows (3 .. MAX_XP; the MMA
-    // issuers step their ring positions by two groups and order their waits
-    // by the ring depth)
+    // as many X stages (groups of [2][bm rows][128 bytes]) as shared memory
+    // allows (3 .. MAX_XP; the MMA issuers step their ring positions by two
+    // groups and order their waits by the ring depth)
+    const int x_stage = 2 * bm * BK * 2;
     const int tail = WS * W_BYTES + 2 * a.sz_bytes + static_cast<int>(sizeof(Barriers));
-    int xp = (dev.max_smem_optin - 1024 - tail) / (2 * X_BYTES);
+    int xp = (dev.max_smem_optin - 1024 - tail) / x_stage;
     if (xp > MAX_XP) xp = MAX_XP;
     if (xp < 3) return cudaErrorNotSupported;
     a.xp = xp;
-    a.off_w = OFF_X + xp * 2 * X_BYTES;  // 1024-aligned (X_BYTES is)
+    a.off_w = OFF_X + xp * x_stage;      // 1024-aligned (x_stage is a multiple of 4 KB)
     a.off_sz = a.off_w + WS * W_BYTES;   // W_BYTES = 14 KB keeps 1024 alignment
     const int smem = 1024 + a.off_sz + 2 * a.sz_bytes + static_cast<int>(sizeof(Barriers));
     // one instance per zero-point mode, each configured once per device
