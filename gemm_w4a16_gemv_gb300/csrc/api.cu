@@ -141,15 +141,16 @@ int check_gemm_args(const char *who, const void *X, const void *qw, const void *
 }
 
 // Decode-sized batches stream the weights on the CUDA cores: M = 1 the GEMV,
-// up to four rows sharing one pass (fewer where K leaves fewer teams per
-// CTA), M <= 8 in passes of that many rows.  Larger M goes to the tensor
-// cores, whose GEMM has a fixed pipeline latency that dominates at small M
-// (measured at N = 15360, K = 3840, GEMM against two passes: M = 5 28.7 /
-// 22.3 us, M = 6 31.5 / 24.6 us, M = 8 30.8 / 29.6 us, M = 12 30.7 / 44.3 us).
+// up to four rows sharing one pass (two passes where K leaves fewer teams
+// per CTA).  Larger M goes to the tensor cores, whose GEMM (X tiles of M
+// rounded up to 16 rows) has a fixed pipeline latency that dominates at
+// small M (N = 15360, K = 3840, GEMM against streaming passes of up to four
+// rows: M = 4 -- / 19.1 us, M = 5 25.0 / 26.2 us, M = 6 25.1 / 30.0 us,
+// M = 8 25.0 / 36.9 us).
 cudaError_t launch_int4_linear(const uint16_t *X, const uint8_t *qw, const uint16_t *s, const uint16_t *z,
                                uint16_t *Y, int64_t M, int64_t N, int64_t K, cudaStream_t st, unsigned int *status,
                                const w4::DeviceInfo &dev) {
-    if (M > 8) return w4::launch_gemm_int4(X, qw, s, z, Y, M, N, K, st, status, dev);
+    if (M > 4) return w4::launch_gemm_int4(X, qw, s, z, Y, M, N, K, st, status, dev);
     const int64_t mv_max = w4::gemv_int4_max_mv(K) >= 4 ? 4 : 2;
     while (M > 0) {
         const int64_t mv = M >= mv_max ? mv_max : M >= 2 ? 2 : 1;

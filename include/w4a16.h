@@ -96,7 +96,7 @@ int w4a16_gemv(const uint16_t *x, const uint8_t *qw, const uint16_t *s,
  * M >= 1 and any N are accepted (rows past M and N in the last tiles are
  * masked).  Decode-sized
  * batches run as the streaming GEMV instead: M <= 4 rows share one pass over
- * the weights, 5 <= M <= 8 take two passes (four rows, then the rest);
+ * the weights (two passes of two rows where K leaves fewer teams per CTA);
  * larger M runs on the tensor cores.
  */
 int w4a16_gemm(const uint16_t *X, const uint8_t *qw, const uint16_t *s,
