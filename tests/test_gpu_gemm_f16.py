@@ -41,6 +41,27 @@ def test_gemm_f16_symmetric(M, N, K):
     assert_close(_run(w4, torch, p, sym=True), ref, "gemm_f16 symmetric")
 
 
+# More tiles than SMs (several waves of CTAs), ragged in M and N, with one to
+# several packed-code stages a tile and one to four issuers.  Every output
+# column is checked on a sample of token rows (the oracle's cost grows with
+# M x N x K).
+@pytest.mark.parametrize("M,N,K,sym", [
+    (600, 20100, 512, False),   # 3 token tiles (the last of 88 rows) x 158 weight tiles (the last of 4 rows)
+    (600, 20100, 512, True),    # the same, symmetric
+    (1000, 5000, 768, False),   # 4 x 40 tiles, three packed-code stages a tile
+    (100, 20600, 1024, False),  # 112-row token tiles: two issuers, 161 tiles
+    (40, 20000, 256, False),    # 48-row token tiles: four issuers, one packed-code stage a tile
+    (600, 20100, 384, False),   # K % 256 == 128: a half packed-code stage ends every tile
+])
+def test_gemm_f16_many_tiles(M, N, K, sym):
+    torch, w4 = cuda_or_skip()
+    p = synth.int4_problem(N, K, M=M, seed=M + N + K + sym)
+    y = _run(w4, torch, p, sym=sym)
+    rows = np.unique(np.array([0, 1, M // 2, M - 2, M - 1] + [r for r in (255, 256, 511, 512) if r < M]))
+    ref = oracle.gemm_int4(p["x"].reshape(M, K)[rows], p["qw"], p["s"], None if sym else p["z"], K=K)
+    assert_close(y[rows], ref, "gemm_f16 %dx%dx%d%s sampled" % (M, N, K, " symmetric" if sym else ""))
+
+
 def test_gemm_f16_full_size_sampled():
     # the prefill shape: every output on the GPU, a sample of tokens on the oracle
     torch, w4 = cuda_or_skip()
@@ -99,6 +120,31 @@ def test_gemm_f16_bounded_wait_reports_timeout_and_recovers():
         assert status == 5  # W4A16_ERR_TIMEOUT
         assert 1.5 < waited < 30.0, waited
         assert_close(_run(w4, torch, p), ref, "gemm_f16 after recovery")
+        assert w4.w4a16_check_device_error() == 0
+
+
+def test_gemm_f16_many_tiles_bounded_wait_reports_timeout_and_recovers():
+    """The same with more tiles than SMs: every CTA's waits run out, the
+    status reports the timeout, each CTA leaves, and the next call is
+    correct."""
+    torch, w4 = cuda_or_skip()
+    M, N, K = 300, 20100, 1024  # 2 x 158 tiles
+    p = synth.int4_problem(N, K, M=M, seed=10)
+    rows = np.array([0, 1, 150, 255, 256, 299])
+    ref = oracle.gemm_int4(p["x"].reshape(M, K)[rows], p["qw"], p["s"], p["z"], K=K)
+    for flag in (w4.INJECT_STALL_PIPELINE, w4.INJECT_STALL_CONSUMERS):
+        assert w4.w4a16_check_device_error() == 0
+        w4.w4a16_debug_inject(flag)
+        try:
+            t0 = time.monotonic()
+            _run(w4, torch, p)
+            status = w4.w4a16_check_device_error()
+            waited = time.monotonic() - t0
+        finally:
+            w4.w4a16_debug_inject(0)
+        assert status == 5  # W4A16_ERR_TIMEOUT
+        assert 1.5 < waited < 30.0, waited
+        assert_close(_run(w4, torch, p)[rows], ref, "gemm_f16 many tiles after recovery")
         assert w4.w4a16_check_device_error() == 0
 
 
