@@ -847,6 +847,7 @@ def profile_cases(torch, w4, dev):
 
     return {"gemv_3840x3840": gemv(3840, 3840), "gemv_up_15360x3840": gemv(*UP),
             "gemv_down_3840x15360": gemv(*DOWN), "gemv_vocab_262144x3840": gemv(262144, 3840),
+            "gemm_m16_15360x3840": gemm(16, 15360, 3840),
             "gemm_m128_15360x3840": gemm(128, 15360, 3840), "gemm_m2048_15360x3840": gemm(2048, 15360, 3840),
             "gemm_f16_m128_15360x3840": gemm(128, 15360, 3840, True),
             "gemm_f16_m2048_15360x3840": gemm(2048, 15360, 3840, True),
