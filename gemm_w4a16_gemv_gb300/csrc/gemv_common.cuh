@@ -48,14 +48,15 @@ __device__ __forceinline__ void mfma_f16x2(uint32_t v, uint32_t x, float &d_lo, 
         : "r"(v), "r"(x));
 }
 
-// Two E2M1 codes (the low byte of `b`; low nibble = even k) -> their values
-// as an f16x2 pair, low half from the low nibble (exact in binary16).
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t b) {
-    uint32_t h2;
-    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
-        : "=r"(h2)
-        : "r"(b));
-    return h2;
+// The eight E2M1 codes of a word -> four f16x2 pairs, h[i] from byte i (low
+// half from its low nibble), exact.  One vector move splits the word into
+// its bytes, so no shift or mask precedes a conversion.
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&h)[4]) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w));
 }
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {

@@ -615,11 +615,10 @@ __device__ __forceinline__ void gemv_consume_fp4(const GemvParams &a, GemvHeader
                 float lo = 0.0f, hi = 0.0f;
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
-                    const uint32_t w = words[m];
-                    mfma_f16x2(e2m1x2_to_f16x2(w), xr[i][4 * m + 0], lo, hi);
-                    mfma_f16x2(e2m1x2_to_f16x2(w >> 8), xr[i][4 * m + 1], lo, hi);
-                    mfma_f16x2(e2m1x2_to_f16x2(w >> 16), xr[i][4 * m + 2], lo, hi);
-                    mfma_f16x2(e2m1x2_to_f16x2(w >> 24), xr[i][4 * m + 3], lo, hi);
+                    uint32_t h[4];
+                    e2m1x8_to_f16x2(words[m], h);
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) mfma_f16x2(h[b], xr[i][4 * m + b], lo, hi);
                 }
                 const float sf = f16_bits_to_f32(ss[(rbase + rr) * a.G + u]) * pw[i];
                 part[rr] = fmaf(sf, lo + hi, part[rr]);
