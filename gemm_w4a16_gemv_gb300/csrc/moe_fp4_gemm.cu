@@ -115,6 +115,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS) moe_route_kernel(const int32_t 
     int *perm = reinterpret_cast<int *>(scratch + l.perm_off);
     int *posof = reinterpret_cast<int *>(scratch + l.posof_off);
     pdl_wait();
+    pdl_launch_dependents();  // the gather's CTAs may start; they wait for this grid before reading
     for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = cur[e] = 0;
     __syncthreads();
     bool bad = false;
@@ -165,6 +166,8 @@ __global__ void __launch_bounds__(GATHER_THREADS) moe_gather_kernel(const uint16
                                                                     unsigned char *scratch) {
     const MoeScratch l = moe_scratch_layout(P, E, K);
     const int p = blockIdx.x;
+    pdl_launch_dependents();  // the GEMM's CTAs may start; they wait for this grid before reading
+    pdl_wait();               // the routing (and X) follow the stream order
     const int pos = reinterpret_cast<const int *>(scratch + l.posof_off)[p];
     if (pos < 0) {
         // an expert id out of range: its output row is zeros
@@ -557,8 +560,23 @@ cudaError_t launch_moe_fp4_gemm(const uint16_t *X, const uint8_t *qw, const uint
         if (cudaError_t e = cudaGetLastError()) return e;
     }
     // 2. gathering
-    moe_gather_kernel<<<P, GATHER_THREADS, 0, st>>>(X, topk, P, static_cast<int>(E), static_cast<int>(K), N, Y, scr);
-    if (cudaError_t e = cudaGetLastError()) return e;
+    // the gather and the GEMM are launched with programmatic stream
+    // serialisation: each may start while the previous launch finishes and
+    // waits for it (griddepcontrol.wait) before reading what it wrote
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(P));
+        cfg.blockDim = dim3(GATHER_THREADS);
+        cfg.stream = st;
+        cfg.attrs = pdl;
+        cfg.numAttrs = 1;
+        if (cudaError_t e = cudaLaunchKernelEx(&cfg, moe_gather_kernel, X, topk, P, static_cast<int>(E),
+                                               static_cast<int>(K), N, Y, scr))
+            return e;
+    }
     // 3. the GEMM
     CUtensorMap tmW, tmS;
     MoeXMaps xm;
@@ -616,8 +634,14 @@ cudaError_t launch_moe_fp4_gemm(const uint16_t *X, const uint8_t *qw, const uint
     // one persistent CTA per SM (at most one per possible work item)
     const int64_t items_max = static_cast<int64_t>(l.tmax) * ((N + BR - 1) / BR);
     const unsigned grid = static_cast<unsigned>(items_max < dev.num_sms ? items_max : dev.num_sms);
-    moe_fp4_gemm_kernel<<<grid, THREADS, smem, st>>>(tmW, tmS, xm, a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = st;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, moe_fp4_gemm_kernel, tmW, tmS, xm, a);
 }
 
 }  // namespace w4
