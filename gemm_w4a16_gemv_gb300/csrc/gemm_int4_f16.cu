@@ -101,6 +101,8 @@ struct Barriers {
 __global__ void __launch_bounds__(PRE_THREADS) x16_prepass_kernel(const uint16_t *__restrict__ X, int K,
                                                                   uint16_t *__restrict__ Xh, float *rowscale) {
     const int m = blockIdx.x;
+    pdl_launch_dependents();  // the GEMM's CTAs may start; they wait for this grid before reading
+    pdl_wait();               // X (and the scratch's previous user) follow the stream order
     const uint4 *x = reinterpret_cast<const uint4 *>(X + static_cast<int64_t>(m) * K);
     uint4 *xh = reinterpret_cast<uint4 *>(Xh + static_cast<int64_t>(m) * K);
     const int nb = K / 8;
@@ -201,6 +203,11 @@ gemm_int4_f16_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bar.tmem_holder;
+    // programmatic dependent launch: this grid may start while the previous
+    // launch of the stream finishes (its setup overlaps that launch's tail);
+    // every global read and write follows the wait
+    pdl_launch_dependents();
+    pdl_wait();
 
     // the tile's scale and zero rows are contiguous in memory: one bulk copy
     // each (the last tile along N, when partial, is loaded by the builders)
@@ -497,8 +504,22 @@ cudaError_t launch_gemm_int4_f16(const uint16_t *X, const uint8_t *qw, const uin
     if (cudaError_t e = cudaMallocFromPoolAsync(&scr, bytes, pool, st)) return e;
     uint16_t *xh = static_cast<uint16_t *>(scr);
     float *rowscale = reinterpret_cast<float *>(static_cast<unsigned char *>(scr) + ((xh_bytes + 255) & ~size_t(255)));
-    x16_prepass_kernel<<<static_cast<unsigned>(M), PRE_THREADS, 0, st>>>(X, static_cast<int>(K), xh, rowscale);
-    cudaError_t err = cudaGetLastError();
+    // the pre-pass and the GEMM are launched with programmatic stream
+    // serialisation: each may start while the previous launch finishes and
+    // waits for it (griddepcontrol.wait) before touching global memory
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaError_t err;
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(M));
+        cfg.blockDim = dim3(PRE_THREADS);
+        cfg.stream = st;
+        cfg.attrs = pdl;
+        cfg.numAttrs = 1;
+        err = cudaLaunchKernelEx(&cfg, x16_prepass_kernel, X, static_cast<int>(K), xh, rowscale);
+    }
 
     // 2. the GEMM
     CUtensorMap tmW, tmX, tmY;
@@ -561,12 +582,15 @@ cudaError_t launch_gemm_int4_f16(const uint16_t *X, const uint8_t *qw, const uin
         static SmemLimit limit[2];  // one per kernel instance
         err = limit[sym ? 1 : 0].ensure(kern, dev.device, smem);
         if (err == cudaSuccess) {
-            const unsigned grid = static_cast<unsigned>(ntn * ntm);
-            if (sym)
-                gemm_int4_f16_kernel<true><<<grid, THREADS, smem, st>>>(tmW, tmX, tmY, a);
-            else
-                gemm_int4_f16_kernel<false><<<grid, THREADS, smem, st>>>(tmW, tmX, tmY, a);
-            err = cudaGetLastError();
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(static_cast<unsigned>(ntn * ntm));
+            cfg.blockDim = dim3(THREADS);
+            cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+            cfg.stream = st;
+            cfg.attrs = pdl;
+            cfg.numAttrs = 1;
+            err = sym ? cudaLaunchKernelEx(&cfg, gemm_int4_f16_kernel<true>, tmW, tmX, tmY, a)
+                      : cudaLaunchKernelEx(&cfg, gemm_int4_f16_kernel<false>, tmW, tmX, tmY, a);
         }
     }
     // the scratch returns to the pool once the work queued on the stream is done

@@ -179,6 +179,11 @@ gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bar.tmem_holder;
+    // programmatic dependent launch: this grid may start while the previous
+    // launch of the stream finishes (its setup overlaps that launch's tail);
+    // every global read and write follows the wait
+    pdl_launch_dependents();
+    pdl_wait();
 
     // Registers per warpgroup, set at the top of each role: the producers and
     // MMA issuers (warps 0-3) need few; each epilogue thread (warps 4-7,
@@ -623,6 +628,11 @@ cudaError_t launch_gemm_int4(const uint16_t *X, const uint8_t *qw, const uint16_
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = st;
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, tmX, tmW, a);
 }
 
