@@ -26,6 +26,10 @@ dequant_kernel(const uint8_t *__restrict__ qw, const uint16_t *__restrict__ s,
     const int64_t chunks_per_row = K / 32;
     const int64_t total = rows * chunks_per_row;
     const int64_t G = K / group;
+    // programmatic dependent launch: the next launch may start; this one's
+    // reads and writes follow the previous launch of the stream
+    pdl_launch_dependents();
+    pdl_wait();
     for (int64_t c = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; c < total;
          c += (int64_t)gridDim.x * blockDim.x) {
         const int64_t r = c / chunks_per_row;
@@ -77,16 +81,19 @@ cudaError_t launch_dequant(int fmt, const uint8_t *qw, const uint16_t *s,
     int64_t blocks = (total + threads - 1) / threads;
     const int64_t cap = static_cast<int64_t>(dev.num_sms) * 8;
     if (blocks > cap) blocks = cap;
-    const dim3 grid(static_cast<unsigned>(blocks));
-    if (fmt == 0 && out_dtype == 0)
-        dequant_kernel<0, 0><<<grid, threads, 0, st>>>(qw, s, z, out, rows, K, group);
-    else if (fmt == 0)
-        dequant_kernel<0, 1><<<grid, threads, 0, st>>>(qw, s, z, out, rows, K, group);
-    else if (out_dtype == 0)
-        dequant_kernel<1, 0><<<grid, threads, 0, st>>>(qw, s, z, out, rows, K, group);
-    else
-        dequant_kernel<1, 1><<<grid, threads, 0, st>>>(qw, s, z, out, rows, K, group);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(threads);
+    cfg.stream = st;
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    if (fmt == 0 && out_dtype == 0) return cudaLaunchKernelEx(&cfg, dequant_kernel<0, 0>, qw, s, z, out, rows, K, group);
+    if (fmt == 0) return cudaLaunchKernelEx(&cfg, dequant_kernel<0, 1>, qw, s, z, out, rows, K, group);
+    if (out_dtype == 0) return cudaLaunchKernelEx(&cfg, dequant_kernel<1, 0>, qw, s, z, out, rows, K, group);
+    return cudaLaunchKernelEx(&cfg, dequant_kernel<1, 1>, qw, s, z, out, rows, K, group);
 }
 
 }  // namespace w4

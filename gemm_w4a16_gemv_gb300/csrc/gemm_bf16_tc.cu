@@ -75,6 +75,10 @@ bf16_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bar.tmem_holder;
+    // programmatic dependent launch: this grid may start while the previous
+    // launch of the stream finishes; every global read and write follows
+    pdl_launch_dependents();
+    pdl_wait();
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -170,8 +174,17 @@ cudaError_t launch_bf16_gemm(const uint16_t *X, const uint16_t *W, uint16_t *Y, 
     static SmemLimit limit;
     if (cudaError_t e = limit.ensure(reinterpret_cast<const void *>(bf16_gemm_tc_kernel), dev.device, smem)) return e;
     const dim3 grid(static_cast<unsigned>((N + TN - 1) / TN), static_cast<unsigned>((M + TM - 1) / TM), 1);
-    bf16_gemm_tc_kernel<<<grid, THREADS, smem, st>>>(tmW, tmX, a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = st;
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, bf16_gemm_tc_kernel, tmW, tmX, a);
 }
 
 }  // namespace w4
