@@ -172,3 +172,31 @@ def test_gemm_f16_in_a_captured_graph():
         ref = oracle.gemm_int4(q["x"], p["qw"], p["s"], p["z"], K=K)
         assert_close(host_bits16(Y).reshape(M, N), ref, "gemm_f16 graph replay")
     assert w4.w4a16_check_device_error() == 0
+
+
+@pytest.mark.parametrize("entry,M", [("w4a16_gemm_f16", 300), ("w4a16_gemm_f16", 16),
+                                     ("w4a16_gemm", 300), ("w4a16_gemm", 16)])
+def test_back_to_back_call_reads_the_previous_output(entry, M):
+    """Two calls on one stream with no synchronisation between them, the
+    second reading the first's output (consecutive launches may overlap by
+    programmatic dependent launch and must still wait for what they read):
+    each result matches the oracle on its actual input."""
+    torch, w4 = cuda_or_skip()
+    fn = getattr(w4, entry)
+    K1, N1, N2 = 256, 384, 256
+    p1 = synth.int4_problem(N1, K1, M=M, seed=31 + M)
+    p2 = synth.int4_problem(N2, N1, M=M, seed=32 + M)
+    X = dev_tensor(p1["x"], torch.bfloat16).view(M, K1)
+    w1 = (dev_tensor(p1["qw"], torch.uint8), dev_tensor(p1["s"], torch.float16), dev_tensor(p1["z"], torch.float16))
+    w2 = (dev_tensor(p2["qw"], torch.uint8), dev_tensor(p2["s"], torch.float16), dev_tensor(p2["z"], torch.float16))
+    Y1 = torch.empty(M, N1, dtype=torch.bfloat16, device="cuda")
+    Y2 = torch.empty(M, N2, dtype=torch.bfloat16, device="cuda")
+    for _ in range(3):  # each round's first call overwrites what the previous second call read
+        fn(X, *w1, Y1)
+        fn(Y1, *w2, Y2)
+    torch.cuda.synchronize()
+    y1 = host_bits16(Y1).reshape(M, N1)
+    y2 = host_bits16(Y2).reshape(M, N2)
+    assert_close(y1, oracle.gemm_int4(p1["x"], p1["qw"], p1["s"], p1["z"], K=K1), "%s first call" % entry)
+    assert_close(y2, oracle.gemm_int4(y1.reshape(-1), p2["qw"], p2["s"], p2["z"], K=N1), "%s second call" % entry)
+    assert w4.w4a16_check_device_error() == 0
