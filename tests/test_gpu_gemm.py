@@ -27,11 +27,15 @@ def test_gemm_small_and_ragged(M, N, K):
     assert_close(_run(w4, torch, p), ref, "gemm %dx%dx%d" % (M, N, K))
 
 
-# small batches on the tensor cores (M = 9..63) and N of any size: odd N with
-# an odd group count, so the tile's scale and zero rows end inside a 16-byte
-# chunk that must be zero-filled past the tensors' end
-@pytest.mark.parametrize("M,N,K", [(9, 113, 384), (16, 225, 640), (31, 1001, 1920), (33, 7, 256),
-                                   (63, 337, 3840), (130, 241, 384), (64, 15360, 3840)])
+# small batches on the tensor cores (M = 5..127: X tiles of M rounded up to
+# 16 rows, one to eight 16-row blocks, the half of the accumulator past 64
+# rows used or not) and N of any size: odd N with an odd group count, so the
+# tile's scale and zero rows end inside a 16-byte chunk that must be
+# zero-filled past the tensors' end
+@pytest.mark.parametrize("M,N,K", [(5, 200, 256), (9, 113, 384), (16, 225, 640), (17, 150, 512),
+                                   (31, 1001, 1920), (33, 7, 256), (48, 129, 768), (63, 337, 3840),
+                                   (65, 96, 384), (80, 300, 640), (100, 113, 1024), (127, 64, 256),
+                                   (130, 241, 384), (64, 15360, 3840)])
 def test_gemm_small_m_and_any_n(M, N, K):
     torch, w4 = cuda_or_skip()
     p = synth.int4_problem(N, K, M=M, seed=M * 13 + N + K)
