@@ -83,6 +83,10 @@ struct GemmF16Args {
     int off_w, off_sz, off_bar;  // shared-memory offsets (X ring at 0)
     int y_tma;                // Y written by one TMA store per tile (N % 8 == 0)
     unsigned int inject;
+    int tiles_full;           // CTAs 0 .. tiles_full - 1: whole tiles (numbered N fastest)
+    int nsplit, cps;          // CTA tiles_full + nsplit x + y: chunks [y cps, y cps + cps) of K of
+                              // tile tiles_full + x (cps a multiple of 4)
+    float *part;              // their binary32 partial sums [x][y][m][r]
 };
 
 struct Barriers {
@@ -168,10 +172,18 @@ gemm_int4_f16_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_const
     Barriers &bar = *reinterpret_cast<Barriers *>(smem + a.off_bar);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    const int tn = blockIdx.x % a.ntn, tm = blockIdx.x / a.ntn;  // N fastest: neighbours share X
+    // this CTA's tile and chunks of K, [c0, c0 + nch) with c0 a multiple of 4
+    // (whole packed-code stages); ring slots and phases count from c0
+    const int b = static_cast<int>(blockIdx.x);
+    const bool partial = b >= a.tiles_full;  // uniform over the CTA
+    const int part_id = b - a.tiles_full;    // index of the partial sums (partial CTAs)
+    const int tile = partial ? a.tiles_full + part_id / a.nsplit : b;
+    const int c0 = partial ? (part_id % a.nsplit) * a.cps : 0;
+    const int nch = partial ? min(a.cps, a.K / CK - c0) : a.K / CK;
+    const int tn = tile % a.ntn, tm = tile / a.ntn;  // N fastest: neighbours share X
     const int n0 = tn * BR, m0 = tm * a.nt;
     const int nt = a.nt;
-    const int nch = a.K / CK;
+    const bool y_tma = a.y_tma && !partial;
     int n_iss = nt <= 64 ? MAX_ISS : (nt <= 128 ? 2 : 1);
     n_iss = n_iss < nch ? n_iss : nch;
     const int xs_n = a.xs_n;  // a multiple of 4 or of n_iss: each issuer waits on its own stages only
@@ -231,7 +243,7 @@ gemm_int4_f16_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_const
                 if (sc >= WS && !mbar_wait(&bar.wempty[ws], ((sc / WS) - 1) & 1, a.status)) break;
                 mbar_arrive_expect_tx(&bar.wfull[ws], W_STAGE);
                 // rows past N and codes past K/2 read as zeros
-                tma_load_2d(smem + a.off_w + ws * W_STAGE, &tmW, sc * 128, n0, &bar.wfull[ws]);
+                tma_load_2d(smem + a.off_w + ws * W_STAGE, &tmW, (c0 / 4 + sc) * 128, n0, &bar.wfull[ws]);
             }
             for (int it = issued > WS ? issued - WS : 0; it < issued; ++it)
                 mbar_wait(&bar.wfull[it % WS], (it / WS) & 1, nullptr);  // no copy in flight at exit
@@ -248,7 +260,7 @@ gemm_int4_f16_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_const
                 if (c >= xs_n && !mbar_wait(&bar.xempty[xs], ((c / xs_n) - 1) & 1, a.status)) break;
                 mbar_arrive_expect_tx(&bar.xfull[xs], x_stage);
                 // rows past M read as zeros
-                tma_load_2d_hint(smem + xs * x_stage, &tmX, c * CK, m0, &bar.xfull[xs], pol);
+                tma_load_2d_hint(smem + xs * x_stage, &tmX, (c0 + c) * CK, m0, &bar.xfull[xs], pol);
             }
             for (int it = issued > xs_n ? issued - xs_n : 0; it < issued; ++it)
                 mbar_wait(&bar.xfull[it % xs_n], (it / xs_n) & 1, nullptr);
@@ -335,7 +347,7 @@ gemm_int4_f16_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_const
                 break;
             }
             // the group's scale and zero point, as binary16 pairs
-            const int g = c >> 1;  // two chunks per group
+            const int g = (c0 + c) >> 1;  // two chunks per group
             const uint32_t sh = s_t[r * a.G + g];
             const uint32_t zh = SYM ? 0x4800u : static_cast<uint32_t>(z_t[r * a.G + g]);  // 8.0 when symmetric
             const uint32_t s2 = sh | (sh << 16);
@@ -391,7 +403,13 @@ gemm_int4_f16_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_const
 #pragma unroll
                     for (int i = 0; i < 16; ++i) acc[i] += __uint_as_float(v[i]);
                 }
-                if (a.y_tma) {
+                if (partial) {
+                    // a K-split tile: binary32 sums [m][r], finished (summed,
+                    // scaled, rounded) by the reduction launch
+                    float *dst = a.part + static_cast<int64_t>(part_id) * nt * BR + r;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) dst[static_cast<int64_t>(16 * p + i) * BR] = acc[i];
+                } else if (y_tma) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         ytile[(16 * p + i) * BR + r] = f32_to_bf16_bits(acc[i] * rs_t[16 * p + i]);
@@ -405,7 +423,7 @@ gemm_int4_f16_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_const
                 }
             }
         }
-        if (a.y_tma) {
+        if (y_tma) {
             // every builder's part written (generic proxy), then one store
             fence_proxy_async_smem();
             named_bar_sync(3, NBW * 32);
@@ -419,6 +437,23 @@ gemm_int4_f16_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_const
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar.done);
     }
+}
+
+// The K-split tiles' outputs: Y[m0 + m, n0 + r] = RNE_bf16(rowscale[m0 + m]
+// x sum over the splits of part[x][y][m][r]), splits summed in order.  One
+// CTA per (tile x, token row m), one thread per weight row r.
+__global__ void __launch_bounds__(BR) f16_split_reduce_kernel(const float *__restrict__ part,
+                                                              const float *__restrict__ rowscale, uint16_t *Y, int M,
+                                                              int N, int nt, int ntn, int tile0, int nsplit) {
+    pdl_launch_dependents();
+    pdl_wait();  // the partial sums and the row scales follow the stream order
+    const int x = blockIdx.x, m = blockIdx.y, r = threadIdx.x;
+    const int tile = tile0 + x;
+    const int n0 = (tile % ntn) * BR, m0 = (tile / ntn) * nt;
+    if (m0 + m >= M || n0 + r >= N) return;
+    float acc = 0.0f;
+    for (int y = 0; y < nsplit; ++y) acc += part[((static_cast<int64_t>(x) * nsplit + y) * nt + m) * BR + r];
+    Y[static_cast<int64_t>(m0 + m) * N + n0 + r] = f32_to_bf16_bits(acc * rowscale[m0 + m]);
 }
 
 // A memory pool per device for the pre-pass output (stream-ordered, kept
@@ -495,15 +530,44 @@ cudaError_t launch_gemm_int4_f16(const uint16_t *X, const uint8_t *qw, const uin
     const int64_t ntn = (N + BR - 1) / BR, ntm = (M + nt - 1) / nt;
     if (ntn * ntm > 0x7FFFFFFFll || M > 0x7FFFFFFFll) return cudaErrorInvalidValue;
 
-    // 1. pre-pass into stream-ordered scratch: X16 [M, K] binary16, then the row scales
+    // Tiles past the last full wave of CTAs (one CTA per SM): when they fill
+    // at most half a wave, each is split along K into nsplit parts of whole
+    // packed-code stages (at least two of them).  The parts are the launch's
+    // last CTAs, so they take the SMs as the last whole tiles finish, and a
+    // reduction launch finishes them from their binary32 partial sums.  With
+    // 960 tiles on 152 SMs (M = 2048, N = 15360) the last 48 tiles would
+    // otherwise make a seventh wave of whole tiles on a third of the SMs.
+    const int64_t tiles = ntn * ntm;
+    const int nch_all = static_cast<int>(K / CK);
+    int64_t tiles_full = tiles, tiles_split = 0;
+    int cps = nch_all, nsplit = 1;
+    if (K % 256 == 0 && tiles > dev.num_sms) {
+        const int64_t rest = tiles % dev.num_sms;
+        if (rest > 0 && 2 * rest <= dev.num_sms) {
+            int parts = static_cast<int>(dev.num_sms / rest);
+            if (parts > nch_all / 8) parts = nch_all / 8;
+            if (parts >= 2) {
+                cps = ((nch_all + parts - 1) / parts + 3) / 4 * 4;
+                nsplit = (nch_all + cps - 1) / cps;
+                tiles_split = rest;
+                tiles_full = tiles - rest;
+            }
+        }
+    }
+
+    // 1. pre-pass into stream-ordered scratch: X16 [M, K] binary16, the row
+    // scales, and the K-split tiles' partial sums
     cudaMemPool_t pool;
     if (cudaError_t e = prepass_pool(dev.device, pool)) return e;
-    const size_t xh_bytes = static_cast<size_t>(M) * static_cast<size_t>(K) * 2;
-    const size_t bytes = ((xh_bytes + 255) & ~size_t(255)) + static_cast<size_t>(M) * 4;
+    const size_t xh_bytes = (static_cast<size_t>(M) * static_cast<size_t>(K) * 2 + 255) & ~size_t(255);
+    const size_t rs_bytes = (static_cast<size_t>(M) * 4 + 255) & ~size_t(255);
+    const size_t part_bytes = static_cast<size_t>(tiles_split) * nsplit * nt * BR * 4;
     void *scr = nullptr;
-    if (cudaError_t e = cudaMallocFromPoolAsync(&scr, bytes, pool, st)) return e;
+    if (cudaError_t e = cudaMallocFromPoolAsync(&scr, xh_bytes + rs_bytes + part_bytes, pool, st)) return e;
     uint16_t *xh = static_cast<uint16_t *>(scr);
-    float *rowscale = reinterpret_cast<float *>(static_cast<unsigned char *>(scr) + ((xh_bytes + 255) & ~size_t(255)));
+    float *rowscale = reinterpret_cast<float *>(static_cast<unsigned char *>(scr) + xh_bytes);
+    float *part = tiles_split ? reinterpret_cast<float *>(static_cast<unsigned char *>(scr) + xh_bytes + rs_bytes)
+                              : nullptr;
     // the pre-pass and the GEMM are launched with programmatic stream
     // serialisation: each may start while the previous launch finishes and
     // waits for it (griddepcontrol.wait) before touching global memory
@@ -577,13 +641,19 @@ cudaError_t launch_gemm_int4_f16(const uint16_t *X, const uint8_t *qw, const uin
         a.off_bar = lay.off_bar;
         a.y_tma = y_tma;
         a.inject = dev.inject;
+        a.tiles_full = static_cast<int>(tiles_full);
+        a.nsplit = nsplit;
+        a.cps = cps;
+        a.part = part;
         const void *kern = sym ? reinterpret_cast<const void *>(gemm_int4_f16_kernel<true>)
                                : reinterpret_cast<const void *>(gemm_int4_f16_kernel<false>);
         static SmemLimit limit[2];  // one per kernel instance
         err = limit[sym ? 1 : 0].ensure(kern, dev.device, smem);
         if (err == cudaSuccess) {
+            // whole tiles first, the K-split parts last: they fill the SMs as
+            // the last whole tiles finish
             cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(static_cast<unsigned>(ntn * ntm));
+            cfg.gridDim = dim3(static_cast<unsigned>(tiles_full + tiles_split * nsplit));
             cfg.blockDim = dim3(THREADS);
             cfg.dynamicSmemBytes = static_cast<size_t>(smem);
             cfg.stream = st;
@@ -591,6 +661,18 @@ cudaError_t launch_gemm_int4_f16(const uint16_t *X, const uint8_t *qw, const uin
             cfg.numAttrs = 1;
             err = sym ? cudaLaunchKernelEx(&cfg, gemm_int4_f16_kernel<true>, tmW, tmX, tmY, a)
                       : cudaLaunchKernelEx(&cfg, gemm_int4_f16_kernel<false>, tmW, tmX, tmY, a);
+        }
+        if (err == cudaSuccess && tiles_split) {
+            // the K-split tiles' outputs from their partial sums
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(static_cast<unsigned>(tiles_split), static_cast<unsigned>(nt));
+            cfg.blockDim = dim3(BR);
+            cfg.stream = st;
+            cfg.attrs = pdl;
+            cfg.numAttrs = 1;
+            err = cudaLaunchKernelEx(&cfg, f16_split_reduce_kernel, static_cast<const float *>(part),
+                                     static_cast<const float *>(rowscale), Y, static_cast<int>(M), static_cast<int>(N),
+                                     nt, static_cast<int>(ntn), static_cast<int>(tiles_full), nsplit);
         }
     }
     // the scratch returns to the pool once the work queued on the stream is done

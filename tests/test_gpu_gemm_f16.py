@@ -52,6 +52,9 @@ def test_gemm_f16_symmetric(M, N, K):
     (100, 20600, 1024, False),  # 112-row token tiles: two issuers, 161 tiles
     (40, 20000, 256, False),    # 48-row token tiles: four issuers, one packed-code stage a tile
     (600, 20100, 384, False),   # K % 256 == 128: a half packed-code stage ends every tile
+    (256, 20096, 2048, False),  # 157 tiles: the 5 past the full wave split 4 ways along K
+    (300, 10000, 1024, False),  # 158 tiles, ragged M and N: the 6 past the full wave split 2 ways
+    (300, 10000, 1024, True),   # the same, symmetric
 ])
 def test_gemm_f16_many_tiles(M, N, K, sym):
     torch, w4 = cuda_or_skip()
