@@ -440,20 +440,57 @@ gemm_int4_f16_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_const
 }
 
 // The K-split tiles' outputs: Y[m0 + m, n0 + r] = RNE_bf16(rowscale[m0 + m]
-// x sum over the splits of part[x][y][m][r]), splits summed in order.  One
-// CTA per (tile x, token row m), one thread per weight row r.
-__global__ void __launch_bounds__(BR) f16_split_reduce_kernel(const float *__restrict__ part,
-                                                              const float *__restrict__ rowscale, uint16_t *Y, int M,
-                                                              int N, int nt, int ntn, int tile0, int nsplit) {
+// x sum over the splits of part[x][y][m][r]), splits summed in order from
+// zero.  One CTA per (tile x, 32 token rows); thread t takes weight rows
+// 4 (t mod 32) .. + 3 (one 16-byte load per split) of token rows
+// 8 k + t / 32, k = 0..3, so that many loads are in flight per thread (the
+// parts are in L2, just written).
+constexpr int RED_THREADS = 256;
+constexpr int RED_ROWS = 32;  // token rows per CTA
+__global__ void __launch_bounds__(RED_THREADS) f16_split_reduce_kernel(const float *__restrict__ part,
+                                                                       const float *__restrict__ rowscale,
+                                                                       uint16_t *Y, int M, int N, int nt, int ntn,
+                                                                       int tile0, int nsplit) {
     pdl_launch_dependents();
     pdl_wait();  // the partial sums and the row scales follow the stream order
-    const int x = blockIdx.x, m = blockIdx.y, r = threadIdx.x;
+    const int x = blockIdx.x;
     const int tile = tile0 + x;
     const int n0 = (tile % ntn) * BR, m0 = (tile / ntn) * nt;
-    if (m0 + m >= M || n0 + r >= N) return;
-    float acc = 0.0f;
-    for (int y = 0; y < nsplit; ++y) acc += part[((static_cast<int64_t>(x) * nsplit + y) * nt + m) * BR + r];
-    Y[static_cast<int64_t>(m0 + m) * N + n0 + r] = f32_to_bf16_bits(acc * rowscale[m0 + m]);
+    const int r = 4 * (threadIdx.x & 31);
+    const int64_t split_stride = static_cast<int64_t>(nt) * (BR / 4);  // float4 units
+    float4 acc[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    const float4 *base = reinterpret_cast<const float4 *>(part) + static_cast<int64_t>(x) * nsplit * split_stride;
+    int mk[4];
+    bool in[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        mk[k] = blockIdx.y * RED_ROWS + 8 * k + (threadIdx.x >> 5);
+        in[k] = mk[k] < nt && m0 + mk[k] < M;
+    }
+#pragma unroll 2
+    for (int y = 0; y < nsplit; ++y) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (!in[k]) continue;
+            const float4 v = base[y * split_stride + (static_cast<int64_t>(mk[k]) * BR + r) / 4];
+            acc[k].x += v.x;
+            acc[k].y += v.y;
+            acc[k].z += v.z;
+            acc[k].w += v.w;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        if (!in[k]) continue;
+        const float rs = rowscale[m0 + mk[k]];
+        uint16_t *dst = Y + static_cast<int64_t>(m0 + mk[k]) * N + n0 + r;
+        const float v[4] = {acc[k].x, acc[k].y, acc[k].z, acc[k].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (n0 + r + e < N) dst[e] = f32_to_bf16_bits(v[e] * rs);
+    }
 }
 
 // A memory pool per device for the pre-pass output (stream-ordered, kept
@@ -665,8 +702,8 @@ cudaError_t launch_gemm_int4_f16(const uint16_t *X, const uint8_t *qw, const uin
         if (err == cudaSuccess && tiles_split) {
             // the K-split tiles' outputs from their partial sums
             cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(static_cast<unsigned>(tiles_split), static_cast<unsigned>(nt));
-            cfg.blockDim = dim3(BR);
+            cfg.gridDim = dim3(static_cast<unsigned>(tiles_split), static_cast<unsigned>((nt + RED_ROWS - 1) / RED_ROWS));
+            cfg.blockDim = dim3(RED_THREADS);
             cfg.stream = st;
             cfg.attrs = pdl;
             cfg.numAttrs = 1;
