@@ -71,6 +71,7 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_ACC = 0;        // accumulators: n_iss x NT <= 256 columns
 constexpr uint32_t TM_A = 256;        // operand stages after them
 constexpr int PRE_THREADS = 256;
+constexpr int PRE_BLOCKS = 8;  // at most 8 blocks of 8 values of X per pre-pass thread: K <= 16384
 
 struct GemmF16Args {
     const uint16_t *s;
@@ -101,7 +102,11 @@ struct Barriers {
 
 // ---------------------------------------------------------------- pre-pass
 // One CTA per row of X: the row's largest |x| (BF16 magnitude bits order as
-// the values), then binary16 x * 2^(14 - e) in the permuted K order.
+// the values), then binary16 x * 2^(14 - e) in the permuted K order.  The
+// row is read once: each thread keeps its NB blocks of 8 values in registers
+// (K / 8 <= NB x PRE_THREADS), all loads in flight together; NB follows K so
+// that short rows keep few registers (and many CTAs per SM).
+template <int NB>
 __global__ void __launch_bounds__(PRE_THREADS) x16_prepass_kernel(const uint16_t *__restrict__ X, int K,
                                                                   uint16_t *__restrict__ Xh, float *rowscale) {
     const int m = blockIdx.x;
@@ -111,10 +116,16 @@ __global__ void __launch_bounds__(PRE_THREADS) x16_prepass_kernel(const uint16_t
     uint4 *xh = reinterpret_cast<uint4 *>(Xh + static_cast<int64_t>(m) * K);
     const int nb = K / 8;
     __shared__ uint32_t red[PRE_THREADS / 32];
+    uint4 xv[NB];
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+        const int b = threadIdx.x + j * PRE_THREADS;
+        xv[j] = b < nb ? x[b] : make_uint4(0u, 0u, 0u, 0u);
+    }
     uint32_t mx = 0;
-    for (int b = threadIdx.x; b < nb; b += PRE_THREADS) {
-        const uint4 v = x[b];
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+        const uint32_t w[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) mx = max(mx, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
     }
@@ -127,8 +138,11 @@ __global__ void __launch_bounds__(PRE_THREADS) x16_prepass_kernel(const uint16_t
     for (int w = 0; w < PRE_THREADS / 32; ++w) mx = max(mx, red[w]);
     const int e = exponent_of_absmax(mx);  // 2^e <= max|x| < 2^(e+1)
     const float inv = pow2f(14 - e);
-    for (int b = threadIdx.x; b < nb; b += PRE_THREADS) {
-        const uint4 v = x[b];
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+        const int b = threadIdx.x + j * PRE_THREADS;
+        if (b >= nb) break;
+        const uint4 v = xv[j];
         // values 0..7 of the block: v.x = {0, 1}, v.y = {2, 3}, v.z = {4, 5}, v.w = {6, 7}
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
         float f[8];
@@ -559,6 +573,7 @@ cudaError_t launch_gemm_int4_f16(const uint16_t *X, const uint8_t *qw, const uin
                                  const DeviceInfo &dev) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
+    if (K / 8 > static_cast<int64_t>(PRE_BLOCKS) * PRE_THREADS) return cudaErrorNotSupported;  // the pre-pass's reach
     const bool sym = z == nullptr;
     const F16Layout lay = f16_layout(M, K, sym);
     const int nt = lay.nt;
@@ -619,7 +634,10 @@ cudaError_t launch_gemm_int4_f16(const uint16_t *X, const uint8_t *qw, const uin
         cfg.stream = st;
         cfg.attrs = pdl;
         cfg.numAttrs = 1;
-        err = cudaLaunchKernelEx(&cfg, x16_prepass_kernel, X, static_cast<int>(K), xh, rowscale);
+        const int64_t per_thread = (K / 8 + PRE_THREADS - 1) / PRE_THREADS;
+        err = per_thread <= 2   ? cudaLaunchKernelEx(&cfg, x16_prepass_kernel<2>, X, static_cast<int>(K), xh, rowscale)
+              : per_thread <= 4 ? cudaLaunchKernelEx(&cfg, x16_prepass_kernel<4>, X, static_cast<int>(K), xh, rowscale)
+                                : cudaLaunchKernelEx(&cfg, x16_prepass_kernel<8>, X, static_cast<int>(K), xh, rowscale);
     }
 
     // 2. the GEMM

@@ -22,10 +22,13 @@ def _run(w4, torch, p, sym=False):
     return host_bits16(Y).reshape(p["M"], p["N"])
 
 
-# one token tile and several (256 rows each), ragged M and N, one group and the largest K
+# one token tile and several (256 rows each), ragged M and N, one group and the largest K;
+# K = 4096 / 4224 / 6144 / 16384: the pre-pass holding 2 (all used) / 3 of 4 / 3 of 4 / 8
+# blocks of 8 values per thread
 @pytest.mark.parametrize("M,N,K", [(1, 16, 128), (9, 113, 384), (16, 225, 640), (64, 1024, 3840),
                                    (128, 128, 128), (130, 256, 512), (257, 400, 384), (300, 129, 1920),
-                                   (513, 96, 768), (128, 16, 16384)])
+                                   (513, 96, 768), (128, 16, 16384), (40, 130, 4096), (70, 200, 4224),
+                                   (33, 300, 6144)])
 def test_gemm_f16_small_and_ragged(M, N, K):
     torch, w4 = cuda_or_skip()
     p = synth.int4_problem(N, K, M=M, seed=M * 5 + N + K)
