@@ -160,7 +160,30 @@ __global__ void __launch_bounds__(ROUTE_THREADS) moe_route_kernel(const int32_t 
 }
 
 // --------------------------------------------------------- 2. gathering
-// One CTA per (token, slot) pair p = m * topk + j.
+__device__ __forceinline__ uint32_t bf16x8_absmax_bits(const uint4 v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) m = max(m, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
+    return m;
+}
+// 8 BF16 values times inv (a power of two), each rounded to binary16, in order
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4 v, float inv) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __half2 h = __floats2half2_rn(bf16_bits_to_f32(w[i] & 0xFFFFu) * inv, bf16_bits_to_f32(w[i] >> 16) * inv);
+        o[i] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// One CTA per (token, slot) pair p = m * topk + j: the token's row, times
+// 2^(14 - e) for its largest |x| in [2^e, 2^(e+1)), into binary16 at the
+// pair's position.  NB > 0: the row is read once, each thread holding its NB
+// blocks of 8 values (K <= 8 NB GATHER_THREADS); NB = 0: any K, read twice.
+template <int NB>
 __global__ void __launch_bounds__(GATHER_THREADS) moe_gather_kernel(const uint16_t *__restrict__ X, int topk, int P,
                                                                     int E, int K, int64_t N, uint16_t *Y,
                                                                     unsigned char *scratch) {
@@ -174,11 +197,25 @@ __global__ void __launch_bounds__(GATHER_THREADS) moe_gather_kernel(const uint16
         for (int64_t n = threadIdx.x; n < N; n += blockDim.x) Y[p * N + n] = 0;
         return;
     }
-    const uint16_t *x = X + static_cast<int64_t>(p / topk) * K;
+    // K % 256 == 0: rows of whole 16-byte blocks, 16-byte aligned
+    const uint4 *x = reinterpret_cast<const uint4 *>(X + static_cast<int64_t>(p / topk) * K);
+    uint4 *xg = reinterpret_cast<uint4 *>(scratch + l.xg_off) + static_cast<int64_t>(pos) * (K / 8);
+    const int nb = K / 8;
     // largest |x| of the token (BF16 magnitude bit patterns order as values)
     __shared__ uint32_t red[GATHER_THREADS / 32];
     uint32_t m = 0;
-    for (int k = threadIdx.x; k < K; k += blockDim.x) m = max(m, static_cast<uint32_t>(x[k]) & 0x7FFFu);
+    uint4 xv[NB > 0 ? NB : 1];
+    if constexpr (NB > 0) {
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+            const int b = threadIdx.x + j * GATHER_THREADS;
+            xv[j] = b < nb ? x[b] : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int j = 0; j < NB; ++j) m = max(m, bf16x8_absmax_bits(xv[j]));
+    } else {
+        for (int b = threadIdx.x; b < nb; b += GATHER_THREADS) m = max(m, bf16x8_absmax_bits(x[b]));
+    }
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, d));
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
@@ -188,8 +225,16 @@ __global__ void __launch_bounds__(GATHER_THREADS) moe_gather_kernel(const uint16
     for (int w = 0; w < GATHER_THREADS / 32; ++w) m = max(m, red[w]);
     const int e = exponent_of_absmax(m);  // 2^e <= max|x| < 2^(e+1)
     const float inv = pow2f(14 - e);      // max|x| * inv in [2^14, 2^15): binary16 holds it
-    __half *xg = reinterpret_cast<__half *>(scratch + l.xg_off) + static_cast<int64_t>(pos) * K;
-    for (int k = threadIdx.x; k < K; k += blockDim.x) xg[k] = __float2half_rn(bf16_bits_to_f32(x[k]) * inv);
+    if constexpr (NB > 0) {
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+            const int b = threadIdx.x + j * GATHER_THREADS;
+            if (b >= nb) break;
+            xg[b] = bf16x8_to_f16x8(xv[j], inv);
+        }
+    } else {
+        for (int b = threadIdx.x; b < nb; b += GATHER_THREADS) xg[b] = bf16x8_to_f16x8(x[b], inv);
+    }
     if (threadIdx.x == 0) reinterpret_cast<float *>(scratch + l.scale_off)[pos] = pow2f(e - 14);
 }
 
@@ -556,16 +601,25 @@ cudaError_t launch_moe_fp4_gemm(const uint16_t *X, const uint8_t *qw, const uint
         const int smem = static_cast<int>(3 * E * sizeof(int));
         static SmemLimit limit;
         if (cudaError_t e = limit.ensure(reinterpret_cast<const void *>(moe_route_kernel), dev.device, smem)) return e;
-        moe_route_kernel<<<1, ROUTE_THREADS, smem, st>>>(ids, P, static_cast<int>(E), scr, status);
-        if (cudaError_t e = cudaGetLastError()) return e;
     }
-    // 2. gathering
-    // the gather and the GEMM are launched with programmatic stream
-    // serialisation: each may start while the previous launch finishes and
-    // waits for it (griddepcontrol.wait) before reading what it wrote
+    // the three launches go with programmatic stream serialisation: each may
+    // start while the previous launch of the stream finishes and waits for it
+    // (griddepcontrol.wait) before touching global memory
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1);
+        cfg.blockDim = dim3(ROUTE_THREADS);
+        cfg.dynamicSmemBytes = static_cast<size_t>(3 * E * sizeof(int));
+        cfg.stream = st;
+        cfg.attrs = pdl;
+        cfg.numAttrs = 1;
+        if (cudaError_t e = cudaLaunchKernelEx(&cfg, moe_route_kernel, ids, P, static_cast<int>(E), scr, status))
+            return e;
+    }
+    // 2. gathering
     {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(static_cast<unsigned>(P));
@@ -573,8 +627,12 @@ cudaError_t launch_moe_fp4_gemm(const uint16_t *X, const uint8_t *qw, const uint
         cfg.stream = st;
         cfg.attrs = pdl;
         cfg.numAttrs = 1;
-        if (cudaError_t e = cudaLaunchKernelEx(&cfg, moe_gather_kernel, X, topk, P, static_cast<int>(E),
-                                               static_cast<int>(K), N, Y, scr))
+        const int per_thread = static_cast<int>((K / 8 + GATHER_THREADS - 1) / GATHER_THREADS);
+        auto gk = per_thread <= 2 ? moe_gather_kernel<2>
+                  : per_thread <= 4 ? moe_gather_kernel<4>
+                  : per_thread <= 8 ? moe_gather_kernel<8>
+                                    : moe_gather_kernel<0>;
+        if (cudaError_t e = cudaLaunchKernelEx(&cfg, gk, X, topk, P, static_cast<int>(E), static_cast<int>(K), N, Y, scr))
             return e;
     }
     // 3. the GEMM

@@ -29,7 +29,8 @@ def _ref(m, ids=None):
     (8, 300, 1024, 16, 8),      # every expert, ragged N over three blocks
     (2, 200, 512, 150, 2),      # 150 rows per expert: tiles of 128 and 22 rows
     (16, 1000, 7168, 40, 6),    # the expert FC's K
-    (3, 130, 16384, 5, 3),      # long K
+    (3, 130, 16384, 5, 3),      # long K (the gather's threads hold 8 blocks of 8 values each)
+    (2, 40, 16640, 3, 2),       # longer: the gather reads the row twice
     (5, 200, 768, 9, 3),        # K % 512 == 256: a half last weight stage in every item
     (8, 256, 1280, 20, 4),      # the same after two full stages, several items per CTA
 ])
