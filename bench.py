@@ -747,15 +747,17 @@ def run_ours(args):
     e2e_steps = min(args.steps, 300)
 
     def e2e_body(i):
-        x_d.copy_(x_pin, non_blocking=True)
+        w4.w4a16_copy(x_d, x_pin)
         step(i, xu_d, xd_d)
-        y_pin.copy_(y_all, non_blocking=True)
+        w4.w4a16_copy(y_pin, y_all)
 
-    # As a decode loop runs it: the step -- pinned host -> device copies of
-    # the activations, the two library calls, device -> host copies of the
-    # outputs -- captured once per weight set into a CUDA graph, replayed
-    # once per step, and the host waits for each step's result.  The graph
-    # copies read and write the host buffers at every replay.
+    # As a decode loop runs it: the step -- the activations copied in from
+    # pinned host memory, the two library calls, the outputs copied out to
+    # pinned host memory, the copies by the library's copy kernel (reading
+    # and writing the mapped host buffers) so that all four launches chain
+    # by programmatic dependent launch -- captured once per weight set into a
+    # CUDA graph, replayed once per step, and the host waits for each step's
+    # result.  The copies read and write the host buffers at every replay.
     e2e_graphs = None
     if not args.no_graph:
         try:
@@ -789,7 +791,8 @@ def run_ours(args):
     e2e = {"value": round(STEP_BYTES * e2e_steps * world / e2e_dt / 1e9, 2), "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
            "sync_per_step": True,
-           "launch": ("one CUDA graph per step (one pinned H2D copy, the two library calls, one D2H copy)"
+           "launch": ("one CUDA graph per step (w4a16_copy of the pinned activations in, the two library "
+                      "calls, w4a16_copy of the outputs out to pinned memory)"
                       if e2e_graphs is not None else "eager (copies and library calls per step)")}
 
     extra = {}

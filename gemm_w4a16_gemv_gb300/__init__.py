@@ -59,6 +59,7 @@ SIGNATURES = {
     "w4a16_gemm": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _INT, _P], _INT),
     "w4a16_gemm_f16": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _INT, _P], _INT),
     "w4a16_bf16_gemm": ([_P, _P, _P, _I64, _I64, _I64, _P], _INT),
+    "w4a16_copy": ([_P, _P, _I64, _P], _INT),
     "fp4_moe_gemv": ([_P, _P, _P, _P, _INT, _P, _I64, _I64, _I64, _INT, _P], _INT),
     "fp4_moe_gemm": ([_P, _P, _P, _P, _INT, _INT, _P, _I64, _I64, _I64, _INT, _P, _I64, _P], _INT),
     "fp4_moe_gemm_scratch_bytes": ([_INT, _INT, _I64, _I64], _I64),
@@ -412,6 +413,30 @@ def w4a16_graph_launch(graph: W4A16Graph, stream=None) -> None:
 
 def w4a16_graph_destroy(graph: W4A16Graph) -> None:
     graph.destroy()
+
+
+def w4a16_copy(dst: torch.Tensor, src: torch.Tensor, stream=None, device=None) -> torch.Tensor:
+    """dst <- src (the same number of bytes, both contiguous) by one kernel on
+    `device` (the CUDA tensor's device; `device` when both are host
+    tensors): a CUDA tensor or a pinned host tensor on either side."""
+    for name, t in (("dst", dst), ("src", src)):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError("%s must be a torch.Tensor" % name)
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % name)
+        if not t.is_cuda and t.numel() > 0 and not t.is_pinned():
+            raise ValueError("%s: a host tensor must be pinned" % name)
+    nbytes = dst.numel() * dst.element_size()
+    if src.numel() * src.element_size() != nbytes:
+        raise ValueError("dst has %d bytes, src %d" % (nbytes, src.numel() * src.element_size()))
+    devs = {t.device for t in (dst, src) if t.is_cuda}
+    if len(devs) > 1:
+        raise ValueError("dst and src are on different devices")
+    dev = devs.pop() if devs else torch.device(device if device is not None else "cuda")
+    with torch.cuda.device(dev):  # the library launches on the current device
+        _check(lib().w4a16_copy(ctypes.c_void_p(dst.data_ptr()), ctypes.c_void_p(src.data_ptr()), nbytes,
+                                _stream(stream, dev)))
+    return dst
 
 
 def w4a16_check_device_error(stream=None) -> int:

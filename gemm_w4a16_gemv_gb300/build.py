@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "libw4a16.so")
 SOURCES = ["api.cu", "dequant.cu", "gemv_int4.cu", "gemv_chain.cu", "moe_fp4.cu", "moe_fp4_gemm.cu",
-           "gemm_int4_tc.cu", "gemm_int4_f16.cu", "gemm_bf16_tc.cu"]
+           "gemm_int4_tc.cu", "gemm_int4_f16.cu", "gemm_bf16_tc.cu", "copy.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",

@@ -376,6 +376,32 @@ cudaError_t launch_chain(w4::ChainOp *plan, int count, unsigned int *scratch, cu
     return cudaSuccess;
 }
 
+// The address through which the current device reaches p: p itself for
+// memory of this device (or managed memory), the mapped device address for
+// pinned host memory; nullptr (with the message set) for anything else.
+void *device_address(const char *who, const char *name, const void *p, int device) {
+    cudaPointerAttributes at;
+    const cudaError_t e = cudaPointerGetAttributes(&at, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        fail(W4A16_ERR_INVALID_ARG, "%s: %s is not CUDA memory (%s)", who, name, cudaGetErrorString(e));
+        return nullptr;
+    }
+    if (at.type == cudaMemoryTypeManaged) return const_cast<void *>(p);
+    if (at.type == cudaMemoryTypeDevice) {
+        if (at.device != device) {
+            fail(W4A16_ERR_INVALID_ARG, "%s: %s is memory of device %d, the current device is %d", who, name,
+                 at.device, device);
+            return nullptr;
+        }
+        return const_cast<void *>(p);
+    }
+    if (at.type == cudaMemoryTypeHost && at.devicePointer) return at.devicePointer;
+    fail(W4A16_ERR_INVALID_ARG, "%s: %s is host memory the device cannot reach (pageable, or pinned unmapped)", who,
+         name);
+    return nullptr;
+}
+
 }  // namespace
 
 extern "C" {
@@ -418,6 +444,21 @@ int w4a16_gemm_f16(const uint16_t *X, const uint8_t *qw, const uint16_t *s, cons
     if (int r = check_device_ptrs(fn, dev.device, {X, qw, s, z, Y})) return r;
     return launched(w4::launch_gemm_int4_f16(X, qw, s, z, Y, M, N, K, static_cast<cudaStream_t>(stream), status, dev),
                     fn);
+}
+
+int w4a16_copy(void *dst, const void *src, int64_t bytes, void *stream) {
+    const char *fn = "w4a16_copy";
+    if (bytes < 0) return fail(W4A16_ERR_INVALID_ARG, "%s: bytes=%lld < 0", fn, (long long)bytes);
+    if (bytes == 0) return ok();  // nothing to copy (an empty buffer's pointer may be null)
+    if (!dst || !src) return fail(W4A16_ERR_INVALID_ARG, "%s: null pointer", fn);
+    w4::DeviceInfo dev;
+    unsigned int *status;
+    if (int r = device_state(dev, status)) return r;
+    void *d = device_address(fn, "dst", dst, dev.device);
+    if (!d) return W4A16_ERR_INVALID_ARG;
+    void *sp = device_address(fn, "src", src, dev.device);
+    if (!sp) return W4A16_ERR_INVALID_ARG;
+    return launched(w4::launch_copy(d, sp, bytes, static_cast<cudaStream_t>(stream), dev), fn);
 }
 
 int w4a16_bf16_gemm(const uint16_t *X, const uint16_t *W, uint16_t *Y, int64_t M, int64_t N, int64_t K,

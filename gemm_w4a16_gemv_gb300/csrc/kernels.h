@@ -113,4 +113,8 @@ cudaError_t launch_bf16_gemm(const uint16_t *X, const uint16_t *W, uint16_t *Y,
                              int64_t M, int64_t N, int64_t K, cudaStream_t st,
                              unsigned int *status, const DeviceInfo &dev);
 
+// dst[0, bytes) = src[0, bytes) by a kernel (addresses the device can
+// dereference, already translated and checked by the caller).
+cudaError_t launch_copy(void *dst, const void *src, int64_t bytes, cudaStream_t st, const DeviceInfo &dev);
+
 }  // namespace w4

@@ -26,7 +26,8 @@
  *  - kernels run on the CURRENT device (cudaSetDevice) and every data
  *    pointer must be memory of that device (device memory of it, or managed
  *    memory): a pointer to another device's memory or to host memory is
- *    refused with W4A16_ERR_INVALID_ARG before anything is launched;
+ *    refused with W4A16_ERR_INVALID_ARG before anything is launched (the
+ *    one exception: w4a16_copy also takes pinned, mapped host memory);
  *  - every data pointer must be 16-byte aligned (else W4A16_ERR_MISALIGNED);
  *  - an output must not overlap any input of the same call (CTAs write
  *    their outputs while others may still read the inputs); this is not
@@ -141,6 +142,27 @@ int w4a16_gemm_f16(const uint16_t *X, const uint8_t *qw, const uint16_t *s,
  */
 int w4a16_bf16_gemm(const uint16_t *X, const uint16_t *W, uint16_t *Y,
                     int64_t M, int64_t N, int64_t K, void *stream);
+
+/*
+ * Copy `bytes` bytes from src to dst with one kernel on `stream`, launched
+ * with programmatic dependent launch: the small transfers of a decode step
+ * ("Lab 5: Gemma4 end-to-end inference optimisation", section "CUDA Graph":
+ * the step's launches captured and replayed as one graph) -- the token's
+ * activation in, the step's result out -- then chain with the library's
+ * kernels instead of being copy-engine operations between them.
+ *   dst, src : memory of the current device, managed memory, or PINNED host
+ *              memory mapped into the device's address space (cudaHostAlloc
+ *              or cudaHostRegister with mapping, which unified addressing
+ *              gives by default); this is the one entry point that takes
+ *              host pointers.  Any alignment (16-byte moves when both are
+ *              16-byte aligned); the ranges must not overlap.
+ *   bytes    : >= 0 (0 launches nothing and accepts null pointers).
+ * Pageable host memory, pinned host memory without a device mapping and
+ * another device's memory are refused with W4A16_ERR_INVALID_ARG before
+ * anything is launched.  The host may read a pinned destination once the
+ * stream has been synchronised.
+ */
+int w4a16_copy(void *dst, const void *src, int64_t bytes, void *stream);
 
 /*
  * Batched-expert FP4 GEMV for one token ("DeepSeek V4 Triton FP4

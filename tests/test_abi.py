@@ -203,3 +203,22 @@ def test_chain_noalloc_host_validation(libw4):
     assert "4032" in _call(libw4, "w4a16_last_error_string").decode()
     ops[3].K = 320
     assert _call(libw4, "w4a16_linear_chain_noalloc", ops, 8, 128, None) == 1     # the GEMV's checks
+
+
+def test_copy_host_validation(libw4):
+    # null pointers and a negative size fail before any CUDA call
+    A = 1 << 20
+    assert _call(libw4, "w4a16_copy", None, A, 16, None) == 1
+    assert _call(libw4, "w4a16_copy", A, None, 16, None) == 1
+    assert _call(libw4, "w4a16_copy", A, A + 64, -1, None) == 1
+    assert "bytes" in _call(libw4, "w4a16_last_error_string").decode()
+    assert _call(libw4, "w4a16_copy", None, None, 0, None) == 0   # empty: nothing to launch
+
+
+def test_copy_binding_refuses_pageable_host_tensors():
+    # the binding refuses a host tensor that is not pinned before calling the library
+    import torch
+    import gemm_w4a16_gemv_gb300 as w4
+    a, b = torch.zeros(8), torch.zeros(8)
+    with pytest.raises(ValueError, match="pinned"):
+        w4.w4a16_copy(a, b)
