@@ -571,13 +571,14 @@ def per_config(torch, w4, synth, dev, stream, hbm_peak, tf_peak):
             tf = 2.0 * M * N * K / t / 1e12
             out[name] = {"us": round(t * 1e6, 2), "TFLOP/s": round(tf, 1), "frac_bf16": round(tf / tf_peak, 3),
                          "weight_sets": ns, "each": spread(torch, fn, 50, stream)}
-            # the binary16-operand variant (w4a16_gemm_f16: pre-pass + GEMM, two launches)
+            # the binary16-operand variant (w4a16_gemm_f16: pre-pass + GEMM, and at
+            # M = 2048 the reduction of the K-split tiles past the last full wave)
             fn16 = lambda i: w4.w4a16_gemm_f16(X, sets[i % ns]["qw"], sets[i % ns]["s"], sets[i % ns]["z"], Y)
             t16 = time_launches(torch, fn16, 20, stream)
             tf16 = 2.0 * M * N * K / t16 / 1e12
             out["gemm_f16_m%d_15360x3840" % M] = {"us": round(t16 * 1e6, 2), "TFLOP/s": round(tf16, 1),
                                                   "frac_bf16": round(tf16 / tf_peak, 3), "weight_sets": ns,
-                                                  "launches_per_call": 2}
+                                                  "launches_per_call": 3 if M >= 2048 else 2}
             del sets
         except Exception as e:  # the tensor-core GEMM may be unavailable on this device
             out[name] = {"unavailable": str(e).splitlines()[0][:120]}
