@@ -103,6 +103,35 @@ __host__ __device__ inline MoeScratch moe_scratch_layout(int64_t P, int64_t E, i
 }
 
 // ------------------------------------------------------------ 1. routing
+// Exclusive prefix sum of one value per thread over the routing CTA; `total`
+// receives the sum of all of them.  ws: ROUTE_THREADS / 32 ints of shared
+// memory (free again when it returns).
+__device__ __forceinline__ int route_exclusive_sum(int v, int *ws, int &total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int x = v;  // inclusive within the warp
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, d);
+        if (lane >= d) x += y;
+    }
+    if (lane == 31) ws[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        int t = ws[lane];  // ROUTE_THREADS / 32 == 32 warp sums
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, t, d);
+            if (lane >= d) t += y;
+        }
+        ws[lane] = t;  // inclusive over the warps
+    }
+    __syncthreads();
+    const int before = w > 0 ? ws[w - 1] : 0;
+    total = ws[ROUTE_THREADS / 32 - 1];
+    __syncthreads();
+    return before + x - v;
+}
+
 // One CTA.  cnt[e]: pairs of expert e; off[e]: first position of its rows.
 __global__ void __launch_bounds__(ROUTE_THREADS) moe_route_kernel(const int32_t *__restrict__ ids, int P, int E,
                                                                   unsigned char *scratch, unsigned int *status) {
@@ -125,27 +154,43 @@ __global__ void __launch_bounds__(ROUTE_THREADS) moe_route_kernel(const int32_t 
         else bad = true;
     }
     if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(status, kDevBadExpert);
-    if (threadIdx.x == 0) {
-        // exclusive prefix sum and the tile table, experts in order; the
-        // tile count and the largest tile's rows go to the scratch header
-        int acc = 0, t = 0, maxrows = 0;
-        for (int e = 0; e < E; ++e) {
-            off[e] = acc;
-            for (int r = 0; r < cnt[e]; r += BT) {
+    // The tile table, experts in order: block-wide exclusive prefix sums of
+    // the experts' row counts (off[e]) and tile counts (its first tile), one
+    // expert per thread in chunks of the CTA's width, each thread writing its
+    // expert's tiles (rows in tiles of BT); the tile count and the largest
+    // tile's rows go to the scratch header.
+    __shared__ int ws[ROUTE_THREADS / 32];
+    __shared__ int max_rows;
+    if (threadIdx.x == 0) max_rows = 0;
+    int row_carry = 0, tile_carry = 0, my_max = 0;
+    for (int e0 = 0; e0 < E; e0 += ROUTE_THREADS) {  // uniform over the CTA
+        const int e = e0 + static_cast<int>(threadIdx.x);
+        const int c = e < E ? cnt[e] : 0;
+        const int ntl = (c + BT - 1) / BT;
+        int rows_total, tiles_total;
+        const int roff = row_carry + route_exclusive_sum(c, ws, rows_total);
+        const int toff = tile_carry + route_exclusive_sum(ntl, ws, tiles_total);
+        if (e < E) {
+            off[e] = roff;
+            for (int j = 0; j < ntl; ++j) {
                 MoeTile tl;
                 tl.expert = e;
-                tl.row0 = acc + r;
-                tl.rows = cnt[e] - r < BT ? cnt[e] - r : BT;
+                tl.row0 = roff + j * BT;
+                tl.rows = c - j * BT < BT ? c - j * BT : BT;
                 tl.pad = 0;
-                tiles[t++] = tl;
-                maxrows = tl.rows > maxrows ? tl.rows : maxrows;
+                tiles[toff + j] = tl;
             }
-            acc += cnt[e];
+            my_max = max(my_max, c < BT ? c : BT);
         }
-        reinterpret_cast<int *>(scratch)[0] = t;
-        reinterpret_cast<int *>(scratch)[1] = maxrows;
+        row_carry += rows_total;
+        tile_carry += tiles_total;
     }
+    atomicMax(&max_rows, my_max);
     __syncthreads();
+    if (threadIdx.x == 0) {
+        reinterpret_cast<int *>(scratch)[0] = tile_carry;
+        reinterpret_cast<int *>(scratch)[1] = max_rows;
+    }
     // positions: within an expert in arrival order (each output row is
     // computed on its own, so the order does not change any result)
     for (int p = threadIdx.x; p < P; p += blockDim.x) {

@@ -33,6 +33,7 @@ def _ref(m, ids=None):
     (2, 40, 16640, 3, 2),       # longer: the gather reads the row twice
     (5, 200, 768, 9, 3),        # K % 512 == 256: a half last weight stage in every item
     (8, 256, 1280, 20, 4),      # the same after two full stages, several items per CTA
+    (1500, 8, 256, 40, 4),      # more experts than the routing CTA's threads: its scans run in two chunks
 ])
 def test_moe_gemm_small_and_ragged(E, N, K, M, topk):
     torch, w4 = cuda_or_skip()
