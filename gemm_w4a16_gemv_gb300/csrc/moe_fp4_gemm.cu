@@ -236,19 +236,11 @@ __global__ void __launch_bounds__(GATHER_THREADS) moe_gather_kernel(const uint16
     const int p = blockIdx.x;
     pdl_launch_dependents();  // the GEMM's CTAs may start; they wait for this grid before reading
     pdl_wait();               // the routing (and X) follow the stream order
-    const int pos = reinterpret_cast<const int *>(scratch + l.posof_off)[p];
-    if (pos < 0) {
-        // an expert id out of range: its output row is zeros
-        for (int64_t n = threadIdx.x; n < N; n += blockDim.x) Y[p * N + n] = 0;
-        return;
-    }
-    // K % 256 == 0: rows of whole 16-byte blocks, 16-byte aligned
+    // K % 256 == 0: rows of whole 16-byte blocks, 16-byte aligned.  The
+    // token's row is requested before the pair's position (which only says
+    // where the row goes), so that the two loads' latencies overlap.
     const uint4 *x = reinterpret_cast<const uint4 *>(X + static_cast<int64_t>(p / topk) * K);
-    uint4 *xg = reinterpret_cast<uint4 *>(scratch + l.xg_off) + static_cast<int64_t>(pos) * (K / 8);
     const int nb = K / 8;
-    // largest |x| of the token (BF16 magnitude bit patterns order as values)
-    __shared__ uint32_t red[GATHER_THREADS / 32];
-    uint32_t m = 0;
     uint4 xv[NB > 0 ? NB : 1];
     if constexpr (NB > 0) {
 #pragma unroll
@@ -256,6 +248,18 @@ __global__ void __launch_bounds__(GATHER_THREADS) moe_gather_kernel(const uint16
             const int b = threadIdx.x + j * GATHER_THREADS;
             xv[j] = b < nb ? x[b] : make_uint4(0u, 0u, 0u, 0u);
         }
+    }
+    const int pos = reinterpret_cast<const int *>(scratch + l.posof_off)[p];  // uniform over the CTA
+    if (pos < 0) {
+        // an expert id out of range: its output row is zeros
+        for (int64_t n = threadIdx.x; n < N; n += blockDim.x) Y[p * N + n] = 0;
+        return;
+    }
+    uint4 *xg = reinterpret_cast<uint4 *>(scratch + l.xg_off) + static_cast<int64_t>(pos) * (K / 8);
+    // largest |x| of the token (BF16 magnitude bit patterns order as values)
+    __shared__ uint32_t red[GATHER_THREADS / 32];
+    uint32_t m = 0;
+    if constexpr (NB > 0) {
 #pragma unroll
         for (int j = 0; j < NB; ++j) m = max(m, bf16x8_absmax_bits(xv[j]));
     } else {
